@@ -1,0 +1,182 @@
+"""fp64 CPU oracle for paged decode attention -- TEST INFRASTRUCTURE ONLY.
+
+Only the test suite, ``__graft_entry__.smoke()`` and the benchmark's CPU
+baseline leg may import this package.  The product path (the CUDA library and
+its Python binding) never touches it and shares no code with it.
+
+The arithmetic lives in ``paged_ref.c`` (plain loops in double); this module
+builds it with gcc and wraps it with ctypes and numpy.  Every function states
+which passage of the PhotonInfer README it restates; see the C file's header
+for the formula and the layouts.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Optional, Tuple
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "paged_ref.c")
+_LIB_PATH = os.path.join(_HERE, "libphoton_oracle.so")
+_lib = None
+
+ERRORS = {0: "ok", -1: "bad argument", -2: "slot out of range", -3: "duplicate slot",
+          -4: "block id out of range", -5: "context length out of range"}
+
+
+class OracleError(RuntimeError):
+    pass
+
+
+def build(force: bool = False) -> str:
+    """Compile paged_ref.c into libphoton_oracle.so (plain -O2, no SIMD flags)."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", "-pthread", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    lib = ctypes.CDLL(build())
+    P, i32, i64, f64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_double
+    lib.ref_cache_write.argtypes = [P, P, P, i32, P, P, i32, i32, i32, i32, i32]
+    lib.ref_gather.argtypes = [P, P, P, P, P, P, i32, i32, i32, i32, i32, i32, i32]
+    lib.ref_paged_decode.argtypes = [P, P, P, P, P, f64, P] + [i32] * 9
+    lib.ref_paged_decode_row.argtypes = [P, P, P, P, P, f64, i32, i32, P] + [i32] * 8
+    lib.ref_attend_range.argtypes = [P, P, P, P, P, f64, i32, i32, i64, i64, P, P, P] + [i32] * 8
+    lib.ref_merge.argtypes = [i32, P, P, P, i32, P]
+    lib.ref_merge.restype = None
+    lib.ref_widen.argtypes = [P, ctypes.c_size_t, i32, P]
+    lib.ref_widen.restype = None
+    for fn in (lib.ref_cache_write, lib.ref_gather, lib.ref_paged_decode,
+               lib.ref_paged_decode_row, lib.ref_attend_range):
+        fn.restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def _ptr(a: np.ndarray) -> int:
+    assert a.flags["C_CONTIGUOUS"], "oracle inputs must be C-contiguous"
+    return a.ctypes.data
+
+
+def _check(rc: int) -> None:
+    if rc != 0:
+        raise OracleError(ERRORS.get(rc, f"error {rc}"))
+
+
+def _dtype_code(a: np.ndarray, dtype: Optional[int]) -> int:
+    if dtype is not None:
+        return dtype
+    if a.dtype == np.float32:
+        return 0
+    if a.dtype == np.float16:
+        return 1
+    raise ValueError("pass dtype explicitly for raw 16-bit storage (bf16)")
+
+
+def cache_write(k_new, v_new, slot_mapping, k_cache, v_cache, *, block_size: int,
+                dtype: Optional[int] = None) -> None:
+    """Batched cache write (README "Technical details: paged attention", the
+    single kernel for multi-sequence K/V writes): bit-copies row t to slot_t,
+    in place on the numpy pools."""
+    lib = _load()
+    T = int(slot_mapping.shape[0])
+    NB, Hkv, bs, d = k_cache.shape
+    assert bs == block_size
+    sm = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    _check(lib.ref_cache_write(_ptr(k_new), _ptr(v_new), _ptr(sm), T, _ptr(k_cache),
+                               _ptr(v_cache), Hkv, d, bs, NB, _dtype_code(k_cache, dtype)))
+
+
+def gather(k_cache, v_cache, block_tables, context_lens, *, dtype: Optional[int] = None
+           ) -> Tuple[np.ndarray, np.ndarray]:
+    """Block-table gather (README "Technical details: paged attention",
+    per-sequence cache offsets): dense [B][Hkv][MBS*bs][d], zero past ctx."""
+    lib = _load()
+    NB, Hkv, bs, d = k_cache.shape
+    B, MBS = block_tables.shape
+    kd = np.empty((B, Hkv, MBS * bs, d), dtype=k_cache.dtype)
+    vd = np.empty_like(kd)
+    _check(lib.ref_gather(_ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
+                          _ptr(kd), _ptr(vd), B, Hkv, d, bs, NB, MBS,
+                          _dtype_code(k_cache, dtype)))
+    return kd, vd
+
+
+def paged_decode(q, k_cache, v_cache, block_tables, context_lens, scale: float, *,
+                 dtype: Optional[int] = None, num_threads: int = 1) -> np.ndarray:
+    """Batched paged decode attention in fp64 (README "Key features: GPU
+    kernels", batched paged attention with numerically stable softmax).
+    Returns float64 [B][Hq][d]."""
+    lib = _load()
+    B, Hq, d = q.shape
+    NB, Hkv, bs, _ = k_cache.shape
+    MBS = block_tables.shape[1]
+    out = np.empty((B, Hq, d), dtype=np.float64)
+    _check(lib.ref_paged_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                _ptr(context_lens), float(scale), _ptr(out), B, Hq, Hkv, d, bs,
+                                NB, MBS, _dtype_code(q, dtype), int(num_threads)))
+    return out
+
+
+def paged_decode_row(q, k_cache, v_cache, block_tables, context_lens, scale: float, b: int,
+                     h: int, *, dtype: Optional[int] = None) -> np.ndarray:
+    """One (sequence, q head) output row of paged_decode, float64 [d]."""
+    lib = _load()
+    B, Hq, d = q.shape
+    NB, Hkv, bs, _ = k_cache.shape
+    MBS = block_tables.shape[1]
+    out = np.empty(d, dtype=np.float64)
+    _check(lib.ref_paged_decode_row(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                    _ptr(context_lens), float(scale), int(b), int(h), _ptr(out),
+                                    B, Hq, Hkv, d, bs, NB, MBS, _dtype_code(q, dtype)))
+    return out
+
+
+def attend_range(q, k_cache, v_cache, block_tables, context_lens, scale: float, b: int, h: int,
+                 j0: int, j1: int, *, dtype: Optional[int] = None):
+    """Partial (m, l, unnormalised o) over logical positions [j0, j1)."""
+    lib = _load()
+    B, Hq, d = q.shape
+    NB, Hkv, bs, _ = k_cache.shape
+    MBS = block_tables.shape[1]
+    m = np.zeros(1, np.float64)
+    l = np.zeros(1, np.float64)
+    o = np.zeros(d, np.float64)
+    _check(lib.ref_attend_range(_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                _ptr(context_lens), float(scale), int(b), int(h), int(j0),
+                                int(j1), _ptr(m), _ptr(l), _ptr(o), B, Hq, Hkv, d, bs, NB, MBS,
+                                _dtype_code(q, dtype)))
+    return float(m[0]), float(l[0]), o
+
+
+def merge(m, l, o) -> np.ndarray:
+    """Partition merge by log-sum-exp weights (the split-KV combination step)."""
+    lib = _load()
+    m = np.ascontiguousarray(m, np.float64)
+    l = np.ascontiguousarray(l, np.float64)
+    o = np.ascontiguousarray(o, np.float64)
+    P, d = o.shape
+    out = np.empty(d, np.float64)
+    lib.ref_merge(P, _ptr(m), _ptr(l), _ptr(o), d, _ptr(out))
+    return out
+
+
+def widen(a: np.ndarray, dtype: Optional[int] = None) -> np.ndarray:
+    """Exact widening of stored fp32/fp16/bf16 elements to float64."""
+    lib = _load()
+    a = np.ascontiguousarray(a)
+    out = np.empty(a.shape, np.float64)
+    lib.ref_widen(_ptr(a), a.size, _dtype_code(a, dtype), _ptr(out))
+    return out

@@ -1,0 +1,414 @@
+"""Pins for the fp64 CPU oracle, checked against things other than itself.
+
+Each test ties the oracle to mathematics the PhotonInfer README's paged
+attention implies ("Key features: GPU-optimized kernels" -- batched paged
+attention, numerically stable softmax; "Technical details: paged attention" --
+block-wise KV cache, per-sequence offsets, batched cache write):
+
+* a dense, unpaged attention computed with torch on CPU in float64 (a library
+  softmax on a layout the test builds itself);
+* closed-form golden fixtures (tests/golden/*.json);
+* invariants: physical block permutation, one-token context, uniform scores,
+  score shift, split/merge by log-sum-exp, threads;
+* brute force for the byte moves (cache write, gather).
+
+No GPU is needed.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# --------------------------------------------------------------- test-side helpers
+def _to_f64(a: np.ndarray, dtype: int) -> np.ndarray:
+    """Widen stored values with numpy only (independent of the oracle's decoder)."""
+    if dtype == W.DTYPE_BF16:
+        return (a.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+    return a.astype(np.float64)
+
+
+def _draw(rng, shape, dtype):
+    x = rng.standard_normal(shape).astype(np.float32)
+    if dtype == W.DTYPE_F32:
+        return x
+    if dtype == W.DTYPE_F16:
+        return x.astype(np.float16)
+    b = x.view(np.uint32)
+    return ((b + np.uint32(0x7FFF) + ((b >> 16) & 1)) >> 16).astype(np.uint16)
+
+
+def _page(dense_k, dense_v, ctx, bs, rng, spare=3, mbs=None, poison=True):
+    """Scatter per-sequence dense K/V [B][Hkv][S][d] into a shuffled paged pool.
+
+    Written independently of the oracle: a fresh random permutation hands out
+    physical blocks; everything not owned is NaN (or zero if poison=False)."""
+    B, Hkv, S, d = dense_k.shape
+    nblk = [(int(c) + bs - 1) // bs for c in ctx]
+    NB = sum(nblk) + spare
+    mbs = mbs or max(1, max(nblk))
+    perm = rng.permutation(NB)
+    tables = np.full((B, mbs), -1, np.int32)
+    fill = np.nan if poison else 0.0
+    kc = np.full((NB, Hkv, bs, d), fill, dtype=dense_k.dtype) if dense_k.dtype != np.uint16 else \
+        np.full((NB, Hkv, bs, d), 0x7FC0 if poison else 0, np.uint16)
+    vc = kc.copy()
+    pos = 0
+    for b in range(B):
+        for i in range(nblk[b]):
+            blk = int(perm[pos]); pos += 1
+            tables[b, i] = blk
+            for off in range(bs):
+                j = i * bs + off
+                if j < ctx[b]:
+                    kc[blk, :, off, :] = dense_k[b, :, j, :]
+                    vc[blk, :, off, :] = dense_v[b, :, j, :]
+    return kc, vc, tables
+
+
+def _torch_dense_attention(q64, k64, v64, ctx, scale, G):
+    """softmax(q K^T * scale) V with torch float64 on CPU; GQA by repeat_interleave."""
+    B, Hq, d = q64.shape
+    out = np.zeros((B, Hq, d))
+    for b in range(B):
+        c = int(ctx[b])
+        if c == 0:
+            continue
+        K = torch.from_numpy(k64[b, :, :c, :]).repeat_interleave(G, dim=0)   # [Hq][c][d]
+        V = torch.from_numpy(v64[b, :, :c, :]).repeat_interleave(G, dim=0)
+        q = torch.from_numpy(q64[b]).unsqueeze(1)                          # [Hq][1][d]
+        att = torch.softmax(torch.matmul(q, K.transpose(1, 2)) * scale, dim=-1)
+        out[b] = torch.matmul(att, V).squeeze(1).numpy()
+    return out
+
+
+def _decode_wl(wl: W.Workload, **kw):
+    return oracle.paged_decode(wl.q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens,
+                               wl.scale, dtype=wl.dtype, **kw)
+
+
+# --------------------------------------------------------------- dense reference
+@pytest.mark.parametrize("dtype", [W.DTYPE_F32, W.DTYPE_F16, W.DTYPE_BF16])
+@pytest.mark.parametrize("Hq,Hkv,d,bs", [(4, 1, 64, 16), (8, 2, 16, 16), (6, 3, 8, 4),
+                                         (16, 8, 32, 16), (2, 2, 8, 8)])
+def test_decode_equals_dense_torch_attention(dtype, Hq, Hkv, d, bs):
+    rng = np.random.default_rng(1000 + Hq * 7 + d + bs + dtype)
+    ctx = np.array([1, bs - 1, bs, bs + 1, 3 * bs + 5, 0], np.int32)
+    B, S = len(ctx), int(ctx.max())
+    dk = _draw(rng, (B, Hkv, S, d), dtype)
+    dv = _draw(rng, (B, Hkv, S, d), dtype)
+    q = _draw(rng, (B, Hq, d), dtype)
+    kc, vc, tables = _page(dk, dv, ctx, bs, rng)
+    scale = 0.7 / math.sqrt(d)
+    got = oracle.paged_decode(q, kc, vc, tables, ctx, scale, dtype=dtype)
+    want = _torch_dense_attention(_to_f64(q, dtype), _to_f64(dk, dtype), _to_f64(dv, dtype),
+                                  ctx, scale, Hq // Hkv)
+    np.testing.assert_allclose(got, want, rtol=0, atol=1e-12)
+
+
+# --------------------------------------------------------------- golden fixtures
+def _single_seq(q_row, k_rows, v_rows, bs, dtype=W.DTYPE_F32):
+    """One sequence, one q head, one KV head; pool built by the test."""
+    k = np.asarray(k_rows, np.float32)
+    v = np.asarray(v_rows, np.float32)
+    c, d = k.shape
+    nb = (c + bs - 1) // bs
+    kc = np.zeros((nb + 1, 1, bs, d), np.float32)
+    vc = np.zeros_like(kc)
+    # put the sequence in blocks 1..nb (block 0 unused, filled with NaN)
+    kc[0] = np.nan
+    vc[0] = np.nan
+    for j in range(c):
+        kc[1 + j // bs, 0, j % bs] = k[j]
+        vc[1 + j // bs, 0, j % bs] = v[j]
+    tables = np.arange(1, nb + 1, dtype=np.int32).reshape(1, nb)
+    q = np.asarray(q_row, np.float32).reshape(1, 1, d)
+    return q, kc, vc, tables, np.array([c], np.int32)
+
+
+def test_golden_two_keys_closed_form():
+    g = json.load(open(os.path.join(GOLDEN, "two_keys_closed_form.json")))
+    q, kc, vc, t, ctx = _single_seq(g["q"], g["k_rows"], g["v_rows"], g["block_size"])
+    out = oracle.paged_decode(q, kc, vc, t, ctx, math.log(3.0), dtype=W.DTYPE_F32)
+    np.testing.assert_allclose(out[0, 0], g["expected_out"], rtol=0, atol=g["tolerance"])
+
+
+def test_golden_large_logits_stable():
+    g = json.load(open(os.path.join(GOLDEN, "stability_large_logits.json")))
+    q, kc, vc, t, ctx = _single_seq(g["q"], g["k_rows"], g["v_rows"], g["block_size"])
+    out = oracle.paged_decode(q, kc, vc, t, ctx, g["scale"], dtype=W.DTYPE_F32)
+    assert np.all(np.isfinite(out))
+    np.testing.assert_array_equal(out[0, 0], np.asarray(g["expected_out"], np.float64))
+
+
+def test_golden_gqa_head_mapping():
+    g = json.load(open(os.path.join(GOLDEN, "gqa_mapping.json")))
+    Hq, Hkv, d, bs = g["num_q_heads"], g["num_kv_heads"], g["head_dim"], g["block_size"]
+    kc = np.full((2, Hkv, bs, d), np.nan, np.float32)
+    vc = np.full((2, Hkv, bs, d), np.nan, np.float32)
+    kc[1, :, 0, :] = np.asarray(g["k_heads"], np.float32)
+    vc[1, :, 0, :] = np.asarray(g["v_heads"], np.float32)
+    q = np.ones((1, Hq, d), np.float32)
+    out = oracle.paged_decode(q, kc, vc, np.array([[1]], np.int32), np.array([1], np.int32),
+                              0.3, dtype=W.DTYPE_F32)
+    np.testing.assert_array_equal(out[0], np.asarray(g["expected_out"], np.float64))
+
+
+# --------------------------------------------------------------- invariants
+@pytest.mark.parametrize("dtype", [W.DTYPE_F32, W.DTYPE_F16])
+def test_block_permutation_invariance_bit_identical(dtype):
+    wl = W.random_small(11, batch=5, num_q_heads=8, num_kv_heads=2, head_dim=64, max_ctx=80,
+                        dtype=dtype, extra_blocks=6)
+    base = _decode_wl(wl)
+    rng = np.random.default_rng(5)
+    perm = rng.permutation(wl.num_blocks)          # new position of each old block
+    kc = np.empty_like(wl.k_cache)
+    vc = np.empty_like(wl.v_cache)
+    kc[perm] = wl.k_cache
+    vc[perm] = wl.v_cache
+    tables = np.where(wl.block_tables >= 0, perm[np.maximum(wl.block_tables, 0)], -1)
+    tables = tables.astype(np.int32)
+    got = oracle.paged_decode(wl.q, kc, vc, tables, wl.context_lens, wl.scale, dtype=dtype)
+    np.testing.assert_array_equal(got, base)
+
+
+@pytest.mark.parametrize("dtype", [W.DTYPE_F32, W.DTYPE_F16, W.DTYPE_BF16])
+def test_one_token_context_returns_v_exactly(dtype):
+    wl = W.random_small(12, batch=3, num_q_heads=4, num_kv_heads=2, head_dim=16, max_ctx=1,
+                        dtype=dtype, context_lens=[1, 1, 1])
+    out = _decode_wl(wl)
+    G = wl.group
+    for b in range(3):
+        blk = wl.block_tables[b, 0]
+        for h in range(wl.num_q_heads):
+            v = _to_f64(wl.v_cache[blk, h // G, 0], dtype)
+            np.testing.assert_array_equal(out[b, h], v)
+
+
+def test_uniform_scores_give_mean_of_v():
+    wl = W.random_small(13, batch=4, num_q_heads=4, num_kv_heads=1, head_dim=32, max_ctx=70,
+                        dtype=W.DTYPE_F32, context_lens=[1, 17, 33, 70])
+    dense_k, dense_v = oracle.gather(wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens)
+    # (a) scale = 0
+    out0 = oracle.paged_decode(wl.q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens,
+                               0.0, dtype=wl.dtype)
+    # (b) q = 0
+    qz = np.zeros_like(wl.q)
+    outq = oracle.paged_decode(qz, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens,
+                               wl.scale, dtype=wl.dtype)
+    # (c) every key identical
+    kc = wl.k_cache.copy()
+    kc[...] = np.float32(0.375)
+    outk = oracle.paged_decode(wl.q, kc, wl.v_cache, wl.block_tables, wl.context_lens,
+                               wl.scale, dtype=wl.dtype)
+    for b, c in enumerate(wl.context_lens):
+        mean = dense_v[b, 0, :c, :].astype(np.float64).mean(axis=0)
+        for out in (out0, outq, outk):
+            for h in range(4):
+                np.testing.assert_allclose(out[b, h], mean, rtol=0, atol=1e-13)
+
+
+def test_score_shift_invariance():
+    wl = W.random_small(14, batch=3, num_q_heads=4, num_kv_heads=2, head_dim=32, max_ctx=50,
+                        dtype=W.DTYPE_F16, context_lens=[9, 31, 50])
+    # fp16 values widened to fp32 are exact, and so is the fp32 sum of two fp16
+    # values of this size, so the shifted keys below are exactly K + u.
+    q32 = wl.q.astype(np.float32)
+    k32 = wl.k_cache.astype(np.float32)
+    v32 = wl.v_cache.astype(np.float32)
+    base = oracle.paged_decode(q32, k32, v32, wl.block_tables, wl.context_lens, wl.scale,
+                               dtype=W.DTYPE_F32)
+    # q is shared by a group; shift every key of KV head kvh by u, s_j moves by
+    # scale*q.u for every j (constant within each (b, h)) -> output unchanged.
+    rng = np.random.default_rng(2)
+    u = rng.standard_normal((wl.num_kv_heads, 1, wl.head_dim)).astype(np.float16)
+    kc = (k32 + u.astype(np.float32)[None]).astype(np.float32)
+    got = oracle.paged_decode(q32, kc, v32, wl.block_tables, wl.context_lens,
+                              wl.scale, dtype=W.DTYPE_F32)
+    np.testing.assert_allclose(got, base, rtol=0, atol=1e-12)
+
+
+def test_split_merge_equals_direct_sum():
+    wl = W.random_small(15, batch=3, num_q_heads=4, num_kv_heads=2, head_dim=16, max_ctx=120,
+                        dtype=W.DTYPE_F16, context_lens=[1, 47, 120])
+    direct = _decode_wl(wl)
+    for b, c in enumerate(wl.context_lens):
+        c = int(c)
+        for cuts in ([0, c], [0, 0, c], [0, 1, c], [0, c // 3, 2 * c // 3, c, c],
+                     list(range(0, c, 16)) + [c]):
+            for h in range(wl.num_q_heads):
+                ms, ls, os_ = [], [], []
+                for j0, j1 in zip(cuts[:-1], cuts[1:]):
+                    m, l, o = oracle.attend_range(wl.q, wl.k_cache, wl.v_cache, wl.block_tables,
+                                                  wl.context_lens, wl.scale, b, h, j0, j1,
+                                                  dtype=wl.dtype)
+                    ms.append(m); ls.append(l); os_.append(o)
+                merged = oracle.merge(np.array(ms), np.array(ls), np.stack(os_))
+                np.testing.assert_allclose(merged, direct[b, h], rtol=0, atol=1e-12)
+
+
+def test_merge_closed_form_two_partials():
+    # Two partials with maxima 0 and ln 2: weights e^-ln2 and 1 on (l, o).
+    m = np.array([0.0, math.log(2.0)])
+    l = np.array([1.0, 1.0])
+    o = np.array([[2.0, 0.0], [0.0, 4.0]])
+    out = oracle.merge(m, l, o)
+    # num = 0.5*(2,0) + 1*(0,4) = (1,4); den = 0.5 + 1 = 1.5
+    np.testing.assert_allclose(out, [1.0 / 1.5, 4.0 / 1.5], rtol=0, atol=1e-15)
+    # an empty partial (l = 0, m = -inf) changes nothing
+    out2 = oracle.merge(np.append(m, -np.inf), np.append(l, 0.0), np.vstack([o, [0.0, 0.0]]))
+    np.testing.assert_array_equal(out2, out)
+    # all empty -> zero
+    np.testing.assert_array_equal(oracle.merge([-np.inf], [0.0], [[0.0, 0.0]]), [0.0, 0.0])
+
+
+def test_zero_context_gives_zeros_and_poison_is_never_read():
+    wl = W.random_small(16, batch=4, num_q_heads=4, num_kv_heads=2, head_dim=16, max_ctx=40,
+                        dtype=W.DTYPE_F16, context_lens=[0, 5, 0, 40], extra_blocks=4)
+    out = _decode_wl(wl)
+    assert np.all(np.isfinite(out))           # NaN pool slack never enters
+    np.testing.assert_array_equal(out[0], 0.0)
+    np.testing.assert_array_equal(out[2], 0.0)
+    # sanity: poisoning an owned row does show up, only in that sequence
+    kc = wl.k_cache.copy()
+    kc[wl.block_tables[1, 0], 0, 2, 3] = np.nan
+    bad = oracle.paged_decode(wl.q, kc, wl.v_cache, wl.block_tables, wl.context_lens, wl.scale,
+                              dtype=wl.dtype)
+    assert np.isnan(bad[1, :2]).all() and np.isfinite(bad[1, 2:]).all()
+    np.testing.assert_array_equal(bad[3], out[3])
+
+
+def test_threads_bit_identical():
+    wl = W.random_small(17, batch=7, num_q_heads=8, num_kv_heads=2, head_dim=64, max_ctx=300,
+                        dtype=W.DTYPE_F16)
+    np.testing.assert_array_equal(_decode_wl(wl, num_threads=1), _decode_wl(wl, num_threads=5))
+
+
+def test_decode_row_matches_full():
+    wl = W.random_small(18, batch=3, num_q_heads=4, num_kv_heads=2, head_dim=32, max_ctx=90,
+                        dtype=W.DTYPE_F16)
+    full = _decode_wl(wl)
+    for b in range(3):
+        for h in range(4):
+            row = oracle.paged_decode_row(wl.q, wl.k_cache, wl.v_cache, wl.block_tables,
+                                          wl.context_lens, wl.scale, b, h, dtype=wl.dtype)
+            np.testing.assert_array_equal(row, full[b, h])
+
+
+def test_widen_matches_numpy():
+    rng = np.random.default_rng(3)
+    x = (rng.standard_normal(4096) * 1000).astype(np.float16)
+    x[:4] = [np.float16(6e-8), np.float16(-0.0), np.float16(65504), np.float16(np.inf)]
+    np.testing.assert_array_equal(oracle.widen(x), x.astype(np.float64))
+    y = rng.standard_normal(512).astype(np.float32)
+    bf = (y.view(np.uint32) >> 16).astype(np.uint16)
+    np.testing.assert_array_equal(oracle.widen(bf, W.DTYPE_BF16), _to_f64(bf, W.DTYPE_BF16))
+
+
+def test_bad_inputs_rejected():
+    wl = W.random_small(19, batch=2, num_q_heads=4, num_kv_heads=2, head_dim=16, max_ctx=20,
+                        dtype=W.DTYPE_F32, context_lens=[20, 3])
+    ctx = wl.context_lens.copy()
+    ctx[0] = wl.max_blocks_per_seq * wl.block_size + 1
+    with pytest.raises(oracle.OracleError):
+        oracle.paged_decode(wl.q, wl.k_cache, wl.v_cache, wl.block_tables, ctx, wl.scale)
+    tables = wl.block_tables.copy()
+    tables[0, 0] = wl.num_blocks
+    with pytest.raises(oracle.OracleError):
+        oracle.paged_decode(wl.q, wl.k_cache, wl.v_cache, tables, wl.context_lens, wl.scale)
+
+
+# --------------------------------------------------------------- byte moves
+@pytest.mark.parametrize("dtype", [W.DTYPE_F32, W.DTYPE_F16, W.DTYPE_BF16])
+def test_cache_write_brute_force(dtype):
+    rng = np.random.default_rng(21 + dtype)
+    NB, Hkv, bs, d, T = 9, 3, 8, 16, 12
+    kc = _draw(rng, (NB, Hkv, bs, d), dtype)
+    vc = _draw(rng, (NB, Hkv, bs, d), dtype)
+    kn = _draw(rng, (T, Hkv, d), dtype)
+    vn = _draw(rng, (T, Hkv, d), dtype)
+    slots = rng.choice(NB * bs, size=T, replace=False).astype(np.int64)
+    slots[[2, 7]] = -1                                        # padding rows
+    k0, v0 = kc.copy(), vc.copy()
+    oracle.cache_write(kn, vn, slots, kc, vc, block_size=bs, dtype=dtype)
+    written = {int(s): t for t, s in enumerate(slots) if s >= 0}
+    for blk in range(NB):
+        for off in range(bs):
+            s = blk * bs + off
+            if s in written:
+                t = written[s]
+                assert kc[blk, :, off].tobytes() == kn[t].tobytes()
+                assert vc[blk, :, off].tobytes() == vn[t].tobytes()
+            else:
+                assert kc[blk, :, off].tobytes() == k0[blk, :, off].tobytes()
+                assert vc[blk, :, off].tobytes() == v0[blk, :, off].tobytes()
+
+
+def test_cache_write_rejects_bad_slots_without_writing():
+    rng = np.random.default_rng(22)
+    NB, Hkv, bs, d = 4, 2, 16, 8
+    kc = _draw(rng, (NB, Hkv, bs, d), W.DTYPE_F16)
+    vc = kc.copy()
+    k0 = kc.copy()
+    kn = _draw(rng, (2, Hkv, d), W.DTYPE_F16)
+    for slots in ([0, NB * bs], [5, 5]):
+        with pytest.raises(oracle.OracleError):
+            oracle.cache_write(kn, kn, np.array(slots, np.int64), kc, vc, block_size=bs)
+        np.testing.assert_array_equal(kc.view(np.uint16), k0.view(np.uint16))
+
+
+@pytest.mark.parametrize("dtype", [W.DTYPE_F32, W.DTYPE_F16])
+def test_gather_closed_form_and_permutation(dtype):
+    wl = W.random_small(23, batch=4, num_q_heads=4, num_kv_heads=2, head_dim=16, max_ctx=50,
+                        dtype=dtype, extra_blocks=5, context_lens=[0, 16, 17, 50])
+    kd, vd = oracle.gather(wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens)
+    bs = wl.block_size
+    span = wl.max_blocks_per_seq * bs
+    for b in range(4):
+        c = int(wl.context_lens[b])
+        for j in range(span):
+            if j < c:
+                blk = wl.block_tables[b, j // bs]
+                assert kd[b, :, j].tobytes() == wl.k_cache[blk, :, j % bs].tobytes()
+                assert vd[b, :, j].tobytes() == wl.v_cache[blk, :, j % bs].tobytes()
+            else:
+                assert not kd[b, :, j].view(np.uint8).any()
+                assert not vd[b, :, j].view(np.uint8).any()
+    assert np.isfinite(kd.astype(np.float64)).all() and np.isfinite(vd.astype(np.float64)).all()
+    perm = np.random.default_rng(1).permutation(wl.num_blocks)
+    kc = np.empty_like(wl.k_cache); kc[perm] = wl.k_cache
+    vc = np.empty_like(wl.v_cache); vc[perm] = wl.v_cache
+    tables = np.where(wl.block_tables >= 0, perm[np.maximum(wl.block_tables, 0)], -1)
+    kd2, vd2 = oracle.gather(kc, vc, tables.astype(np.int32), wl.context_lens)
+    assert kd2.tobytes() == kd.tobytes() and vd2.tobytes() == vd.tobytes()
+
+
+# --------------------------------------------------------------- the named workloads
+def test_tiny_workload_shape_and_finite():
+    wl = W.tiny()
+    assert wl.block_tables.tolist()[0][1:] == [-1, -1, -1]
+    assert (wl.block_tables >= 0).sum() == 4 and wl.num_blocks == 8
+    out = _decode_wl(wl)
+    assert out.shape == (2, 4, 64) and np.isfinite(out).all()
+
+
+def test_step_order_cache_write_then_decode():
+    """The step writes each sequence's new row at position ctx-1, then attends
+    over [0, ctx): the new row must take part (its V appears when its key
+    dominates)."""
+    wl = W.random_small(24, batch=3, num_q_heads=2, num_kv_heads=1, head_dim=16, max_ctx=40,
+                        dtype=W.DTYPE_F32, context_lens=[1, 16, 33])
+    kc, vc = wl.k_cache.copy(), wl.v_cache.copy()
+    kn = (wl.q[:, :1, :] * 50.0).astype(np.float32)       # key aligned with q head 0
+    oracle.cache_write(kn, wl.v_new, wl.slot_mapping, kc, vc, block_size=wl.block_size)
+    out = oracle.paged_decode(wl.q, kc, vc, wl.block_tables, wl.context_lens, 1.0)
+    for b in range(3):
+        np.testing.assert_allclose(out[b, 0], wl.v_new[b, 0].astype(np.float64), atol=1e-6)
