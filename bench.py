@@ -1,0 +1,459 @@
+#!/usr/bin/env python
+"""Benchmark of the paged decode-attention step on GB300.
+
+One step = the whole hot path over one batch: the batched cache write of the
+new K/V rows, then split-KV paged decode attention with its partition merge,
+in one stream, through the library's C ABI.  Default workload: Qwen3-style
+long context -- 64 sequences, 16 q / 8 KV heads, head_dim 128, 16-token
+blocks, fp16, context lengths log-uniform in [128, 8192], a 40 000-block
+pool in random order.
+
+Prints one JSON line.  value = algorithmic HBM bytes of the step (every K/V
+row inside the contexts, q, out, block-table entries used, context lengths,
+plus the cache write's rows and slots) / device time per step, in GB/s.
+L2 is flushed (a 512 MB write) before every timed step, outside the timed
+events.
+
+--impl reference times the fp64 CPU oracle instead (the only reference this
+method has), on a bounded sample of the same workload, on the host cores.
+Multi-GPU (torchrun): every rank runs its own batch (sequences shard with no
+exchange), value = all ranks' bytes / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "paged-decode KV GB/s and fraction of GB300 HBM peak; decode tokens/s per layer"
+FALLBACK_HBM_GBS = 6800.0
+L2_FLUSH_BYTES = 512 << 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="qwen_b64", choices=sorted(W.NAMED))
+    ap.add_argument("--partition", type=int, default=0, help="tokens per partition; 0 = default")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--json-out", default="")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------- helpers
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def make_workload(name: str, rank: int) -> W.Workload:
+    if rank == 0:
+        return W.NAMED[name]()
+    # weak scaling: every rank draws its own batch of the same recipe
+    seeds = {"qwen_b64": 2, "mix_b256": 3, "llama_b16": 1, "tiny": 0}
+    if name == "qwen_b64":
+        return W.qwen_b64(seed=seeds[name] + 1000 * rank)
+    if name == "mix_b256":
+        return W.mix_b256(seed=seeds[name] + 1000 * rank)
+    if name == "llama_b16":
+        return W.llama_b16(seed=seeds[name] + 1000 * rank)
+    return W.NAMED[name]()
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        data = json.load(open(path))
+    except Exception:
+        return None, "fallback"
+    def find(d, keys):
+        if isinstance(d, dict):
+            for k in keys:
+                if k in d and isinstance(d[k], (int, float)):
+                    return float(d[k])
+            for v in d.values():
+                r = find(v, keys)
+                if r is not None:
+                    return r
+        return None
+    v = find(data, ["hbm_gbs", "hbm_gbs_burst", "hbm_copy_gbs", "hbm_GBps"])
+    return (v, "measured") if v else (None, "fallback")
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_kv_attention_photon_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh")):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(workload: str):
+    """Per-launch DRAM bytes of the attention kernel from a committed ncu summary,
+    or None if the summary is missing or was taken on other kernel sources."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        d = json.load(open(path))
+    except Exception:
+        return None
+    e = d.get(workload)
+    if not e or e.get("kernel_source_sha") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu_index = gpu_index
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.gpu_index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is None:
+            return False
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        self.lines = [l for l in out.splitlines() if l.strip()]
+        return False
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in getattr(self, "lines", []):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------- CPU oracle timing
+def oracle_sample(wl: W.Workload, max_tokens: int):
+    """First sequences of the batch whose contexts sum to <= max_tokens (>= 1 seq)."""
+    csum = np.cumsum(wl.context_lens.astype(np.int64))
+    n = int(max(1, np.searchsorted(csum, max_tokens, side="right")))
+    n = min(n, wl.num_seqs)
+    return n, int(csum[n - 1])
+
+
+def time_oracle_step(wl: W.Workload, n: int, threads: int):
+    import oracle
+    kc, vc = wl.k_cache, wl.v_cache
+    t0 = time.perf_counter()
+    oracle.cache_write(wl.k_new[:n], wl.v_new[:n], wl.slot_mapping[:n], kc, vc,
+                       block_size=wl.block_size, dtype=wl.dtype)
+    oracle.paged_decode(wl.q[:n], kc, vc, np.ascontiguousarray(wl.block_tables[:n]),
+                        np.ascontiguousarray(wl.context_lens[:n]), wl.scale, dtype=wl.dtype,
+                        num_threads=threads)
+    return time.perf_counter() - t0
+
+
+def sample_bytes(wl: W.Workload, n: int) -> int:
+    sub = W.Workload(**{**wl.__dict__, "num_seqs": n, "context_lens": wl.context_lens[:n],
+                        "block_tables": wl.block_tables[:n], "q": wl.q[:n],
+                        "k_new": wl.k_new[:n], "v_new": wl.v_new[:n],
+                        "slot_mapping": wl.slot_mapping[:n]})
+    return sub.decode_bytes() + sub.cache_write_bytes()
+
+
+def cpu_baseline(wl: W.Workload, budget_s: float = 20.0):
+    import oracle
+    oracle.build()
+    threads = os.cpu_count() or 1
+    # calibrate on a small sample, then size the measured sample to the budget
+    n0, tok0 = oracle_sample(wl, 4000)
+    dt0 = time_oracle_step(wl, n0, threads)
+    rate = tok0 / max(dt0, 1e-6)
+    n, tok = oracle_sample(wl, int(rate * budget_s / 4))
+    dt = time_oracle_step(wl, n, threads)
+    gbs = sample_bytes(wl, n) / dt / 1e9
+    return {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"first {n} of {wl.num_seqs} sequences ({tok} tokens attended), "
+                      f"cache write + decode, fp64, {threads} threads, one run of {dt:.2f} s"}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    oracle.build()
+    wl = W.NAMED[args.workload]()
+    threads = os.cpu_count() or 1
+    total_budget = 150.0
+    n0, tok0 = oracle_sample(wl, 4000)
+    rate = tok0 / max(time_oracle_step(wl, n0, threads), 1e-6)
+    per_step = total_budget / max(1, args.steps + args.warmup)
+    n, tok = oracle_sample(wl, int(rate * per_step))
+    for _ in range(args.warmup):
+        time_oracle_step(wl, n, threads)
+    times = [time_oracle_step(wl, n, threads) for _ in range(args.steps)]
+    ms = 1e3 * sum(times) / len(times)
+    gbs = sample_bytes(wl, n) / (ms / 1e3) / 1e9
+    sample = (f"first {n} of {wl.num_seqs} sequences ({tok} tokens attended) per step, "
+              f"cache write + decode, fp64 oracle, {threads} threads")
+    line = {"impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "sample_sequences": n},
+            "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": threads,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------- GPU arm
+def run_ours(args):
+    import torch
+    import paged_kv_attention_photon_gb300 as P
+
+    world, rank, local = dist_env()
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+        pg = dist
+    torch.cuda.set_device(local)
+    P.build()
+
+    wl = make_workload(args.workload, rank)
+    shape = P.PagedShape.make(partition_size=args.partition, **wl.shape_dict())
+    plan = P.photon_paged_decode_plan(shape)
+
+    def dev(a):
+        a = np.ascontiguousarray(a)
+        return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).cuda()
+
+    q, kc, vc = dev(wl.q), dev(wl.k_cache), dev(wl.v_cache)
+    bt, cl = dev(wl.block_tables), dev(wl.context_lens)
+    kn, vn, sm = dev(wl.k_new), dev(wl.v_new), dev(wl.slot_mapping)
+    out = torch.empty_like(q)
+    ws_bytes = P.photon_paged_decode_workspace_size(shape)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device="cuda")
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    T = wl.slot_mapping.shape[0]
+    stream = torch.cuda.current_stream()
+
+    def step():
+        P.photon_cache_write(kn, vn, sm, T, kc, vc, shape, stream)
+        P.photon_paged_decode(q, kc, vc, bt, cl, wl.scale, out, ws, ws_bytes, shape, stream)
+
+    for _ in range(max(3, args.warmup)):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    st, bits = P.photon_get_last_device_error(stream)
+    if st != 0:
+        raise RuntimeError(f"device error word {bits} during warm-up")
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    kev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(K)]
+    for a, b in kev:  # materialise the events so their raw handles exist
+        a.record(stream)
+        b.record(stream)
+    torch.cuda.synchronize()
+
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    cvd = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    sampler = ClockSampler(cvd.split(",")[local] if cvd else str(local))
+    with sampler:
+        t_wall0 = time.perf_counter()
+        for i in range(K):
+            flush.zero_()
+            P.photon_debug_set_attention_events(kev[i][0], kev[i][1])
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall0
+    P.photon_debug_set_attention_events(None, None)
+    if pg:
+        pg.barrier()
+    st, bits = P.photon_get_last_device_error(stream)
+    if st != 0:
+        raise RuntimeError(f"device error word {bits} during the timed steps")
+
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    attn_ms = [a.elapsed_time(b) for a, b in kev]
+    ms = sum(step_ms) / K
+    attn_mean_ms = sum(attn_ms) / K
+
+    step_bytes = wl.decode_bytes() + wl.cache_write_bytes()
+    decode_bytes = wl.decode_bytes()
+
+    # max over ranks of the step time, sum of bytes
+    if pg:
+        t = torch.tensor([ms, attn_mean_ms], dtype=torch.float64)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms_max, attn_max = float(t[0]), float(t[1])
+        tb = torch.tensor([float(step_bytes), float(wl.num_seqs), float(wl.tokens_attended())],
+                          dtype=torch.float64)
+        pg.all_reduce(tb)
+        tot_bytes, tot_seqs, tot_tokens = float(tb[0]), float(tb[1]), float(tb[2])
+    else:
+        ms_max, attn_max = ms, attn_mean_ms
+        tot_bytes, tot_seqs, tot_tokens = float(step_bytes), float(wl.num_seqs), \
+            float(wl.tokens_attended())
+
+    value = tot_bytes / (ms_max / 1e3) / 1e9
+
+    # ---- end to end through the public API, host buffers, copies inside the timing
+    e2e = None
+    if not args.no_e2e:
+        h_in = [torch.from_numpy(np.ascontiguousarray(a.view(np.int16) if a.dtype == np.uint16
+                                                       else a)).pin_memory()
+                for a in (wl.q, wl.k_new, wl.v_new, wl.slot_mapping, wl.block_tables,
+                          wl.context_lens)]
+        d_in = [q, kn, vn, sm, bt, cl]
+        h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in h_in)
+        d2h = h_out.numel() * h_out.element_size()
+        ee = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(K)]
+
+        def e2e_step(i):
+            ee[i][0].record(stream)
+            for h, d in zip(h_in, d_in):
+                d.copy_(h, non_blocking=True)
+            step()
+            h_out.copy_(out, non_blocking=True)
+            ee[i][1].record(stream)
+
+        for i in range(min(3, K)):
+            flush.zero_()
+            e2e_step(i)
+        torch.cuda.synchronize()
+        for i in range(K):
+            flush.zero_()
+            e2e_step(i)
+        torch.cuda.synchronize()
+        e2e_ms = sum(a.elapsed_time(b) for a, b in ee) / K
+        if pg:
+            t = torch.tensor([e2e_ms], dtype=torch.float64)
+            pg.all_reduce(t, op=pg.ReduceOp.MAX)
+            e2e_ms = float(t[0])
+        e2e = {"value": round(tot_bytes / (e2e_ms / 1e3) / 1e9, 2), "unit": "GB/s",
+               "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(h2d),
+               "d2h_bytes_per_step": int(d2h)}
+
+    peak, peak_kind = measured_peaks()
+    if peak is None:
+        peak = FALLBACK_HBM_GBS
+    achieved = decode_bytes / (attn_mean_ms / 1e3) / 1e9
+    roofline = {"bound": "hbm", "kernel": "paged_decode_split_kernel",
+                "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} HBM copy bandwidth",
+                "traffic": ncu_traffic(args.workload),
+                "algorithmic_bytes_per_launch": int(decode_bytes),
+                "ms_per_launch": round(attn_mean_ms, 5)}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(wl)
+
+    if rank == 0:
+        clocks = sampler.summary()
+        line = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+            "steps": K, "warmup": max(3, args.warmup), "ms_per_step": round(ms_max, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": W.DTYPE_NAMES[wl.dtype], "data": "synthetic",
+            "config": {"workload": wl.name, "batch": wl.num_seqs,
+                       "q_heads": wl.num_q_heads, "kv_heads": wl.num_kv_heads,
+                       "head_dim": wl.head_dim, "block_size": wl.block_size,
+                       "num_blocks": wl.num_blocks, "tokens_attended": wl.tokens_attended(),
+                       "partition_size": plan["partition_size"],
+                       "l2": "flushed before every step (512 MB write), outside the timed events",
+                       "parallelism": f"dp{world} (independent batches per GPU)"},
+            "hbm_fraction": round(value / peak, 4),
+            "decode_tokens_per_s_per_layer": round(tot_seqs / (ms_max / 1e3), 1),
+            "tokens_attended_per_s": round(tot_tokens / (ms_max / 1e3), 1),
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": K * (1 + plan["kernels_per_call"]),
+            "clocks": clocks,
+            "wall_ms_per_step_incl_flush": round(1e3 * t_wall / K, 4),
+            "step_ms_p10_p90": [round(float(np.percentile(step_ms, 10)), 5),
+                                round(float(np.percentile(step_ms, 90)), 5)],
+        }
+        s = json.dumps(line)
+        print(s, flush=True)
+        if args.json_out:
+            with open(args.json_out, "w") as f:
+                f.write(s + "\n")
+    if pg:
+        pg.barrier()
+        pg.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

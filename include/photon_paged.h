@@ -1,0 +1,171 @@
+/*
+ * photon_paged.h -- C ABI of the GB300 paged decode-attention library
+ * (libphoton_paged.so, CUDA kernels built for sm_103a).
+ *
+ * What the library computes comes from the PhotonInfer README
+ * ("openaitx.github.io/projects/lumia431/photon_infer/README-ko.html"):
+ *   - "Key features / GPU-optimized kernels": batched paged attention with a
+ *     block-wise KV cache; softmax computed in a numerically stable way;
+ *     vectorised 128-bit memory access;
+ *   - "Technical details / Paged attention": block-wise KV cache without
+ *     fragmentation, per-sequence cache offsets (block tables), and a single
+ *     kernel that writes the new K/V rows of many sequences;
+ *   - "Key features / Modern C++20 architecture": errors are returned as
+ *     explicit values (a Result-style status), and buffers are passed without
+ *     copies (the caller owns every buffer).
+ * The page gives no formula.  The operation is scaled dot-product attention
+ * of one new query row per sequence over that sequence's cached rows, with
+ * grouped query heads:
+ *     out[b][h] = sum_j softmax_j(scale * q[b][h] . K_j[kvh]) V_j[kvh],
+ *     kvh = h / (num_q_heads / num_kv_heads),  j = 0 .. context_lens[b]-1,
+ *     K_j, V_j found at cache[block_tables[b][j / block_size]][kvh][j % block_size].
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Every pointer argument named as a buffer is a DEVICE pointer on the
+ *   current CUDA device, owned by the caller, and must be 16-byte aligned.
+ *   The library allocates no memory, makes no host<->device copies and never
+ *   synchronises on the decode/cache-write path; all work is enqueued on
+ *   `stream` (NULL = the legacy default stream).
+ * - Every entry point returns a photon_status_t.  Argument errors are found on
+ *   the host before anything is launched and leave every buffer untouched.
+ *   Nothing throws or aborts across this boundary.
+ * - Index errors that only the device can see (a block id outside the pool,
+ *   a slot outside the pool, a context length outside [0, max_blocks_per_seq *
+ *   block_size]) never fault or trap: the offending row / block / sequence is
+ *   skipped (a bad sequence is treated as empty, a bad block as absent) and a
+ *   sticky device error word is set; photon_get_last_device_error() reads and
+ *   clears it.
+ *
+ * Layouts (row-major, element type = shape->dtype)
+ *   k, v (new rows)         [num_tokens][num_kv_heads][head_dim]
+ *   q, out                  [num_seqs][num_q_heads][head_dim]
+ *   k_cache, v_cache        [num_blocks][num_kv_heads][block_size][head_dim]
+ *                           (head-major inside a block: the block_size rows of
+ *                           one KV head are one contiguous chunk)
+ *   slot_mapping            int64 [num_tokens]; slot = block * block_size +
+ *                           offset; a negative slot marks a padding row
+ *   block_tables            int32 [num_seqs][max_blocks_per_seq]; entries past
+ *                           ceil(context_len / block_size) are never read
+ *                           (padding -1 by convention)
+ *   context_lens            int32 [num_seqs]; counts the new token
+ */
+#ifndef PHOTON_PAGED_H
+#define PHOTON_PAGED_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same opaque type as CUDA's cudaStream_t, so a cudaStream_t passes as is. */
+typedef struct CUstream_st* photon_stream_t;
+
+typedef enum {
+  PHOTON_OK = 0,
+  PHOTON_ERR_INVALID_ARG = 1,   /* null pointer, negative size, Hq % Hkv != 0, ... */
+  PHOTON_ERR_UNSUPPORTED = 2,   /* head_dim / block_size / dtype not built        */
+  PHOTON_ERR_MISALIGNED = 3,    /* a buffer is not 16-byte aligned                */
+  PHOTON_ERR_WORKSPACE = 4,     /* workspace missing or smaller than required     */
+  PHOTON_ERR_CUDA = 5,          /* a CUDA runtime call or launch failed           */
+  PHOTON_ERR_DEVICE_BOUNDS = 6  /* the device saw an out-of-range index (sticky)  */
+} photon_status_t;
+
+typedef enum { PHOTON_F32 = 0, PHOTON_F16 = 1, PHOTON_BF16 = 2 } photon_dtype_t;
+
+/* Problem description shared by all calls.
+ *   head_dim ∈ {64, 128}; block_size == 16; num_q_heads % num_kv_heads == 0
+ *   with group size num_q_heads / num_kv_heads ∈ {1, 2, 4, 8};
+ *   dtype ∈ {PHOTON_F32, PHOTON_F16, PHOTON_BF16}.
+ *   partition_size: tokens per split-KV partition for photon_paged_decode, a
+ *   multiple of block_size in [block_size, 4096]; 0 selects the library
+ *   default.  Ignored by the other calls. */
+typedef struct {
+  int32_t num_seqs;
+  int32_t num_q_heads;
+  int32_t num_kv_heads;
+  int32_t head_dim;
+  int32_t block_size;
+  int32_t num_blocks;
+  int32_t max_blocks_per_seq;
+  int32_t dtype;           /* photon_dtype_t */
+  int32_t partition_size;  /* 0 = default */
+} photon_paged_shape_t;
+
+/* Batched cache write ("Technical details / Paged attention": one kernel for
+ * the K/V writes of many sequences).  For every row t < num_tokens with
+ * slot_mapping[t] >= 0 and every KV head h, copies k[t][h][:] and v[t][h][:]
+ * bit for bit to k_cache / v_cache[slot / block_size][h][slot % block_size][:].
+ * Rows with a negative slot are skipped.  A slot >= num_blocks * block_size is
+ * skipped and sets the device error word.  Two rows with the same slot race
+ * (the caller must not pass duplicates).  num_tokens == 0 is a no-op.
+ * Uses shape: num_kv_heads, head_dim, block_size, num_blocks, dtype. */
+photon_status_t photon_cache_write(const void* k, const void* v, const int64_t* slot_mapping,
+                                   int32_t num_tokens, void* k_cache, void* v_cache,
+                                   const photon_paged_shape_t* shape, photon_stream_t stream);
+
+/* Bytes of device workspace photon_paged_decode needs for this shape (split-KV
+ * partials and the work list).  Depends on num_seqs, num_q_heads,
+ * num_kv_heads, head_dim, block_size, max_blocks_per_seq and partition_size.
+ * Returns 0 for an invalid shape. */
+size_t photon_paged_decode_workspace_size(const photon_paged_shape_t* shape);
+
+/* Batched paged decode attention ("Key features / GPU-optimized kernels":
+ * batched paged attention, numerically stable softmax).  Computes, for every
+ * sequence b and q head h, the formula in this file's header, in fp32
+ * arithmetic from the stored dtype, and stores out[b][h][:] rounded to the
+ * stored dtype (round to nearest even).  A sequence with context 0 gets a
+ * zero row.  The context of each sequence is cut into partitions of
+ * partition_size tokens that are attended in parallel and then merged by
+ * their log-sum-exp weights.  `workspace` (device, >= the size reported by
+ * photon_paged_decode_workspace_size) is scratch owned by the caller; its
+ * contents need no initialisation and are undefined afterwards; two calls
+ * that may run at the same time must not share it.  scale must be finite. */
+photon_status_t photon_paged_decode(const void* q, const void* k_cache, const void* v_cache,
+                                    const int32_t* block_tables, const int32_t* context_lens,
+                                    float scale, void* out, void* workspace,
+                                    size_t workspace_bytes, const photon_paged_shape_t* shape,
+                                    photon_stream_t stream);
+
+/* Test / diagnostic export: the block-table gather the decode kernel performs,
+ * materialised.  k_dense, v_dense are [num_seqs][num_kv_heads][max_blocks_per_seq
+ * * block_size][head_dim]; row j of sequence b is a bit copy of the cached row
+ * at logical position j for j < context_lens[b] and zero bytes after. */
+photon_status_t photon_paged_gather(const void* k_cache, const void* v_cache,
+                                    const int32_t* block_tables, const int32_t* context_lens,
+                                    void* k_dense, void* v_dense,
+                                    const photon_paged_shape_t* shape, photon_stream_t stream);
+
+/* Synchronises `stream`, then reads and clears the current device's sticky
+ * error word.  Returns PHOTON_ERR_DEVICE_BOUNDS if any kernel of this library
+ * skipped an out-of-range index since the last call, PHOTON_ERR_CUDA if the
+ * synchronisation itself failed, PHOTON_OK otherwise.  If `bits` is not NULL
+ * it receives the word: 1 = block id out of range, 2 = slot out of range,
+ * 4 = context length out of range. */
+photon_status_t photon_get_last_device_error(photon_stream_t stream, uint32_t* bits);
+
+/* Static text for a status code (never NULL). */
+const char* photon_status_string(photon_status_t status);
+
+/* Diagnostic: launch geometry photon_paged_decode would use for `shape` on the
+ * current device: the partition size in tokens, the largest number of
+ * partitions a sequence can have, the number of CTAs of the attention kernel
+ * and the number of kernels one call launches.  Any output pointer may be
+ * NULL. */
+photon_status_t photon_paged_decode_plan(const photon_paged_shape_t* shape,
+                                         int32_t* partition_size, int32_t* max_partitions,
+                                         int32_t* attention_ctas, int32_t* kernels_per_call);
+
+/* Diagnostic timing hook: when both are non-NULL, photon_paged_decode records
+ * start_event right before and stop_event right after its split-KV attention
+ * kernel, on the call's stream (cudaEvent_t values passed as void*).  Pass
+ * NULL, NULL to turn it off.  Process-wide; not for concurrent use. */
+photon_status_t photon_debug_set_attention_events(void* start_event, void* stop_event);
+
+#ifdef __cplusplus
+}  /* extern "C" */
+#endif
+
+#endif /* PHOTON_PAGED_H */

@@ -1,0 +1,194 @@
+"""Python binding of libphoton_paged.so (GB300 paged decode attention).
+
+Argument marshalling only: every step of the cache write, the block-table
+gather, the split-KV attention and the partition merge runs in the CUDA
+kernels of the shared library.  There is no Python or CPU fallback: if the
+library is missing, importing this package fails.
+
+Buffers may be given as torch CUDA tensors (their ``data_ptr()`` is passed) or
+as raw integer device addresses.  ``stream`` is a ``torch.cuda.Stream``, a raw
+``cudaStream_t`` integer, or None for torch's current stream.
+
+Functions carry the names of the C entry points declared in
+``include/photon_paged.h`` and raise :class:`PhotonError` on a non-OK status.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+from typing import Optional, Tuple
+
+from . import _build
+
+__all__ = [
+    "PhotonError", "PagedShape", "build", "library_path", "exported_symbols",
+    "photon_cache_write", "photon_paged_decode_workspace_size", "photon_paged_decode",
+    "photon_paged_gather", "photon_get_last_device_error", "photon_status_string",
+    "photon_paged_decode_plan", "photon_debug_set_attention_events",
+    "F32", "F16", "BF16", "STATUS",
+]
+
+F32, F16, BF16 = 0, 1, 2
+STATUS = {0: "PHOTON_OK", 1: "PHOTON_ERR_INVALID_ARG", 2: "PHOTON_ERR_UNSUPPORTED",
+          3: "PHOTON_ERR_MISALIGNED", 4: "PHOTON_ERR_WORKSPACE", 5: "PHOTON_ERR_CUDA",
+          6: "PHOTON_ERR_DEVICE_BOUNDS"}
+
+
+class PhotonError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)} "
+                         f"({_string(status)})")
+
+
+class PagedShape(ctypes.Structure):
+    """Mirror of photon_paged_shape_t."""
+
+    _fields_ = [("num_seqs", ctypes.c_int32), ("num_q_heads", ctypes.c_int32),
+                ("num_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("block_size", ctypes.c_int32), ("num_blocks", ctypes.c_int32),
+                ("max_blocks_per_seq", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("partition_size", ctypes.c_int32)]
+
+    @classmethod
+    def make(cls, *, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size=16,
+             num_blocks, max_blocks_per_seq, dtype, partition_size=0) -> "PagedShape":
+        return cls(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                   max_blocks_per_seq, dtype, partition_size)
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def build(force: bool = False) -> str:
+    """Compile the CUDA sources for sm_103a (in-tree) and return the .so path."""
+    return _build.build(force=force)
+
+
+_lib = None
+
+
+def _load() -> ctypes.CDLL:
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing: build it with "
+                          "paged_kv_attention_photon_gb300.build() (needs nvcc)")
+    lib = ctypes.CDLL(path)
+    P, I32, SZ = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+    SP = ctypes.POINTER(PagedShape)
+    lib.photon_cache_write.argtypes = [P, P, P, I32, P, P, SP, P]
+    lib.photon_paged_decode_workspace_size.argtypes = [SP]
+    lib.photon_paged_decode_workspace_size.restype = SZ
+    lib.photon_paged_decode.argtypes = [P, P, P, P, P, ctypes.c_float, P, P, SZ, SP, P]
+    lib.photon_paged_gather.argtypes = [P, P, P, P, P, P, SP, P]
+    lib.photon_get_last_device_error.argtypes = [P, ctypes.POINTER(ctypes.c_uint32)]
+    lib.photon_status_string.argtypes = [ctypes.c_int]
+    lib.photon_status_string.restype = ctypes.c_char_p
+    lib.photon_paged_decode_plan.argtypes = [SP] + [ctypes.POINTER(I32)] * 4
+    lib.photon_debug_set_attention_events.argtypes = [P, P]
+    for fn in ("photon_cache_write", "photon_paged_decode", "photon_paged_gather",
+               "photon_get_last_device_error", "photon_paged_decode_plan",
+               "photon_debug_set_attention_events"):
+        getattr(lib, fn).restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def exported_symbols() -> Tuple[str, ...]:
+    """Names of the functions declared in include/photon_paged.h."""
+    hdr = os.path.join(_build.INCLUDE, "photon_paged.h")
+    text = open(hdr).read()
+    return tuple(sorted(set(re.findall(r"^\S.*?\b(photon_\w+)\(", text, re.M))))
+
+
+def _string(status: int) -> str:
+    try:
+        return _load().photon_status_string(int(status)).decode()
+    except Exception:  # pragma: no cover - only used inside error messages
+        return "?"
+
+
+def _ptr(x) -> Optional[int]:
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _check(status: int, where: str) -> None:
+    if status != 0:
+        raise PhotonError(status, where)
+
+
+# ------------------------------------------------------------------ entry points
+def photon_status_string(status: int) -> str:
+    return _string(status)
+
+
+def photon_cache_write(k, v, slot_mapping, num_tokens: int, k_cache, v_cache,
+                       shape: PagedShape, stream=None) -> None:
+    _check(_load().photon_cache_write(_ptr(k), _ptr(v), _ptr(slot_mapping), int(num_tokens),
+                                      _ptr(k_cache), _ptr(v_cache), ctypes.byref(shape),
+                                      _stream(stream)), "photon_cache_write")
+
+
+def photon_paged_decode_workspace_size(shape: PagedShape) -> int:
+    return int(_load().photon_paged_decode_workspace_size(ctypes.byref(shape)))
+
+
+def photon_paged_decode(q, k_cache, v_cache, block_tables, context_lens, scale: float, out,
+                        workspace, workspace_bytes: int, shape: PagedShape, stream=None) -> None:
+    _check(_load().photon_paged_decode(_ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                       _ptr(block_tables), _ptr(context_lens),
+                                       float(scale), _ptr(out), _ptr(workspace),
+                                       int(workspace_bytes), ctypes.byref(shape),
+                                       _stream(stream)), "photon_paged_decode")
+
+
+def photon_paged_gather(k_cache, v_cache, block_tables, context_lens, k_dense, v_dense,
+                        shape: PagedShape, stream=None) -> None:
+    _check(_load().photon_paged_gather(_ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                       _ptr(context_lens), _ptr(k_dense), _ptr(v_dense),
+                                       ctypes.byref(shape), _stream(stream)),
+           "photon_paged_gather")
+
+
+def photon_get_last_device_error(stream=None) -> Tuple[int, int]:
+    """Returns (status, bits); does not raise for PHOTON_ERR_DEVICE_BOUNDS."""
+    bits = ctypes.c_uint32(0)
+    st = _load().photon_get_last_device_error(_stream(stream), ctypes.byref(bits))
+    if st not in (0, 6):
+        raise PhotonError(st, "photon_get_last_device_error")
+    return int(st), int(bits.value)
+
+
+def photon_paged_decode_plan(shape: PagedShape) -> dict:
+    vals = [ctypes.c_int32(0) for _ in range(4)]
+    _check(_load().photon_paged_decode_plan(ctypes.byref(shape), *[ctypes.byref(v) for v in vals]),
+           "photon_paged_decode_plan")
+    return dict(partition_size=vals[0].value, max_partitions=vals[1].value,
+                attention_ctas=vals[2].value, kernels_per_call=vals[3].value)
+
+
+def photon_debug_set_attention_events(start_event=None, stop_event=None) -> None:
+    def raw(ev):
+        if ev is None:
+            return None
+        return ev.cuda_event if hasattr(ev, "cuda_event") else int(ev)
+    _check(_load().photon_debug_set_attention_events(raw(start_event), raw(stop_event)),
+           "photon_debug_set_attention_events")

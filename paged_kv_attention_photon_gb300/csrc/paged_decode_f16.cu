@@ -1,0 +1,8 @@
+// paged_decode_f16.cu -- instantiates the paged decode kernels for f16 storage.
+#include "paged_decode.cuh"
+
+namespace photon {
+cudaError_t launch_paged_decode_f16(const DecodeArgs& a, cudaStream_t stream) {
+  return launch_decode_t<__half>(a, stream);
+}
+}  // namespace photon

@@ -1,0 +1,275 @@
+// photon_api.cu -- the extern "C" boundary of libphoton_paged.so.
+//
+// Host-side argument checks, workspace carving, the sticky device error word
+// and dispatch to the kernels.  Error handling follows the PhotonInfer
+// README's "Modern C++20 architecture" notes (errors propagate as explicit
+// Result-style values, buffers are used in place without copies): every call
+// returns a status, nothing throws across the boundary, and the library never
+// allocates or copies the caller's data.
+#include <atomic>
+#include <climits>
+#include <cmath>
+#include <cstring>
+
+#include "../../include/photon_paged.h"
+#include "photon_common.cuh"
+
+namespace {
+
+// Sticky device error word, one per device that loads the library.
+__device__ uint32_t g_photon_error_word;
+
+constexpr int kMaxDevices = 64;
+std::atomic<uint32_t*> g_err_ptr[kMaxDevices];
+
+std::atomic<cudaEvent_t> g_ev_start{nullptr};
+std::atomic<cudaEvent_t> g_ev_stop{nullptr};
+
+constexpr int kDefaultPartition = 256;
+constexpr int kMaxPartition = 4096;
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+size_t elem_bytes(int32_t dtype) { return dtype == PHOTON_F32 ? 4u : 2u; }
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Checks shared by every call.  Launches nothing, touches no CUDA state.
+photon_status_t check_shape(const photon_paged_shape_t* s) {
+  if (!s) return PHOTON_ERR_INVALID_ARG;
+  if (s->num_seqs < 0 || s->num_q_heads <= 0 || s->num_kv_heads <= 0 || s->num_blocks < 0 ||
+      s->max_blocks_per_seq <= 0 || s->head_dim <= 0 || s->block_size <= 0)
+    return PHOTON_ERR_INVALID_ARG;
+  if (s->num_q_heads % s->num_kv_heads != 0) return PHOTON_ERR_INVALID_ARG;
+  const int g = s->num_q_heads / s->num_kv_heads;
+  if (g != 1 && g != 2 && g != 4 && g != 8) return PHOTON_ERR_UNSUPPORTED;
+  if (s->head_dim != 64 && s->head_dim != 128) return PHOTON_ERR_UNSUPPORTED;
+  if (s->block_size != photon::kBlockSize) return PHOTON_ERR_UNSUPPORTED;
+  if (s->dtype != PHOTON_F32 && s->dtype != PHOTON_F16 && s->dtype != PHOTON_BF16)
+    return PHOTON_ERR_UNSUPPORTED;
+  if (s->partition_size != 0 &&
+      (s->partition_size < s->block_size || s->partition_size > kMaxPartition ||
+       s->partition_size % s->block_size != 0))
+    return PHOTON_ERR_INVALID_ARG;
+  // Index arithmetic inside the kernels stays in 32-bit for these.
+  if ((int64_t)s->max_blocks_per_seq * s->block_size > INT_MAX / 2) return PHOTON_ERR_UNSUPPORTED;
+  if (s->num_seqs > 65535 || s->num_kv_heads > 65535) return PHOTON_ERR_UNSUPPORTED;
+  return PHOTON_OK;
+}
+
+int partition_of(const photon_paged_shape_t* s) {
+  return s->partition_size ? s->partition_size : kDefaultPartition;
+}
+
+int max_partitions_of(const photon_paged_shape_t* s) {
+  const int64_t span = (int64_t)s->max_blocks_per_seq * s->block_size;
+  const int part = partition_of(s);
+  return (int)((span + part - 1) / part);
+}
+
+struct WorkspaceLayout {
+  size_t off_m, off_l, off_o, total;
+};
+
+WorkspaceLayout layout_of(const photon_paged_shape_t* s) {
+  WorkspaceLayout w{};
+  const size_t rows = (size_t)s->num_seqs * s->num_q_heads * (size_t)max_partitions_of(s);
+  w.off_m = 0;
+  w.off_l = round_up(w.off_m + rows * sizeof(float), 256);
+  w.off_o = round_up(w.off_l + rows * sizeof(float), 256);
+  w.total = round_up(w.off_o + rows * (size_t)s->head_dim * sizeof(float), 256);
+  if (rows == 0) w.total = 0;
+  return w;
+}
+
+// Device address of the error word for the current device.
+photon_status_t error_word(uint32_t** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PHOTON_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return PHOTON_ERR_UNSUPPORTED;
+  uint32_t* p = g_err_ptr[dev].load(std::memory_order_acquire);
+  if (!p) {
+    void* addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_photon_error_word) != cudaSuccess) return PHOTON_ERR_CUDA;
+    p = static_cast<uint32_t*>(addr);
+    g_err_ptr[dev].store(p, std::memory_order_release);
+  }
+  *out = p;
+  return PHOTON_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* photon_status_string(photon_status_t status) {
+  switch (status) {
+    case PHOTON_OK: return "ok";
+    case PHOTON_ERR_INVALID_ARG: return "invalid argument";
+    case PHOTON_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+    case PHOTON_ERR_MISALIGNED: return "buffer not 16-byte aligned";
+    case PHOTON_ERR_WORKSPACE: return "workspace missing or too small";
+    case PHOTON_ERR_CUDA: return "CUDA runtime error";
+    case PHOTON_ERR_DEVICE_BOUNDS: return "device saw an out-of-range index";
+  }
+  return "unknown status";
+}
+
+photon_status_t photon_cache_write(const void* k, const void* v, const int64_t* slot_mapping,
+                                   int32_t num_tokens, void* k_cache, void* v_cache,
+                                   const photon_paged_shape_t* shape, photon_stream_t stream) {
+  photon_status_t st = check_shape(shape);
+  if (st != PHOTON_OK) return st;
+  if (num_tokens < 0) return PHOTON_ERR_INVALID_ARG;
+  if (num_tokens == 0) return PHOTON_OK;
+  if (!k || !v || !slot_mapping || !k_cache || !v_cache) return PHOTON_ERR_INVALID_ARG;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
+    return PHOTON_ERR_MISALIGNED;
+  uint32_t* err = nullptr;
+  if ((st = error_word(&err)) != PHOTON_OK) return st;
+  photon::CacheWriteArgs a{};
+  a.k = k;
+  a.v = v;
+  a.slot_mapping = slot_mapping;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.err = err;
+  a.T = num_tokens;
+  a.Hkv = shape->num_kv_heads;
+  a.row_bytes = (int)(shape->head_dim * elem_bytes(shape->dtype));
+  a.block_size = shape->block_size;
+  a.NB = shape->num_blocks;
+  return photon::launch_cache_write(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PHOTON_OK
+             : PHOTON_ERR_CUDA;
+}
+
+size_t photon_paged_decode_workspace_size(const photon_paged_shape_t* shape) {
+  if (check_shape(shape) != PHOTON_OK) return 0;
+  return layout_of(shape).total;
+}
+
+photon_status_t photon_paged_decode_plan(const photon_paged_shape_t* shape,
+                                         int32_t* partition_size, int32_t* max_partitions,
+                                         int32_t* attention_ctas, int32_t* kernels_per_call) {
+  photon_status_t st = check_shape(shape);
+  if (st != PHOTON_OK) return st;
+  const int pmax = max_partitions_of(shape);
+  if (partition_size) *partition_size = partition_of(shape);
+  if (max_partitions) *max_partitions = pmax;
+  if (attention_ctas) *attention_ctas = pmax * shape->num_kv_heads * shape->num_seqs;
+  if (kernels_per_call) *kernels_per_call = shape->num_seqs == 0 ? 0 : (pmax > 1 ? 2 : 1);
+  return PHOTON_OK;
+}
+
+photon_status_t photon_paged_decode(const void* q, const void* k_cache, const void* v_cache,
+                                    const int32_t* block_tables, const int32_t* context_lens,
+                                    float scale, void* out, void* workspace,
+                                    size_t workspace_bytes, const photon_paged_shape_t* shape,
+                                    photon_stream_t stream) {
+  photon_status_t st = check_shape(shape);
+  if (st != PHOTON_OK) return st;
+  if (!std::isfinite(scale)) return PHOTON_ERR_INVALID_ARG;
+  if (shape->num_seqs == 0) return PHOTON_OK;
+  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
+    return PHOTON_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(block_tables) ||
+      !aligned16(context_lens) || !aligned16(out))
+    return PHOTON_ERR_MISALIGNED;
+  const WorkspaceLayout wl = layout_of(shape);
+  if (wl.total > 0) {
+    if (!workspace || workspace_bytes < wl.total) return PHOTON_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return PHOTON_ERR_MISALIGNED;
+  }
+  uint32_t* err = nullptr;
+  if ((st = error_word(&err)) != PHOTON_OK) return st;
+
+  photon::DecodeArgs a{};
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  a.out = out;
+  char* ws = static_cast<char*>(workspace);
+  a.ws_m = reinterpret_cast<float*>(ws + wl.off_m);
+  a.ws_l = reinterpret_cast<float*>(ws + wl.off_l);
+  a.ws_o = reinterpret_cast<float*>(ws + wl.off_o);
+  a.err = err;
+  a.qscale = (float)((double)scale * 1.4426950408889634);  // scale * log2(e)
+  a.B = shape->num_seqs;
+  a.Hq = shape->num_q_heads;
+  a.Hkv = shape->num_kv_heads;
+  a.D = shape->head_dim;
+  a.NB = shape->num_blocks;
+  a.MBS = shape->max_blocks_per_seq;
+  a.part = partition_of(shape);
+  a.pmax = max_partitions_of(shape);
+  a.ev_start = g_ev_start.load(std::memory_order_acquire);
+  a.ev_stop = g_ev_stop.load(std::memory_order_acquire);
+  if (!a.ev_start || !a.ev_stop) a.ev_start = a.ev_stop = nullptr;
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  switch (shape->dtype) {
+    case PHOTON_F32: e = photon::launch_paged_decode_f32(a, s); break;
+    case PHOTON_F16: e = photon::launch_paged_decode_f16(a, s); break;
+    default: e = photon::launch_paged_decode_bf16(a, s); break;
+  }
+  return e == cudaSuccess ? PHOTON_OK : PHOTON_ERR_CUDA;
+}
+
+photon_status_t photon_paged_gather(const void* k_cache, const void* v_cache,
+                                    const int32_t* block_tables, const int32_t* context_lens,
+                                    void* k_dense, void* v_dense,
+                                    const photon_paged_shape_t* shape, photon_stream_t stream) {
+  photon_status_t st = check_shape(shape);
+  if (st != PHOTON_OK) return st;
+  if (shape->num_seqs == 0) return PHOTON_OK;
+  if (!k_cache || !v_cache || !block_tables || !context_lens || !k_dense || !v_dense)
+    return PHOTON_ERR_INVALID_ARG;
+  if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(block_tables) ||
+      !aligned16(context_lens) || !aligned16(k_dense) || !aligned16(v_dense))
+    return PHOTON_ERR_MISALIGNED;
+  uint32_t* err = nullptr;
+  if ((st = error_word(&err)) != PHOTON_OK) return st;
+  photon::GatherArgs a{};
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  a.k_dense = k_dense;
+  a.v_dense = v_dense;
+  a.err = err;
+  a.B = shape->num_seqs;
+  a.Hkv = shape->num_kv_heads;
+  a.row_bytes = (int)(shape->head_dim * elem_bytes(shape->dtype));
+  a.block_size = shape->block_size;
+  a.NB = shape->num_blocks;
+  a.MBS = shape->max_blocks_per_seq;
+  return photon::launch_gather(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PHOTON_OK
+             : PHOTON_ERR_CUDA;
+}
+
+photon_status_t photon_get_last_device_error(photon_stream_t stream, uint32_t* bits) {
+  if (cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return PHOTON_ERR_CUDA;
+  uint32_t word = 0;
+  const uint32_t zero = 0;
+  if (cudaMemcpyFromSymbol(&word, g_photon_error_word, sizeof(word)) != cudaSuccess ||
+      cudaMemcpyToSymbol(g_photon_error_word, &zero, sizeof(zero)) != cudaSuccess)
+    return PHOTON_ERR_CUDA;
+  if (bits) *bits = word;
+  return word ? PHOTON_ERR_DEVICE_BOUNDS : PHOTON_OK;
+}
+
+photon_status_t photon_debug_set_attention_events(void* start_event, void* stop_event) {
+  if ((start_event == nullptr) != (stop_event == nullptr)) return PHOTON_ERR_INVALID_ARG;
+  g_ev_start.store(static_cast<cudaEvent_t>(start_event), std::memory_order_release);
+  g_ev_stop.store(static_cast<cudaEvent_t>(stop_event), std::memory_order_release);
+  return PHOTON_OK;
+}
+
+}  // extern "C"

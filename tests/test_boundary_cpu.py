@@ -1,0 +1,111 @@
+"""Host-side checks of the C-ABI library: it builds, loads, exports every
+symbol the header declares, and rejects bad arguments with the documented
+status before touching CUDA.  Needs no GPU."""
+import ctypes
+import math
+
+import pytest
+
+import paged_kv_attention_photon_gb300 as P
+
+
+@pytest.fixture(scope="module")
+def lib():
+    P.build()
+    return P._load()
+
+
+def _shape(**over):
+    base = dict(num_seqs=4, num_q_heads=16, num_kv_heads=8, head_dim=128, block_size=16,
+                num_blocks=100, max_blocks_per_seq=8, dtype=P.F16, partition_size=0)
+    base.update(over)
+    return P.PagedShape.make(**base)
+
+
+FAKE = 0x10000          # aligned non-null "device" addresses: never dereferenced,
+FAKE2 = 0x20000         # every case below fails validation before any launch
+
+
+def test_exports_every_declared_symbol(lib):
+    names = P.exported_symbols()
+    assert {"photon_cache_write", "photon_paged_decode", "photon_paged_decode_workspace_size",
+            "photon_paged_gather", "photon_get_last_device_error",
+            "photon_status_string"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for code in range(7):
+        assert P.photon_status_string(code) not in ("", "unknown status")
+    assert P.photon_status_string(99) == "unknown status"
+
+
+def _decode_status(shape, *, q=FAKE, kc=FAKE, vc=FAKE, bt=FAKE, cl=FAKE, out=FAKE2,
+                   ws=FAKE2, ws_bytes=1 << 40, scale=0.1):
+    return P._load().photon_paged_decode(q, kc, vc, bt, cl, scale, out, ws, ws_bytes,
+                                         ctypes.byref(shape), None)
+
+
+def test_decode_validation(lib):
+    ok = _shape()
+    assert _decode_status(_shape(num_q_heads=12)) == 1          # Hq % Hkv != 0
+    assert _decode_status(_shape(num_q_heads=24, num_kv_heads=8)) == 2   # group 3
+    assert _decode_status(_shape(head_dim=96)) == 2
+    assert _decode_status(_shape(block_size=32)) == 2
+    assert _decode_status(_shape(dtype=7)) == 2
+    assert _decode_status(_shape(partition_size=24)) == 1
+    assert _decode_status(_shape(partition_size=8192)) == 1
+    assert _decode_status(_shape(num_seqs=-1)) == 1
+    assert _decode_status(ok, q=None) == 1
+    assert _decode_status(ok, out=None) == 1
+    assert _decode_status(ok, q=FAKE + 8) == 3
+    assert _decode_status(ok, bt=FAKE + 4) == 3
+    assert _decode_status(ok, ws=None) == 4
+    assert _decode_status(ok, ws_bytes=16) == 4
+    assert _decode_status(ok, scale=math.nan) == 1
+    assert _decode_status(ok, scale=math.inf) == 1
+    assert lib.photon_paged_decode(None, None, None, None, None, 0.1, None, None, 0, None,
+                                   None) == 1
+    # an empty batch is a no-op, whatever the pointers
+    assert _decode_status(_shape(num_seqs=0), q=None, out=None, ws=None, ws_bytes=0) == 0
+
+
+def test_cache_write_validation(lib):
+    s = _shape()
+    f = lib.photon_cache_write
+    assert f(FAKE, FAKE, FAKE, 0, FAKE, FAKE, ctypes.byref(s), None) == 0     # no rows: no-op
+    assert f(FAKE, FAKE, FAKE, -1, FAKE, FAKE, ctypes.byref(s), None) == 1
+    assert f(None, FAKE, FAKE, 4, FAKE, FAKE, ctypes.byref(s), None) == 1
+    assert f(FAKE, FAKE, FAKE + 4, 4, FAKE, FAKE, ctypes.byref(s), None) == 3
+    assert f(FAKE, FAKE + 8, FAKE, 4, FAKE, FAKE, ctypes.byref(s), None) == 3
+    assert f(FAKE, FAKE, FAKE, 4, FAKE, FAKE, ctypes.byref(_shape(head_dim=80)), None) == 2
+
+
+def test_gather_validation(lib):
+    s = _shape()
+    f = lib.photon_paged_gather
+    assert f(FAKE, FAKE, FAKE, FAKE, None, FAKE, ctypes.byref(s), None) == 1
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE + 2, FAKE, ctypes.byref(s), None) == 3
+    assert f(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.byref(_shape(num_seqs=0)), None) == 0
+
+
+def test_workspace_size_and_plan(lib):
+    s = _shape(num_seqs=64, max_blocks_per_seq=512, partition_size=256)
+    pl = P.photon_paged_decode_plan(s)
+    assert pl["partition_size"] == 256 and pl["max_partitions"] == 32
+    ws = P.photon_paged_decode_workspace_size(s)
+    rows = 64 * 16 * 32
+    assert ws >= rows * (128 + 2) * 4
+    assert ws % 256 == 0
+    assert P.photon_paged_decode_workspace_size(_shape(head_dim=96)) == 0
+    assert P.photon_paged_decode_workspace_size(_shape(num_seqs=0)) == 0
+    d = P.photon_paged_decode_plan(_shape())
+    assert d["partition_size"] > 0 and d["partition_size"] % 16 == 0
+    with pytest.raises(P.PhotonError):
+        P.photon_paged_decode_plan(_shape(num_q_heads=3))
+
+
+def test_events_hook_argument_check(lib):
+    assert lib.photon_debug_set_attention_events(FAKE, None) == 1
+    assert lib.photon_debug_set_attention_events(None, None) == 0
