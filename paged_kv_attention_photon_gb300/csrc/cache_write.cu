@@ -13,6 +13,8 @@ namespace photon {
 namespace {
 
 __global__ void __launch_bounds__(256) cache_write_kernel(CacheWriteArgs a) {
+  pdl_launch_dependents();  // a PDL-launched successor may start its prologue
+  pdl_wait_primary();       // inputs may come from the previous kernel in the stream
   const int cpr = a.row_bytes >> 4;                    // 16-byte chunks per row
   const int64_t total = (int64_t)a.T * a.Hkv * 2 * cpr;
   const int64_t nslots = (int64_t)a.NB * a.block_size;
@@ -84,8 +86,7 @@ int grid_for(int64_t total, int threads) {
 cudaError_t launch_cache_write(const CacheWriteArgs& a, cudaStream_t stream) {
   const int64_t total = (int64_t)a.T * a.Hkv * 2 * (a.row_bytes >> 4);
   if (total == 0) return cudaSuccess;
-  cache_write_kernel<<<grid_for(total, 256), 256, 0, stream>>>(a);
-  return cudaGetLastError();
+  return launch_pdl(cache_write_kernel, dim3(grid_for(total, 256)), dim3(256), 0, stream, a);
 }
 
 cudaError_t launch_gather(const GatherArgs& a, cudaStream_t stream) {

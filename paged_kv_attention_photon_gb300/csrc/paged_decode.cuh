@@ -5,31 +5,52 @@
 // stable way, 128-bit vectorised loads; "Technical details / Paged attention":
 // per-sequence cache offsets (here: block tables).
 //
-// Work decomposition.  The context [0, ctx_b) of sequence b is cut into
-// partitions of `part` tokens (a multiple of the 16-token block).  One CTA
-// owns one (partition, KV head, sequence) and computes, for the G query heads
-// that share the KV head (GQA), the running max m, the weight sum l and the
-// unnormalised weighted sum of V over its tokens.  A sequence with a single
-// partition writes its output row directly; longer ones leave (m, l, o) in
-// the workspace and the merge kernel combines them by their log-sum-exp
-// weights:  M = max_p m_p,  out = sum_p 2^(m_p-M) o_p / sum_p 2^(m_p-M) l_p.
+// Two launches per call, chained with programmatic dependent launch so each
+// one's start-up overlaps its predecessor:
+//   1. attention: a persistent grid that fills every SM.  Work items are
+//      (sequence, partition, KV head); split-KV partitioning cuts each context
+//      into ceil(ctx / part) partitions, so long sequences give many items and
+//      short ones few.  In each CTA one producer warp derives its items from
+//      context_lens and streams the K and V chunks of
+//      the blocks they name from the pool into a ring of shared-memory stages
+//      with 1-D bulk copies (cp.async.bulk, completion on an mbarrier); the
+//      consumer warps compute scores, an online softmax and the weighted V sum
+//      from shared memory.  A block's rows for one KV head are one contiguous
+//      chunk of the pool ([num_blocks][Hkv][16][d]), so every copy is a single
+//      16-byte-aligned run of 16*d elements.  A sequence with one partition
+//      writes its output row directly; a longer one leaves (m, l, o) per
+//      partition in the workspace;
+//   2. merge: out = sum_p 2^(m_p - M) o_p / sum_p 2^(m_p - M) l_p with
+//      M = max_p m_p, for every (sequence, q head) with two or more partitions,
+//      and the zero rows of empty sequences.
+//      (Merging inside the attention kernel, by the CTA that finishes a
+//      sequence's last partition, needs a device-scope fence per partition;
+//      under a full HBM stream those fences and the serialised merges cost far
+//      more than this short kernel.)
 //
-// Inside a CTA each warp takes whole 16-token blocks (blocks w, w+4, ...).
-// A block's K (and V) rows for one KV head are one contiguous chunk of the
-// pool.  Eight lanes cover one token row with 16-byte loads (a quarter-warp
-// reads 128 contiguous bytes), so a warp holds four rows per load step and
-// four steps cover the block.  Scores are reduced across the eight lanes of a
-// row with three xor-shuffles; each loaded K/V element is reused by all G
-// heads from registers.  The softmax is the online form: per block the warp
-// takes the block maximum, rescales its running (l, o) by 2^(m_old - m_new)
-// and accumulates 2^(s - m_new).  Scores are kept in the log2 domain (q is
-// pre-multiplied by scale * log2 e), so exp is one exp2f.
+// Consumer arithmetic.  Each consumer warp takes one 16-token block of a stage.
+// Eight lanes cover one token row with 16-byte shared-memory loads (a quarter
+// warp reads 128 contiguous bytes: no bank conflicts), four rows per load step,
+// four steps per block.  A lane keeps its slice of the G query rows of the KV
+// head's group (GQA) in registers, pre-multiplied by scale*log2(e), so every
+// loaded K/V element serves all G heads and exp is one exp2f.  Scores are
+// summed over the eight lanes of a row with three xor-shuffles.  The softmax is
+// the online form: per block the warp takes the block maximum, rescales its
+// running (l, o) by 2^(m_old - m_new) and accumulates 2^(s - m_new) and
+// 2^(s - m_new) * V.  At the end of an item the warps' states are combined
+// through shared memory by the same log-sum-exp rule.
 #pragma once
 
 #include <float.h>
 #include <math.h>
 
 #include "photon_common.cuh"
+
+// PHOTON_FAST_EXP selects the PTX ex2.approx.ftz instruction for the softmax
+// weights instead of the exp2f library call (a tuning knob; off by default).
+#ifndef PHOTON_FAST_EXP
+#define PHOTON_FAST_EXP 0
+#endif
 
 namespace photon {
 
@@ -45,102 +66,82 @@ struct DecodeCfg {
   static_assert(kRowChunks % kLanesPerRow == 0, "row must split over 8 lanes");
 };
 
-template <typename T, int D, int G>
-__global__ void __launch_bounds__(kDecodeWarps * 32)
-    paged_decode_split_kernel(const DecodeArgs a) {
+__device__ __forceinline__ float softmax_exp2(float x) {
+#if PHOTON_FAST_EXP
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+#else
+  return exp2f(x);
+#endif
+}
+
+// Stage header written by the producer, read by the consumers after the
+// stage's full barrier completes.
+struct StageHdr {
+  int b, kvh, p, nparts;
+  int tok_end, blk0;   // exclusive token end of the item; first logical block of the stage
+  int nblk;            // blocks carried by this stage (<= consumer warps)
+  int flags;           // kFirst | kLast | kDone, valid-block mask << 8
+};
+enum : int { kFirst = 1, kLast = 2, kDone = 4 };
+
+// Runs of the work list: the full partitions, then up to log2(4096/16) + 1 = 9
+// classes of tail partitions.
+constexpr int kMaxRuns = 10;
+
+// Persistent-kernel geometry: NC consumer warps, 1 producer warp, S ring stages.
+template <typename T, int D, int G, int NC, int S>
+struct PersistCfg {
   using C = DecodeCfg<T, D, G>;
-  constexpr int NW = kDecodeWarps;
-  const int p = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  static constexpr int kThreads = (NC + 1) * 32;
+  static constexpr int kBlockElems = kBlockSize * D;
+  static constexpr int kBlockBytes = kBlockElems * (int)sizeof(T);
+  static constexpr int kQBytes = G * D * (int)sizeof(T);
+  static constexpr int kQStride = (kQBytes + 127) / 128 * 128;
+  static constexpr int kStageBytes = 2 * NC * kBlockBytes;     // K blocks, then V blocks
+  static constexpr int kOffFull = 0;
+  static constexpr int kOffEmpty = kOffFull + 8 * S;
+  static constexpr int kOffSync = kOffEmpty + 8 * S;
+  static constexpr int kOffAbort = kOffSync + 8;
+  static constexpr int kOffRuns = kOffAbort + 4;                        // int[kMaxRuns + 1]
+  static constexpr int kOffHdr = (kOffRuns + 4 * (kMaxRuns + 1) + 15) / 16 * 16;
+  static constexpr int kOffQ = (kOffHdr + (int)sizeof(StageHdr) * S + 127) / 128 * 128;
+  static constexpr int kOffKV = kOffQ + kQStride * S;
+  static constexpr int kOffPm = kOffKV + kStageBytes * S;       // float[NC][G]
+  static constexpr int kOffPl = kOffPm + 4 * NC * G;            // float[NC][G]
+  static constexpr int kOffPo = (kOffPl + 4 * NC * G + 15) / 16 * 16;   // float[NC][G][D]
+  static constexpr int kSmemBytes = kOffPo + 4 * NC * G * D;
+};
+
+// ------------------------------------------------------------------ consumer math
+// Process one 16-token block held in shared memory (ks: K rows, vs: V rows,
+// row-major [16][D]); rows >= n_valid are masked.
+template <typename T, int D, int G>
+__device__ __forceinline__ void attend_block(const T* __restrict__ ks, const T* __restrict__ vs,
+                                             int n_valid, const float (&qf)[G][DecodeCfg<T, D, G>::kEPL],
+                                             float (&m)[G], float (&l)[G],
+                                             float (&o)[G][DecodeCfg<T, D, G>::kEPL], int lane) {
+  using C = DecodeCfg<T, D, G>;
   const int c = lane & 7, tg = lane >> 3;
-
-  __shared__ float sm_m[NW][G], sm_l[NW][G];
-  __shared__ __align__(16) float sm_o[NW][G][D];
-
-  const int ctx = __ldg(a.context_lens + b);
-  const int span = a.MBS * kBlockSize;
-  const bool bad_ctx = ctx < 0 || ctx > span;
-  const int nparts = bad_ctx ? 0 : (ctx + a.part - 1) / a.part;
-  if (nparts == 0) {
-    // Empty (or rejected) context: the output row is zero.
-    if (p == 0) {
-      if (bad_ctx && kvh == 0 && threadIdx.x == 0) raise_error(a.err, kErrContext);
-      T* out = static_cast<T*>(a.out) + ((size_t)b * a.Hq + (size_t)kvh * G) * D;
-      for (int i = threadIdx.x; i < G * D; i += blockDim.x) out[i] = Elem<T>::narrow(0.f);
-    }
-    return;
-  }
-  if (p >= nparts) return;
-
-  const int tok_begin = p * a.part;
-  const int tok_end = min(ctx, tok_begin + a.part);
-  const int blk_begin = tok_begin / kBlockSize;
-  const int blk_end = (tok_end + kBlockSize - 1) / kBlockSize;
-
-  // q rows of the G heads of this group; each lane keeps its own elements,
-  // pre-scaled into the log2 domain.
-  float qf[G][C::kEPL];
+  float sc[C::kSteps][G];
   {
-    const T* qb = static_cast<const T*>(a.q) + ((size_t)b * a.Hq + (size_t)kvh * G) * D;
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-#pragma unroll
-      for (int i = 0; i < C::kPPL; ++i) {
-        const uint4 raw =
-            *reinterpret_cast<const uint4*>(qb + (size_t)g * D + (c + 8 * i) * C::kChunk);
-        float t[C::kChunk];
-        Elem<T>::widen(raw, t);
-#pragma unroll
-        for (int e = 0; e < C::kChunk; ++e) qf[g][i * C::kChunk + e] = t[e] * a.qscale;
-      }
-    }
-  }
-
-  float m[G], l[G], o[G][C::kEPL];
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-    m[g] = -INFINITY;
-    l[g] = 0.f;
-#pragma unroll
-    for (int e = 0; e < C::kEPL; ++e) o[g][e] = 0.f;
-  }
-
-  const T* kpool = static_cast<const T*>(a.k_cache);
-  const T* vpool = static_cast<const T*>(a.v_cache);
-  const int32_t* table = a.block_tables + (size_t)b * a.MBS;
-
-  for (int blk = blk_begin + warp; blk < blk_end; blk += NW) {
-    const int phys = __ldg(table + blk);
-    if (phys < 0 || phys >= a.NB) {
-      if (lane == 0) raise_error(a.err, kErrBlock);
-      continue;  // the block's tokens are treated as absent
-    }
-    const int n_valid = min(kBlockSize, tok_end - blk * kBlockSize);
-    const size_t chunk = ((size_t)phys * a.Hkv + kvh) * (size_t)(kBlockSize * D);
-
-    uint4 kr[C::kSteps][C::kPPL], vr[C::kSteps][C::kPPL];
+    uint4 kr[C::kSteps][C::kPPL];
 #pragma unroll
     for (int s = 0; s < C::kSteps; ++s) {
       const int row = s * C::kRowsPerStep + tg;
 #pragma unroll
-      for (int i = 0; i < C::kPPL; ++i) {
-        const size_t off = chunk + (size_t)row * D + (c + 8 * i) * C::kChunk;
-        if (row < n_valid) {
-          kr[s][i] = ld_stream16(kpool + off);
-          vr[s][i] = ld_stream16(vpool + off);
-        } else {
-          kr[s][i] = make_uint4(0, 0, 0, 0);
-          vr[s][i] = make_uint4(0, 0, 0, 0);
-        }
-      }
+      for (int i = 0; i < C::kPPL; ++i)
+        kr[s][i] = row < n_valid
+                       ? *reinterpret_cast<const uint4*>(ks + row * D + (c + 8 * i) * C::kChunk)
+                       : make_uint4(0, 0, 0, 0);
     }
-
-    float sc[C::kSteps][G];
 #pragma unroll
     for (int s = 0; s < C::kSteps; ++s) {
       float kf[C::kEPL];
 #pragma unroll
       for (int i = 0; i < C::kPPL; ++i) Elem<T>::widen(kr[s][i], kf + i * C::kChunk);
+      const int row = s * C::kRowsPerStep + tg;
 #pragma unroll
       for (int g = 0; g < G; ++g) {
         float acc = 0.f;
@@ -149,153 +150,637 @@ __global__ void __launch_bounds__(kDecodeWarps * 32)
         acc += __shfl_xor_sync(0xffffffffu, acc, 1);
         acc += __shfl_xor_sync(0xffffffffu, acc, 2);
         acc += __shfl_xor_sync(0xffffffffu, acc, 4);
-        const int row = s * C::kRowsPerStep + tg;
         sc[s][g] = row < n_valid ? acc : -INFINITY;
       }
     }
-
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      float mx = sc[0][g];
-#pragma unroll
-      for (int s = 1; s < C::kSteps; ++s) mx = fmaxf(mx, sc[s][g]);
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-      const float mnew = fmaxf(m[g], mx);
-      if (mnew > m[g]) {  // warp-uniform: m and mx are identical on all lanes
-        const float corr = exp2f(m[g] - mnew);
-        l[g] *= corr;
-#pragma unroll
-        for (int e = 0; e < C::kEPL; ++e) o[g][e] *= corr;
-        m[g] = mnew;
-      }
-    }
-
-#pragma unroll
-    for (int s = 0; s < C::kSteps; ++s) {
-      float vf[C::kEPL];
-#pragma unroll
-      for (int i = 0; i < C::kPPL; ++i) Elem<T>::widen(vr[s][i], vf + i * C::kChunk);
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        const float pw = exp2f(sc[s][g] - m[g]);
-        l[g] += pw;
-#pragma unroll
-        for (int e = 0; e < C::kEPL; ++e) o[g][e] = fmaf(pw, vf[e], o[g][e]);
-      }
-    }
   }
-
-  // Sum over the four row groups of the warp (lanes with the same c).
 #pragma unroll
   for (int g = 0; g < G; ++g) {
-    l[g] += __shfl_xor_sync(0xffffffffu, l[g], 8);
-    l[g] += __shfl_xor_sync(0xffffffffu, l[g], 16);
+    float mx = sc[0][g];
 #pragma unroll
-    for (int e = 0; e < C::kEPL; ++e) {
-      o[g][e] += __shfl_xor_sync(0xffffffffu, o[g][e], 8);
-      o[g][e] += __shfl_xor_sync(0xffffffffu, o[g][e], 16);
+    for (int s = 1; s < C::kSteps; ++s) mx = fmaxf(mx, sc[s][g]);
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+    if (mx > m[g]) {  // warp-uniform: m and mx agree on all lanes
+      const float corr = softmax_exp2(m[g] - mx);
+      l[g] *= corr;
+#pragma unroll
+      for (int e = 0; e < C::kEPL; ++e) o[g][e] *= corr;
+      m[g] = mx;
     }
   }
-  if (tg == 0) {
+  uint4 vr[C::kSteps][C::kPPL];
+#pragma unroll
+  for (int s = 0; s < C::kSteps; ++s) {
+    const int row = s * C::kRowsPerStep + tg;
+#pragma unroll
+    for (int i = 0; i < C::kPPL; ++i)
+      vr[s][i] = row < n_valid
+                     ? *reinterpret_cast<const uint4*>(vs + row * D + (c + 8 * i) * C::kChunk)
+                     : make_uint4(0, 0, 0, 0);
+  }
+#pragma unroll
+  for (int s = 0; s < C::kSteps; ++s) {
+    float vf[C::kEPL];
+#pragma unroll
+    for (int i = 0; i < C::kPPL; ++i) Elem<T>::widen(vr[s][i], vf + i * C::kChunk);
 #pragma unroll
     for (int g = 0; g < G; ++g) {
+      const float pw = softmax_exp2(sc[s][g] - m[g]);   // 0 for masked rows
+      l[g] += pw;
 #pragma unroll
-      for (int i = 0; i < C::kPPL; ++i)
-#pragma unroll
-        for (int e = 0; e < C::kChunk; ++e)
-          sm_o[warp][g][(c + 8 * i) * C::kChunk + e] = o[g][i * C::kChunk + e];
-      if (c == 0) {
-        sm_m[warp][g] = m[g];
-        sm_l[warp][g] = l[g];
-      }
-    }
-  }
-  __syncthreads();
-
-  // Combine the warps' partial states.
-  for (int idx = threadIdx.x; idx < G * D; idx += blockDim.x) {
-    const int g = idx / D, e = idx % D;
-    float M = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < NW; ++w)
-      if (sm_l[w][g] > 0.f) M = fmaxf(M, sm_m[w][g]);
-    float L = 0.f, O = 0.f;
-#pragma unroll
-    for (int w = 0; w < NW; ++w) {
-      if (sm_l[w][g] > 0.f) {
-        const float wt = exp2f(sm_m[w][g] - M);
-        L = fmaf(wt, sm_l[w][g], L);
-        O = fmaf(wt, sm_o[w][g][e], O);
-      }
-    }
-    const int h = kvh * G + g;
-    if (nparts == 1) {
-      T* out = static_cast<T*>(a.out) + ((size_t)b * a.Hq + h) * D;
-      out[e] = Elem<T>::narrow(L > 0.f ? O / L : 0.f);
-    } else {
-      const size_t row = ((size_t)b * a.Hq + h) * a.pmax + p;
-      a.ws_o[row * D + e] = O;
-      if (e == 0) {
-        a.ws_m[row] = M;
-        a.ws_l[row] = L;
-      }
+      for (int e = 0; e < C::kEPL; ++e) o[g][e] = fmaf(pw, vf[e], o[g][e]);
     }
   }
 }
 
-// One warp per (sequence, q head): combine the partitions' (m, l, o).
+// Arrive-and-wait of the NC consumer warps on `bar` (bounded).
+__device__ __forceinline__ bool consumer_sync(uint64_t* bar, uint32_t& phase, int lane) {
+  __syncwarp();
+  if (lane == 0) mbar_arrive(bar);
+  const bool ok = mbar_wait_bounded(bar, phase);
+  phase ^= 1u;
+  return ok;
+}
+
+#ifdef PHOTON_PROBE
+// Per-CTA timeline for tuning builds only (never compiled into the library by
+// default): [0] start, [1] first stage issued, [2] producer done, [3] first
+// stage consumed, [4] consumers done, [7] items.
+constexpr int kProbeCtas = 1024;
+constexpr int kProbeSlots = 48;  // [8 + 2k]: item k's first copy issued, [9 + 2k]: item k combined
+static __device__ unsigned long long g_probe[kProbeCtas][kProbeSlots];
+#define PROBE_SET(i, v) \
+  do { if (blockIdx.x < kProbeCtas && (i) < kProbeSlots) g_probe[blockIdx.x][i] = (v); } while (0)
+#else
+#define PROBE_SET(i, v) do { } while (0)
+#endif
+
+// ------------------------------------------------------------------ attention kernel
+template <typename T, int D, int G, int NC, int S>
+__global__ void __launch_bounds__((NC + 1) * 32, 1)
+    paged_decode_attention_kernel(const DecodeArgs a) {
+  using PC = PersistCfg<T, D, G, NC, S>;
+  using C = DecodeCfg<T, D, G>;
+  extern __shared__ __align__(128) unsigned char smem[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + PC::kOffFull);
+  uint64_t* empty = reinterpret_cast<uint64_t*>(smem + PC::kOffEmpty);
+  uint64_t* sync = reinterpret_cast<uint64_t*>(smem + PC::kOffSync);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + PC::kOffAbort);
+  StageHdr* hdr = reinterpret_cast<StageHdr*>(smem + PC::kOffHdr);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], NC);
+    }
+    mbar_init(sync, NC);
+    *abort_flag = 0;
+    mbar_init_fence();
+  }
+  __syncthreads();
+  // Everything below may read what the previous kernel in the stream wrote
+  // (the cache write's rows, context lengths, block tables, q).
+  pdl_wait_primary();
+  // The merge kernel may be scheduled as CTAs retire; it waits for this grid.
+  pdl_launch_dependents();
+
+  // Number of full partitions over the batch, counted by the whole CTA.
+  const int span = a.MBS * kBlockSize;
+  auto ctx_of = [&](int b) -> int {
+    const int c = b < a.B ? __ldg(a.context_lens + b) : 0;
+    return (c < 0 || c > span) ? 0 : c;  // rejected lengths count as empty
+  };
+  // Run sizes of the work list, counted by the whole CTA: run 0 holds the
+  // full partitions, run 1 + k the tail partitions of class k, where a tail of
+  // nb blocks (of P16 = part / 16 per partition) has class
+  // floor(log2(floor(P16 / nb))): halves of the partition size, largest first.
+  const int P16 = a.part / kBlockSize;
+  const int nclass = 32 - __clz(P16);  // classes 0 .. log2(P16)
+  auto tail_class = [&](int ctxv) -> int {
+    const int tail = ctxv % a.part;
+    if (!tail) return -1;
+    const int nb = (tail + kBlockSize - 1) / kBlockSize;
+    return 31 - __clz(P16 / nb);
+  };
+  int* run_start = reinterpret_cast<int*>(smem + PC::kOffRuns);  // pairs before run r
+  bool dynamic = false;
+  {
+    int cnt[kMaxRuns];
+#pragma unroll
+    for (int r = 0; r < kMaxRuns; ++r) cnt[r] = 0;
+    for (int b = threadIdx.x; b < a.B; b += PC::kThreads) {
+      const int c = ctx_of(b);
+      cnt[0] += c / a.part;
+      const int k = tail_class(c);
+#pragma unroll
+      for (int r = 1; r < kMaxRuns; ++r) cnt[r] += (k == r - 1) ? 1 : 0;
+    }
+    int* red = reinterpret_cast<int*>(smem + PC::kOffPo);  // scratch until the first item ends
+#pragma unroll
+    for (int r = 0; r < kMaxRuns; ++r) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) cnt[r] += __shfl_xor_sync(0xffffffffu, cnt[r], o);
+      if (lane == 0) red[r * (NC + 1) + warp] = cnt[r];
+    }
+    if (threadIdx.x == 0) red[kMaxRuns * (NC + 1)] = a.ws_ctrl[0] == kQueueReady ? 1 : 0;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      int acc = 0;
+      for (int r = 0; r < kMaxRuns; ++r) {
+        run_start[r] = acc;
+        for (int w = 0; w < NC + 1; ++w) acc += red[r * (NC + 1) + w];
+      }
+      run_start[kMaxRuns] = acc;
+    }
+    dynamic = red[kMaxRuns * (NC + 1)] != 0;
+    __syncthreads();
+  }
+  (void)nclass;
+
+  auto fail = [&](void) {
+    if (lane == 0) {
+      raise_error(a.err, kErrTimeout);
+      *abort_flag = 1;
+    }
+  };
+
+  if (warp == NC) {
+    // ================================================================ producer
+    // Work list, derived here from context_lens with no planning kernel.  The
+    // (sequence, partition) pairs come in runs -- first every full partition
+    // (sequence order, then partition order), then the partial tail
+    // partitions, class by class from the longest to the shortest -- so the
+    // items handed out last are the smallest (longest-processing-time first,
+    // without a sort).  Each pair is expanded over the KV heads
+    // (item = pair * Hkv + kvh).  The warp keeps a
+    // window of 32 sequences (lane j: sequence wb + j's context length, its
+    // pair count in the current run and the pairs before it) and slides it
+    // forward as its items advance, with the next window's lengths already
+    // loaded.  A three-deep software pipeline keeps every round trip off the
+    // copy stream: while item i's stages are issued, the block-table slice of
+    // item i+1 is in flight and item i+2 is located.
+    PROBE_SET(0, global_timer_ns());
+    const T* kpool = static_cast<const T*>(a.k_cache);
+    const T* vpool = static_cast<const T*>(a.v_cache);
+    const T* qbase = static_cast<const T*>(a.q);
+    uint32_t st = 0;
+    bool aborted = false;
+    int items_done = 0;
+
+    int run = 0;  // 0: full partitions, 1 + k: tail partitions of class k
+    int wb = 0, wbase = 0, w_ctx = 0, w_np = 0, w_excl = 0, w_tot = 0;
+    auto set_window = [&](int ctxv) {
+      w_ctx = ctxv;
+      w_np = run == 0 ? ctxv / a.part : (tail_class(ctxv) == run - 1 ? 1 : 0);
+      int incl = w_np;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      w_excl = incl - w_np;
+      w_tot = __shfl_sync(0xffffffffu, incl, 31);
+    };
+    // The first two windows stay in registers: a batch of up to 64 sequences
+    // never reloads context lengths when a new run starts.
+    const int ctx_w0 = ctx_of(lane), ctx_w1 = ctx_of(32 + lane);
+    set_window(ctx_w0);
+    int pre_ctx = ctx_w1;
+    // (sequence, partition) of pair index `pair`; false past the last pair.
+    // Pairs must be asked for in nondecreasing order.
+    auto locate = [&](int pair, WorkItem& it) -> bool {
+      if (pair >= run_start[kMaxRuns]) return false;
+      if (pair >= run_start[run + 1]) {
+        do {
+          ++run;
+        } while (pair >= run_start[run + 1]);
+        wb = 0;
+        wbase = 0;
+        set_window(ctx_w0);
+        pre_ctx = ctx_w1;
+      }
+      const int q = pair - run_start[run];
+      while (q >= wbase + w_tot) {
+        if (wb + 32 >= a.B) return false;  // never walks past the batch
+        wbase += w_tot;
+        wb += 32;
+        set_window(pre_ctx);
+        pre_ctx = wb + 32 < 64 ? ctx_w1 : ctx_of(wb + 32 + lane);
+      }
+      const int rel = q - wbase;
+      // lanes with excl <= rel form a prefix; the last of them owns the pair
+      const int j = 31 - __clz(__ballot_sync(0xffffffffu, w_excl <= rel));
+      const int excl = __shfl_sync(0xffffffffu, w_excl, j);
+      const int ctxj = __shfl_sync(0xffffffffu, w_ctx, j);
+      const int nfull = ctxj / a.part;
+      it.b = wb + j;
+      it.p = run == 0 ? rel - excl : nfull;
+      it.tok_end = run == 0 ? (it.p + 1) * a.part : ctxj;
+      it.nparts = nfull + (ctxj % a.part != 0 ? 1 : 0);
+      return true;
+    };
+    // Lane j holds the physical block of logical block (chunk*32 + j) of the item.
+    auto load_table = [&](const WorkItem& it, int chunk) -> int {
+      const int blk0 = it.p * (a.part / kBlockSize);
+      const int nblk = (it.tok_end - it.p * a.part + kBlockSize - 1) / kBlockSize;
+      const int j = chunk * 32 + lane;
+      return j < nblk ? __ldg(a.block_tables + (size_t)it.b * a.MBS + blk0 + j) : -1;
+    };
+
+    // The first two items of every CTA are fixed (c and c + N); after that a
+    // clean queue hands out 2N, 2N + 1, ... in the order CTAs ask (so a CTA
+    // on a faster path takes more), and a fresh workspace falls back to the
+    // fixed stride.  Each CTA's indices increase, as locate() requires.
+    const int N = gridDim.x;
+    unsigned long long* queue = a.ws_ctrl + 1;
+    int next_static = blockIdx.x + 2 * N;
+    auto grab = [&]() -> int {  // value valid in lane 0 (dynamic) or all lanes (static)
+      if (!dynamic) {
+        const int v = next_static;
+        next_static += N;
+        return v;
+      }
+      return lane == 0 ? 2 * N + (int)atomicAdd(queue, 1ull) : 0;
+    };
+    auto bcast = [&](int raw) -> int { return dynamic ? __shfl_sync(0xffffffffu, raw, 0) : raw; };
+    int g0 = blockIdx.x, g1 = g0 + N;
+    int g2raw = grab();
+    WorkItem it0{}, it1{};
+    bool v0 = locate(g0 / a.Hkv, it0);
+    bool v1 = v0 && locate(g1 / a.Hkv, it1);
+    int tb0 = v0 ? load_table(it0, 0) : -1;
+    while (v0 && !aborted) {
+      const int g2 = bcast(g2raw);
+      g2raw = grab();
+      WorkItem it2{};
+      const bool v2 = v1 && locate(g2 / a.Hkv, it2);
+      const int tb1 = v1 ? load_table(it1, 0) : -1;
+
+      const int kvh = g0 % a.Hkv;
+      const int tok_begin = it0.p * a.part;
+      const int blk0 = tok_begin / kBlockSize;
+      const int nblk = (it0.tok_end - tok_begin + kBlockSize - 1) / kBlockSize;
+      const size_t head_off = (size_t)kvh * PC::kBlockElems;
+      int tb = tb0, chunk = 0;
+      for (int k0 = 0; k0 < nblk; k0 += NC) {
+        if (k0 >= 32 * (chunk + 1)) tb = load_table(it0, ++chunk);
+        const int slot = st % S;
+        const uint32_t ph = (st / S) & 1u;
+        bool ok_wait = true;
+        if (lane == 0) ok_wait = mbar_wait_bounded(&empty[slot], ph ^ 1u);
+        if (!__shfl_sync(0xffffffffu, ok_wait ? 1 : 0, 0)) {
+          fail();
+          aborted = true;
+          break;
+        }
+        const int nb = min(NC, nblk - k0);
+        const int phys = __shfl_sync(0xffffffffu, tb, (k0 + lane) & 31);
+        const int tok = (blk0 + k0 + lane) * kBlockSize;
+        const int rows = min(kBlockSize, it0.tok_end - tok);
+        const bool valid = lane < nb && phys >= 0 && phys < a.NB;
+        if (lane < nb && !valid) raise_error(a.err, kErrBlock);
+        const unsigned mask = __ballot_sync(0xffffffffu, valid);
+        int bytes = valid ? 2 * rows * D * (int)sizeof(T) : 0;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
+        const bool first = k0 == 0;
+        if (lane == 0) {
+          StageHdr h;
+          h.b = it0.b;
+          h.kvh = kvh;
+          h.p = it0.p;
+          h.nparts = it0.nparts;
+          h.tok_end = it0.tok_end;
+          h.blk0 = blk0 + k0;
+          h.nblk = nb;
+          h.flags = (first ? kFirst : 0) | (k0 + NC >= nblk ? kLast : 0) | (int)(mask << 8);
+          hdr[slot] = h;
+          mbar_arrive_expect_tx(&full[slot], (uint32_t)(bytes + (first ? PC::kQBytes : 0)));
+        }
+        __syncwarp();
+        unsigned char* stage = smem + PC::kOffKV + slot * PC::kStageBytes;
+        if (valid) {
+          const size_t src = (size_t)phys * a.Hkv * PC::kBlockElems + head_off;
+          const uint32_t nbytes = (uint32_t)(rows * D * (int)sizeof(T));
+          bulk_copy_g2s(stage + lane * PC::kBlockBytes, kpool + src, nbytes, &full[slot]);
+          bulk_copy_g2s(stage + (NC + lane) * PC::kBlockBytes, vpool + src, nbytes, &full[slot]);
+        }
+        if (first && lane == 0)
+          bulk_copy_g2s(smem + PC::kOffQ + slot * PC::kQStride,
+                        qbase + ((size_t)it0.b * a.Hq + (size_t)kvh * G) * D, PC::kQBytes,
+                        &full[slot]);
+        if (st == 0) PROBE_SET(1, global_timer_ns());
+        if (first && lane == 0) PROBE_SET(8 + 2 * items_done, global_timer_ns());
+        ++st;
+      }
+      ++items_done;
+      g0 = g1;
+      it0 = it1;
+      v0 = v1;
+      tb0 = tb1;
+      g1 = g2;
+      it1 = it2;
+      v1 = v2;
+    }
+    if (!aborted) {
+      // End marker: a stage with no data.
+      const int slot = st % S;
+      const uint32_t ph = (st / S) & 1u;
+      bool ok_wait = true;
+      if (lane == 0) ok_wait = mbar_wait_bounded(&empty[slot], ph ^ 1u);
+      if (__shfl_sync(0xffffffffu, ok_wait ? 1 : 0, 0)) {
+        if (lane == 0) {
+          hdr[slot].flags = kDone;
+          mbar_arrive(&full[slot]);
+        }
+      } else {
+        fail();
+        aborted = true;
+      }
+    }
+    PROBE_SET(2, global_timer_ns());
+    PROBE_SET(7, items_done);
+    if (aborted && lane == 0) {
+      // Let the copies still in flight land before the CTA retires.
+      const uint32_t first_st = st > (uint32_t)S ? st - S : 0u;
+      for (uint32_t s2 = first_st; s2 < st; ++s2)
+        (void)mbar_wait_bounded(&full[s2 % S], (s2 / S) & 1u);
+    }
+    return;
+  }
+
+  // ================================================================== consumers
+  float qf[G][C::kEPL];
+  float m[G], l[G], o[G][C::kEPL];
+  float* pm = reinterpret_cast<float*>(smem + PC::kOffPm);
+  float* pl = reinterpret_cast<float*>(smem + PC::kOffPl);
+  float* po = reinterpret_cast<float*>(smem + PC::kOffPo);
+  const int c = lane & 7, tg = lane >> 3;
+  const int ctid = threadIdx.x;  // 0 .. NC*32-1
+  uint32_t st = 0, sync_phase = 0;
+#ifdef PHOTON_PROBE
+  int items_seen = 0;
+#endif
+
+  while (true) {
+    const int slot = st % S;
+    const uint32_t ph = (st / S) & 1u;
+    if (!mbar_wait_bounded(&full[slot], ph) || *abort_flag) {
+      fail();
+      return;
+    }
+    if (st == 0 && ctid == 0) PROBE_SET(3, global_timer_ns());
+    const StageHdr h = hdr[slot];
+    if (h.flags & kDone) {
+      if (ctid == 0) PROBE_SET(4, global_timer_ns());
+      return;
+    }
+    if (h.flags & kFirst) {
+      const T* qs = reinterpret_cast<const T*>(smem + PC::kOffQ + slot * PC::kQStride);
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        m[g] = -INFINITY;
+        l[g] = 0.f;
+#pragma unroll
+        for (int i = 0; i < C::kPPL; ++i) {
+          const uint4 raw = *reinterpret_cast<const uint4*>(qs + g * D + (c + 8 * i) * C::kChunk);
+          float t[C::kChunk];
+          Elem<T>::widen(raw, t);
+#pragma unroll
+          for (int e = 0; e < C::kChunk; ++e) {
+            qf[g][i * C::kChunk + e] = t[e] * a.qscale;
+            o[g][i * C::kChunk + e] = 0.f;
+          }
+        }
+      }
+    }
+    if (warp < h.nblk && ((h.flags >> (8 + warp)) & 1)) {
+      const T* stage = reinterpret_cast<const T*>(smem + PC::kOffKV + slot * PC::kStageBytes);
+      const int n_valid = min(kBlockSize, h.tok_end - (h.blk0 + warp) * kBlockSize);
+      attend_block<T, D, G>(stage + warp * PC::kBlockElems, stage + (NC + warp) * PC::kBlockElems,
+                            n_valid, qf, m, l, o, lane);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[slot]);
+    ++st;
+    if (!(h.flags & kLast)) continue;
+
+    // ---- end of the item: combine the warps' (m, l, o)
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+      l[g] += __shfl_xor_sync(0xffffffffu, l[g], 8);
+      l[g] += __shfl_xor_sync(0xffffffffu, l[g], 16);
+#pragma unroll
+      for (int e = 0; e < C::kEPL; ++e) {
+        o[g][e] += __shfl_xor_sync(0xffffffffu, o[g][e], 8);
+        o[g][e] += __shfl_xor_sync(0xffffffffu, o[g][e], 16);
+      }
+    }
+    if (tg == 0) {
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+#pragma unroll
+        for (int i = 0; i < C::kPPL; ++i)
+#pragma unroll
+          for (int e = 0; e < C::kChunk; ++e)
+            po[(warp * G + g) * D + (c + 8 * i) * C::kChunk + e] = o[g][i * C::kChunk + e];
+        if (c == 0) {
+          pm[warp * G + g] = m[g];
+          pl[warp * G + g] = l[g];
+        }
+      }
+    }
+    if (!consumer_sync(sync, sync_phase, lane)) {
+      fail();
+      return;
+    }
+    for (int idx = ctid; idx < G * D; idx += NC * 32) {
+      const int g = idx / D, e = idx % D;
+      float M = -INFINITY;
+#pragma unroll
+      for (int w = 0; w < NC; ++w)
+        if (pl[w * G + g] > 0.f) M = fmaxf(M, pm[w * G + g]);
+      float L = 0.f, O = 0.f;
+#pragma unroll
+      for (int w = 0; w < NC; ++w) {
+        const float lw = pl[w * G + g];
+        if (lw > 0.f) {
+          const float wt = exp2f(pm[w * G + g] - M);
+          L = fmaf(wt, lw, L);
+          O = fmaf(wt, po[(w * G + g) * D + e], O);
+        }
+      }
+      const int hq = h.kvh * G + g;
+      if (h.nparts == 1) {
+        T* out = static_cast<T*>(a.out) + ((size_t)h.b * a.Hq + hq) * D;
+        out[e] = Elem<T>::narrow(L > 0.f ? O / L : 0.f);
+      } else {
+        const size_t row = ((size_t)h.b * a.Hq + hq) * a.pmax + h.p;
+        a.ws_o[row * D + e] = O;
+        if (e == 0) {
+          a.ws_m[row] = M;
+          a.ws_l[row] = L;
+        }
+      }
+    }
+    // the partial buffers are rewritten at the next item's end
+    if (!consumer_sync(sync, sync_phase, lane)) {
+      fail();
+      return;
+    }
+#ifdef PHOTON_PROBE
+    if (ctid == 0) PROBE_SET(9 + 2 * items_seen, global_timer_ns());
+    ++items_seen;
+#endif
+  }
+}
+
+// ------------------------------------------------------------------ merge kernel
+// One warp per (sequence, q head).  Empty (or rejected) contexts get a zero
+// row; sequences with two or more partitions get the merge:
+//   M = max_p m_p,  w_p = 2^(m_p - M) (0 for an empty partition),
+//   out = sum_p w_p o_p / sum_p w_p l_p.
+// Built for latency: a lane owns D/32 consecutive output elements, and the
+// partial rows of up to 32 partitions are loaded unconditionally and at once,
+// together with the (m, l) pairs (lane p holds those of partition p), so a
+// sequence with <= 32 partitions costs one round trip to L2.
+constexpr int kMergeWarps = 4;
+
 template <typename T, int D>
 __global__ void __launch_bounds__(kMergeWarps * 32) paged_decode_merge_kernel(const DecodeArgs a) {
   constexpr int EPL = D / 32;
+  pdl_wait_primary();
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    // The attention grid is done handing out items: leave the queue clean for
+    // the next call.
+    a.ws_ctrl[1] = 0ull;
+    a.ws_ctrl[0] = kQueueReady;
+  }
   const int item = blockIdx.x * kMergeWarps + (threadIdx.x >> 5);
   if (item >= a.B * a.Hq) return;
   const int lane = threadIdx.x & 31;
-  const int b = item / a.Hq, h = item % a.Hq;
+  const int b = item / a.Hq;
   const int ctx = __ldg(a.context_lens + b);
-  if (ctx < 0 || ctx > a.MBS * kBlockSize) return;  // split kernel wrote zeros
+  T* out = static_cast<T*>(a.out) + (size_t)item * D + lane * EPL;
+  if (ctx <= 0 || ctx > a.MBS * kBlockSize) {
+    // empty or rejected context: a zero row
+    if (ctx != 0 && lane == 0 && item % a.Hq == 0) raise_error(a.err, kErrContext);
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) out[e] = Elem<T>::narrow(0.f);
+    return;
+  }
   const int nparts = (ctx + a.part - 1) / a.part;
-  if (nparts < 2) return;                             // split kernel wrote out
-  const size_t row0 = ((size_t)b * a.Hq + h) * a.pmax;
+  if (nparts < 2) return;                             // the attention kernel wrote out
+  const size_t row0 = (size_t)item * a.pmax;          // item = b * Hq + h
   const float* pm = a.ws_m + row0;
   const float* pl = a.ws_l + row0;
   const float* po = a.ws_o + row0 * D + lane * EPL;
 
-  float M = -INFINITY;
-  for (int p = lane; p < nparts; p += 32)
-    if (pl[p] > 0.f) M = fmaxf(M, pm[p]);
-#pragma unroll
-  for (int s = 16; s > 0; s >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, s));
-
-  float L = 0.f, O[EPL];
+  float O[EPL];
 #pragma unroll
   for (int e = 0; e < EPL; ++e) O[e] = 0.f;
-  for (int p = 0; p < nparts; ++p) {
-    const float lp = pl[p];
-    if (!(lp > 0.f)) continue;
-    const float wt = exp2f(pm[p] - M);
-    L = fmaf(wt, lp, L);
+  float M = -INFINITY, L = 0.f;
+  for (int p0 = 0; p0 < nparts; p0 += 32) {
+    const int n = min(32, nparts - p0);
+    float v[32][EPL];
 #pragma unroll
-    for (int e = 0; e < EPL; ++e) O[e] = fmaf(wt, po[(size_t)p * D + e], O[e]);
+    for (int u = 0; u < 32; ++u)
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) v[u][e] = u < n ? po[(size_t)(p0 + u) * D + e] : 0.f;
+    const float lp = lane < n ? pl[p0 + lane] : 0.f;
+    const float mp = lane < n && lp > 0.f ? pm[p0 + lane] : -INFINITY;
+    // running max over the chunks; rescale what was accumulated so far
+    float mc = mp;
+#pragma unroll
+    for (int s = 16; s > 0; s >>= 1) mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, s));
+    const float Mn = fmaxf(M, mc);
+    if (Mn == -INFINITY) continue;                    // nothing in this chunk or before
+    const float scale_old = exp2f(M - Mn);            // 0 when M = -inf
+    const float w = lp > 0.f ? exp2f(mp - Mn) : 0.f;
+    float lw = w * lp;
+#pragma unroll
+    for (int s = 16; s > 0; s >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, s);
+    L = L * scale_old + lw;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) O[e] *= scale_old;
+#pragma unroll
+    for (int u = 0; u < 32; ++u) {
+      const float wu = __shfl_sync(0xffffffffu, w, u);
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) O[e] = fmaf(wu, v[u][e], O[e]);
+    }
+    M = Mn;
   }
-  T* out = static_cast<T*>(a.out) + ((size_t)b * a.Hq + h) * D + lane * EPL;
   const float inv = L > 0.f ? 1.f / L : 0.f;
 #pragma unroll
-  for (int e = 0; e < EPL; ++e) out[e] = Elem<T>::narrow(L > 0.f ? O[e] * inv : 0.f);
+  for (int e = 0; e < EPL; ++e) out[e] = Elem<T>::narrow(O[e] * inv);
+}
+
+// Resident CTAs per SM of an attention-kernel instantiation (queried once per
+// device, after raising its dynamic shared-memory limit).
+template <typename T, int D, int G, int NC, int S>
+int attention_ctas_per_sm() {
+  using PC = PersistCfg<T, D, G, NC, S>;
+  constexpr int kMaxDev = 64;
+  static int cache[kMaxDev];  // 0 = not yet queried
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
+  if (cache[dev] > 0) return cache[dev];
+  auto kern = paged_decode_attention_kernel<T, D, G, NC, S>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PC::kSmemBytes) !=
+      cudaSuccess)
+    return 0;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, PC::kThreads, PC::kSmemBytes) !=
+      cudaSuccess)
+    return 0;
+  cache[dev] = n;
+  return n;
+}
+
+// Tuning knobs (compile time): consumer warps per CTA and the shared-memory
+// ring budget per CTA.  With the defaults two CTAs share an SM.
+#ifndef PHOTON_CONSUMER_WARPS
+#define PHOTON_CONSUMER_WARPS 4
+#endif
+#ifndef PHOTON_RING_KB
+#define PHOTON_RING_KB 96
+#endif
+constexpr int kRingBytes = PHOTON_RING_KB * 1024;
+
+template <typename T, int D>
+constexpr int stages_for(int nc) {
+  return (kRingBytes / (2 * nc * kBlockSize * D * (int)sizeof(T))) < 2
+             ? 2
+             : (kRingBytes / (2 * nc * kBlockSize * D * (int)sizeof(T)));
 }
 
 template <typename T, int D, int G>
-cudaError_t launch_decode_impl(const DecodeArgs& a, cudaStream_t stream) {
-  const dim3 grid(a.pmax, a.Hkv, a.B);
+cudaError_t launch_decode_impl(const DecodeArgs& a0, cudaStream_t stream) {
+  constexpr int NC = PHOTON_CONSUMER_WARPS;
+  constexpr int S = stages_for<T, D>(NC);
+  using PC = PersistCfg<T, D, G, NC, S>;
+  DecodeArgs a = a0;
+  // Every buffer the kernels touch must have been carved out by the caller.
+  if (!a.q || !a.k_cache || !a.v_cache || !a.block_tables || !a.context_lens || !a.out ||
+      !a.ws_m || !a.ws_l || !a.ws_o || !a.ws_ctrl || !a.err)
+    return cudaErrorInvalidValue;
+  const int per_sm = attention_ctas_per_sm<T, D, G, NC, S>();
+  if (per_sm <= 0) return cudaErrorInvalidConfiguration;
+  const int grid = per_sm * a.num_sms;
+
   if (a.ev_start) cudaEventRecord(a.ev_start, stream);
-  paged_decode_split_kernel<T, D, G><<<grid, kDecodeWarps * 32, 0, stream>>>(a);
-  if (a.ev_stop) cudaEventRecord(a.ev_stop, stream);
-  cudaError_t err = cudaGetLastError();
-  if (err != cudaSuccess || a.pmax < 2) return err;
+  cudaError_t err = launch_pdl(paged_decode_attention_kernel<T, D, G, NC, S>, dim3(grid),
+                               dim3(PC::kThreads), PC::kSmemBytes, stream, a);
+  if (err != cudaSuccess) return err;
   const int items = a.B * a.Hq;
-  paged_decode_merge_kernel<T, D>
-      <<<(items + kMergeWarps - 1) / kMergeWarps, kMergeWarps * 32, 0, stream>>>(a);
-  return cudaGetLastError();
+  err = launch_pdl(paged_decode_merge_kernel<T, D>, dim3((items + kMergeWarps - 1) / kMergeWarps),
+                   dim3(kMergeWarps * 32), 0, stream, a);
+  if (err != cudaSuccess) return err;
+  if (a.ev_stop) cudaEventRecord(a.ev_stop, stream);
+  return cudaSuccess;
 }
 
 template <typename T, int D>

@@ -6,3 +6,10 @@ cudaError_t launch_paged_decode_f16(const DecodeArgs& a, cudaStream_t stream) {
   return launch_decode_t<__half>(a, stream);
 }
 }  // namespace photon
+
+#ifdef PHOTON_PROBE
+// Tuning builds only: copy the per-CTA timeline of the last fp16 decode.
+extern "C" int photon_probe_read(void* dst, size_t bytes) {
+  return (int)cudaMemcpyFromSymbol(dst, photon::g_probe, bytes);
+}
+#endif

@@ -25,8 +25,11 @@ std::atomic<uint32_t*> g_err_ptr[kMaxDevices];
 std::atomic<cudaEvent_t> g_ev_start{nullptr};
 std::atomic<cudaEvent_t> g_ev_stop{nullptr};
 
-constexpr int kDefaultPartition = 256;
 constexpr int kMaxPartition = 4096;
+// Default partition: about 128 KB of K+V per (partition, KV head) work item,
+// i.e. a few microseconds of one SM's share of HBM bandwidth, so the last
+// items of the persistent grid finish close together.
+constexpr int kItemBytes = 128 * 1024;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -58,7 +61,12 @@ photon_status_t check_shape(const photon_paged_shape_t* s) {
 }
 
 int partition_of(const photon_paged_shape_t* s) {
-  return s->partition_size ? s->partition_size : kDefaultPartition;
+  if (s->partition_size) return s->partition_size;
+  const int per_token = 2 * s->head_dim * (int)elem_bytes(s->dtype);  // K + V bytes
+  int part = kItemBytes / per_token / s->block_size * s->block_size;
+  if (part < s->block_size) part = s->block_size;
+  if (part > kMaxPartition) part = kMaxPartition;
+  return part;
 }
 
 int max_partitions_of(const photon_paged_shape_t* s) {
@@ -67,19 +75,40 @@ int max_partitions_of(const photon_paged_shape_t* s) {
   return (int)((span + part - 1) / part);
 }
 
+// Workspace: [queue control][m][l][o] (the last three per sequence, q head
+// and partition), each section 256-byte aligned.
 struct WorkspaceLayout {
-  size_t off_m, off_l, off_o, total;
+  size_t off_ctrl, off_m, off_l, off_o, total;
 };
 
 WorkspaceLayout layout_of(const photon_paged_shape_t* s) {
   WorkspaceLayout w{};
-  const size_t rows = (size_t)s->num_seqs * s->num_q_heads * (size_t)max_partitions_of(s);
-  w.off_m = 0;
+  const size_t pairs = (size_t)s->num_seqs * (size_t)max_partitions_of(s);
+  const size_t rows = pairs * s->num_q_heads;
+  w.off_ctrl = 0;
+  w.off_m = 256;
   w.off_l = round_up(w.off_m + rows * sizeof(float), 256);
   w.off_o = round_up(w.off_l + rows * sizeof(float), 256);
   w.total = round_up(w.off_o + rows * (size_t)s->head_dim * sizeof(float), 256);
   if (rows == 0) w.total = 0;
   return w;
+}
+
+// SM count of the current device (cached per device).
+std::atomic<int> g_num_sms[kMaxDevices];
+
+photon_status_t num_sms(int* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return PHOTON_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return PHOTON_ERR_UNSUPPORTED;
+  int n = g_num_sms[dev].load(std::memory_order_relaxed);
+  if (n <= 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      return PHOTON_ERR_CUDA;
+    g_num_sms[dev].store(n, std::memory_order_relaxed);
+  }
+  *out = n;
+  return PHOTON_OK;
 }
 
 // Device address of the error word for the current device.
@@ -158,8 +187,13 @@ photon_status_t photon_paged_decode_plan(const photon_paged_shape_t* shape,
   const int pmax = max_partitions_of(shape);
   if (partition_size) *partition_size = partition_of(shape);
   if (max_partitions) *max_partitions = pmax;
-  if (attention_ctas) *attention_ctas = pmax * shape->num_kv_heads * shape->num_seqs;
-  if (kernels_per_call) *kernels_per_call = shape->num_seqs == 0 ? 0 : (pmax > 1 ? 2 : 1);
+  if (kernels_per_call) *kernels_per_call = shape->num_seqs == 0 ? 0 : 2;
+  if (attention_ctas) {
+    // The persistent grid fills the device: two CTAs per SM of the current
+    // device (0 when no device is visible).
+    int sms = 0;
+    *attention_ctas = num_sms(&sms) == PHOTON_OK ? 2 * sms : 0;
+  }
   return PHOTON_OK;
 }
 
@@ -184,6 +218,8 @@ photon_status_t photon_paged_decode(const void* q, const void* k_cache, const vo
   }
   uint32_t* err = nullptr;
   if ((st = error_word(&err)) != PHOTON_OK) return st;
+  int sms = 0;
+  if ((st = num_sms(&sms)) != PHOTON_OK) return st;
 
   photon::DecodeArgs a{};
   a.q = q;
@@ -196,6 +232,8 @@ photon_status_t photon_paged_decode(const void* q, const void* k_cache, const vo
   a.ws_m = reinterpret_cast<float*>(ws + wl.off_m);
   a.ws_l = reinterpret_cast<float*>(ws + wl.off_l);
   a.ws_o = reinterpret_cast<float*>(ws + wl.off_o);
+  a.ws_ctrl = reinterpret_cast<unsigned long long*>(ws + wl.off_ctrl);
+  a.num_sms = sms;
   a.err = err;
   a.qscale = (float)((double)scale * 1.4426950408889634);  // scale * log2(e)
   a.B = shape->num_seqs;

@@ -74,6 +74,13 @@ __device__ __forceinline__ uint4 ld_stream16(const void* p) {
 }
 
 // ------------------------------------------------------------------ launches
+// One partition p of sequence b (the KV head is added by the kernel).  tok_end
+// is the exclusive end of the partition's token range, nparts the number of
+// partitions of the sequence.
+struct WorkItem {
+  int b, p, tok_end, nparts;
+};
+
 struct DecodeArgs {
   const void* q;
   const void* k_cache;
@@ -81,13 +88,15 @@ struct DecodeArgs {
   const int32_t* block_tables;
   const int32_t* context_lens;
   void* out;
-  float* ws_m;      // [B][Hq][pmax]   running max (log2 domain) per partition
-  float* ws_l;      // [B][Hq][pmax]   sum of weights per partition
-  float* ws_o;      // [B][Hq][pmax][D] unnormalised weighted V sum per partition
-  uint32_t* err;    // sticky device error word
-  float qscale;     // scale * log2(e): scores are kept in the log2 domain
+  float* ws_m;        // [B][Hq][pmax]    running max (log2 domain) per partition
+  float* ws_l;        // [B][Hq][pmax]    sum of weights per partition
+  float* ws_o;        // [B][Hq][pmax][D] unnormalised weighted V sum per partition
+  unsigned long long* ws_ctrl;  // work-queue control: [0] guard word, [1] queue counter
+  uint32_t* err;      // sticky device error word
+  float qscale;       // scale * log2(e): scores are kept in the log2 domain
   int B, Hq, Hkv, D, NB, MBS, part, pmax;
-  cudaEvent_t ev_start, ev_stop;  // optional timing hook around the split kernel
+  int num_sms;        // SMs of the current device
+  cudaEvent_t ev_start, ev_stop;  // optional timing hook around the decode kernels
 };
 
 struct CacheWriteArgs {
@@ -120,9 +129,112 @@ cudaError_t launch_paged_decode_f32(const DecodeArgs& a, cudaStream_t stream);
 cudaError_t launch_paged_decode_f16(const DecodeArgs& a, cudaStream_t stream);
 cudaError_t launch_paged_decode_bf16(const DecodeArgs& a, cudaStream_t stream);
 
-// Block size, partition bounds and threads per CTA of the decode kernels.
+
+// Launch with programmatic stream serialization: the kernel may be scheduled
+// while its predecessor in the stream finishes and must call
+// pdl_wait_primary() before touching memory the predecessor writes.
+template <typename Kernel, typename... Args>
+cudaError_t launch_pdl(Kernel kernel, dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 constexpr int kBlockSize = 16;
-constexpr int kDecodeWarps = 4;
-constexpr int kMergeWarps = 4;
+// Guard value the merge kernel leaves in ws_ctrl[0] after resetting the
+// queue counter; any other value (a fresh workspace) makes the attention
+// kernel hand items out statically for that call.
+constexpr unsigned long long kQueueReady = 0x70686f746f6e5131ull;
+
+}  // namespace photon
+
+// ------------------------------------------------------------------ PTX helpers
+namespace photon {
+
+enum : uint32_t { kErrTimeout = 8u };
+// A bounded wait gives up after this long (ns of %globaltimer), flags
+// kErrTimeout and lets the kernel unwind instead of hanging.
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long global_timer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+               : "memory");
+}
+
+__device__ __forceinline__ void mbar_init_fence() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t tx_bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+               "r"(tx_bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Waits for the phase of `bar` with the given parity to complete; false after
+// kWaitLimitNs.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_timer_ns();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 32; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+// 1-D bulk copy global -> this CTA's shared memory, completing on `bar`
+// (both addresses 16-byte aligned, bytes a multiple of 16).
+__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes,
+                                              uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// Programmatic dependent launch controls (no-ops without the launch attribute).
+__device__ __forceinline__ void pdl_wait_primary() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 
 }  // namespace photon

@@ -102,6 +102,7 @@ def test_workspace_size_and_plan(lib):
     assert P.photon_paged_decode_workspace_size(_shape(num_seqs=0)) == 0
     d = P.photon_paged_decode_plan(_shape())
     assert d["partition_size"] > 0 and d["partition_size"] % 16 == 0
+    assert d["kernels_per_call"] in (2, 3)
     with pytest.raises(P.PhotonError):
         P.photon_paged_decode_plan(_shape(num_q_heads=3))
 

@@ -122,7 +122,7 @@ def build(name: str, *, num_q_heads: int, num_kv_heads: int, head_dim: int,
           context_lens: np.ndarray, num_blocks: int, dtype: int, scale: float,
           rng: np.random.Generator, block_size: int = 16,
           max_blocks_per_seq: Optional[int] = None, free_list_new_blocks: bool = False,
-          seed: int = 0) -> Workload:
+          seed: int = 0, shuffle_pool: bool = True) -> Workload:
     """Assemble a workload from sampled context lengths.
 
     The physical pool is handed out from one random permutation.  With
@@ -141,6 +141,8 @@ def build(name: str, *, num_q_heads: int, num_kv_heads: int, head_dim: int,
     assert int(nblk.sum()) <= num_blocks, "pool too small"
 
     perm = rng.permutation(num_blocks).astype(np.int32)
+    if not shuffle_pool:   # contiguous pool: each sequence's blocks in order
+        perm = np.arange(num_blocks, dtype=np.int32)
     tables = np.full((B, mbs), -1, dtype=np.int32)
     if free_list_new_blocks:
         prev = np.maximum(ctx.astype(np.int64) - 1, 0)
@@ -240,7 +242,7 @@ def qwen_context_lens(rng: np.random.Generator, batch: int = 64) -> np.ndarray:
 
 
 def qwen_b64(seed: int = 2, batch: int = 64, num_blocks: int = 40000,
-             dtype: int = DTYPE_F16) -> Workload:
+             dtype: int = DTYPE_F16, shuffle_pool: bool = True) -> Workload:
     """Qwen3-style long context: 64 sequences, 16q/8kv heads, d=128, contexts
     log-uniform in [128, 8192], a fragmented 40 000-block pool in random order."""
     rng = np.random.Generator(np.random.PCG64(seed))
@@ -248,7 +250,7 @@ def qwen_b64(seed: int = 2, batch: int = 64, num_blocks: int = 40000,
     return build("qwen_b64" if batch == 64 else f"qwen_b{batch}", num_q_heads=16,
                  num_kv_heads=8, head_dim=128, context_lens=ctx,
                  num_blocks=num_blocks, dtype=dtype, scale=1.0 / math.sqrt(128.0),
-                 rng=rng, max_blocks_per_seq=512, seed=seed)
+                 rng=rng, max_blocks_per_seq=512, seed=seed, shuffle_pool=shuffle_pool)
 
 
 def mix_context_lens(rng: np.random.Generator, batch: int = 256) -> np.ndarray:
@@ -296,6 +298,7 @@ NAMED = {
     "llama_b16": llama_b16,
     "qwen_b64": qwen_b64,
     "mix_b256": mix_b256,
+    "qwen_b64_pool10k": lambda: qwen_b64(num_blocks=10000),
     "sweep_b4": lambda: sweep(4),
     "sweep_b8": lambda: sweep(8),
     "sweep_b16": lambda: sweep(16),
