@@ -129,6 +129,32 @@ photon_status_t photon_paged_decode(const void* q, const void* k_cache, const vo
                                     size_t workspace_bytes, const photon_paged_shape_t* shape,
                                     photon_stream_t stream);
 
+/* photon_paged_decode without a caller-provided workspace.  The pages have no
+ * counterpart of this call; it exists for callers that cannot allocate device
+ * memory for the decode: an engine that reserved nearly all of HBM for its KV
+ * pool at start-up (a later cudaMalloc would fail or cut into that pool), a
+ * plugin that is given no allocator by its host, or a decode path that must
+ * not call cudaMalloc/cudaFree because those calls can synchronise the device.
+ * Arguments, layouts, arithmetic and results are those of photon_paged_decode.
+ * The split-KV scratch comes from one array built into the library:
+ *   - its size is fixed at 32 MiB per GPU, held by every GPU that loads the
+ *     library until the process exits; a problem whose
+ *     photon_paged_decode_workspace_size() exceeds 32 MiB is rejected with
+ *     PHOTON_ERR_WORKSPACE before anything is launched;
+ *   - the first call made with a given device current looks up the array's
+ *     device address for that device (cudaGetSymbolAddress); make that first
+ *     call before starting any stream capture;
+ *   - every call on a device uses the same array and leaves its last contents
+ *     there; nothing in it needs to be cleared between calls, but calls whose
+ *     kernels may overlap on the GPU (different streams, no ordering) race on
+ *     it and must not be issued.
+ * No memory is allocated and nothing is copied between host and device. */
+photon_status_t photon_paged_decode_noalloc(const void* q, const void* k_cache,
+                                            const void* v_cache, const int32_t* block_tables,
+                                            const int32_t* context_lens, float scale, void* out,
+                                            const photon_paged_shape_t* shape,
+                                            photon_stream_t stream);
+
 /* Test / diagnostic export: the block-table gather the decode kernel performs,
  * materialised.  k_dense, v_dense are [num_seqs][num_kv_heads][max_blocks_per_seq
  * * block_size][head_dim]; row j of sequence b is a bit copy of the cached row

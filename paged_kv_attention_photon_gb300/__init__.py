@@ -26,6 +26,7 @@ __all__ = [
     "photon_cache_write", "photon_paged_decode_workspace_size", "photon_paged_decode",
     "photon_paged_gather", "photon_get_last_device_error", "photon_status_string",
     "photon_paged_decode_plan", "photon_debug_set_attention_events",
+    "photon_paged_decode_noalloc",
     "F32", "F16", "BF16", "STATUS",
 ]
 
@@ -91,9 +92,10 @@ def _load() -> ctypes.CDLL:
     lib.photon_status_string.restype = ctypes.c_char_p
     lib.photon_paged_decode_plan.argtypes = [SP] + [ctypes.POINTER(I32)] * 4
     lib.photon_debug_set_attention_events.argtypes = [P, P]
+    lib.photon_paged_decode_noalloc.argtypes = [P, P, P, P, P, ctypes.c_float, P, SP, P]
     for fn in ("photon_cache_write", "photon_paged_decode", "photon_paged_gather",
                "photon_get_last_device_error", "photon_paged_decode_plan",
-               "photon_debug_set_attention_events"):
+               "photon_debug_set_attention_events", "photon_paged_decode_noalloc"):
         getattr(lib, fn).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -158,6 +160,16 @@ def photon_paged_decode(q, k_cache, v_cache, block_tables, context_lens, scale: 
                                        float(scale), _ptr(out), _ptr(workspace),
                                        int(workspace_bytes), ctypes.byref(shape),
                                        _stream(stream)), "photon_paged_decode")
+
+
+def photon_paged_decode_noalloc(q, k_cache, v_cache, block_tables, context_lens, scale: float,
+                                out, shape: PagedShape, stream=None) -> None:
+    """photon_paged_decode with the library's built-in 32 MiB scratch instead of a
+    caller-allocated workspace, for callers that cannot allocate device memory."""
+    _check(_load().photon_paged_decode_noalloc(_ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                               _ptr(block_tables), _ptr(context_lens),
+                                               float(scale), _ptr(out), ctypes.byref(shape),
+                                               _stream(stream)), "photon_paged_decode_noalloc")
 
 
 def photon_paged_gather(k_cache, v_cache, block_tables, context_lens, k_dense, v_dense,
