@@ -129,6 +129,30 @@ photon_status_t photon_paged_decode(const void* q, const void* k_cache, const vo
                                     size_t workspace_bytes, const photon_paged_shape_t* shape,
                                     photon_stream_t stream);
 
+/* One decode step in one call: the batched cache write of the step's new rows
+ * followed by the paged decode, with exactly the result of
+ * photon_cache_write(k_new, v_new, slot_mapping, num_seqs, ...) and then
+ * photon_paged_decode(...) on the same stream (README "Technical details /
+ * Paged attention": the per-step K/V write of many sequences, and the batched
+ * attention over the block-wise cache).  Precondition of the fused form: one
+ * new row per sequence -- row b of k_new / v_new ([num_seqs][Hkv][d]) is the
+ * token at position context_lens[b] - 1 of sequence b, and slot_mapping[b]
+ * (int64 [num_seqs]) is the slot the block table gives for that position.
+ * The attention takes that row straight from k_new / v_new and the kernel that
+ * consumes it also stores it into the cache, so no separate scatter pass runs.
+ * A slot that disagrees with the block table is flagged (device error bit 2);
+ * that row is then neither stored nor attended from k_new (the cache row is
+ * used).  Rows of sequences with context 0 are ignored.  Workspace, layouts
+ * and errors as photon_paged_decode. */
+photon_status_t photon_paged_decode_step(const void* k_new, const void* v_new,
+                                         const int64_t* slot_mapping, const void* q,
+                                         void* k_cache, void* v_cache,
+                                         const int32_t* block_tables,
+                                         const int32_t* context_lens, float scale, void* out,
+                                         void* workspace, size_t workspace_bytes,
+                                         const photon_paged_shape_t* shape,
+                                         photon_stream_t stream);
+
 /* photon_paged_decode without a caller-provided workspace.  The pages have no
  * counterpart of this call; it exists for callers that cannot allocate device
  * memory for the decode: an engine that reserved nearly all of HBM for its KV

@@ -26,7 +26,7 @@ __all__ = [
     "photon_cache_write", "photon_paged_decode_workspace_size", "photon_paged_decode",
     "photon_paged_gather", "photon_get_last_device_error", "photon_status_string",
     "photon_paged_decode_plan", "photon_debug_set_attention_events",
-    "photon_paged_decode_noalloc",
+    "photon_paged_decode_noalloc", "photon_paged_decode_step",
     "F32", "F16", "BF16", "STATUS",
 ]
 
@@ -93,9 +93,12 @@ def _load() -> ctypes.CDLL:
     lib.photon_paged_decode_plan.argtypes = [SP] + [ctypes.POINTER(I32)] * 4
     lib.photon_debug_set_attention_events.argtypes = [P, P]
     lib.photon_paged_decode_noalloc.argtypes = [P, P, P, P, P, ctypes.c_float, P, SP, P]
+    lib.photon_paged_decode_step.argtypes = [P, P, P, P, P, P, P, P, ctypes.c_float, P, P, SZ,
+                                             SP, P]
     for fn in ("photon_cache_write", "photon_paged_decode", "photon_paged_gather",
                "photon_get_last_device_error", "photon_paged_decode_plan",
-               "photon_debug_set_attention_events", "photon_paged_decode_noalloc"):
+               "photon_debug_set_attention_events", "photon_paged_decode_noalloc",
+               "photon_paged_decode_step"):
         getattr(lib, fn).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -160,6 +163,18 @@ def photon_paged_decode(q, k_cache, v_cache, block_tables, context_lens, scale: 
                                        float(scale), _ptr(out), _ptr(workspace),
                                        int(workspace_bytes), ctypes.byref(shape),
                                        _stream(stream)), "photon_paged_decode")
+
+
+def photon_paged_decode_step(k_new, v_new, slot_mapping, q, k_cache, v_cache, block_tables,
+                             context_lens, scale: float, out, workspace, workspace_bytes: int,
+                             shape: PagedShape, stream=None) -> None:
+    """Cache write of each sequence's new row + paged decode in one call."""
+    _check(_load().photon_paged_decode_step(_ptr(k_new), _ptr(v_new), _ptr(slot_mapping),
+                                            _ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                            _ptr(block_tables), _ptr(context_lens),
+                                            float(scale), _ptr(out), _ptr(workspace),
+                                            int(workspace_bytes), ctypes.byref(shape),
+                                            _stream(stream)), "photon_paged_decode_step")
 
 
 def photon_paged_decode_noalloc(q, k_cache, v_cache, block_tables, context_lens, scale: float,

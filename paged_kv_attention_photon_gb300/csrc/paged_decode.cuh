@@ -46,10 +46,11 @@
 
 #include "photon_common.cuh"
 
-// PHOTON_FAST_EXP selects the PTX ex2.approx.ftz instruction for the softmax
-// weights instead of the exp2f library call (a tuning knob; off by default).
+// PHOTON_FAST_EXP selects the PTX ex2.approx.ftz instruction (relative error
+// about 2^-22; results below 2^-126 flush to zero) for the softmax weights
+// instead of the exp2f library call.
 #ifndef PHOTON_FAST_EXP
-#define PHOTON_FAST_EXP 0
+#define PHOTON_FAST_EXP 1
 #endif
 
 namespace photon {
@@ -83,6 +84,9 @@ struct StageHdr {
   int tok_end, blk0;   // exclusive token end of the item; first logical block of the stage
   int nblk;            // blocks carried by this stage (<= consumer warps)
   int flags;           // kFirst | kLast | kDone, valid-block mask << 8
+  // fused step: the stage block (new_warp) whose row new_row is this
+  // sequence's new token, to be stored at physical block new_phys; -1 if none
+  int new_warp, new_phys, new_row, pad;
 };
 enum : int { kFirst = 1, kLast = 2, kDone = 4 };
 
@@ -108,10 +112,11 @@ struct PersistCfg {
   static constexpr int kOffHdr = (kOffRuns + 4 * (kMaxRuns + 1) + 15) / 16 * 16;
   static constexpr int kOffQ = (kOffHdr + (int)sizeof(StageHdr) * S + 127) / 128 * 128;
   static constexpr int kOffKV = kOffQ + kQStride * S;
-  static constexpr int kOffPm = kOffKV + kStageBytes * S;       // float[NC][G]
-  static constexpr int kOffPl = kOffPm + 4 * NC * G;            // float[NC][G]
-  static constexpr int kOffPo = (kOffPl + 4 * NC * G + 15) / 16 * 16;   // float[NC][G][D]
-  static constexpr int kSmemBytes = kOffPo + 4 * NC * G * D;
+  // Per-warp partial state at an item's end, double-buffered by item parity.
+  static constexpr int kOffPm = kOffKV + kStageBytes * S;       // float[2][NC][G]
+  static constexpr int kOffPl = kOffPm + 4 * 2 * NC * G;        // float[2][NC][G]
+  static constexpr int kOffPo = (kOffPl + 4 * 2 * NC * G + 15) / 16 * 16;   // float[2][NC][G][D]
+  static constexpr int kSmemBytes = kOffPo + 4 * 2 * NC * G * D;
 };
 
 // ------------------------------------------------------------------ consumer math
@@ -240,6 +245,17 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
     mbar_init_fence();
   }
   __syncthreads();
+  // Warm L2 with the context lengths and block tables while the previous
+  // kernel finishes (a hint only: the values are read after the wait).
+  {
+    const size_t tid = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    const size_t nthr = (size_t)gridDim.x * blockDim.x;
+    const size_t tbytes = (size_t)a.B * a.MBS * sizeof(int32_t);
+    for (size_t off = tid * 128; off < tbytes; off += nthr * 128)
+      prefetch_l2(reinterpret_cast<const char*>(a.block_tables) + off);
+    for (size_t off = tid * 128; off < (size_t)a.B * sizeof(int32_t); off += nthr * 128)
+      prefetch_l2(reinterpret_cast<const char*>(a.context_lens) + off);
+  }
   // Everything below may read what the previous kernel in the stream wrote
   // (the cache write's rows, context lengths, block tables, q).
   pdl_wait_primary();
@@ -411,12 +427,19 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
     bool v0 = locate(g0 / a.Hkv, it0);
     bool v1 = v0 && locate(g1 / a.Hkv, it1);
     int tb0 = v0 ? load_table(it0, 0) : -1;
+    // fused step: slot of the sequence's new row, needed by its last partition
+    const bool fused = a.k_new != nullptr;
+    auto load_slot = [&](const WorkItem& it) -> long long {
+      return fused && it.p == it.nparts - 1 ? (long long)__ldg(a.slot_mapping + it.b) : -1ll;
+    };
+    long long sl0 = v0 ? load_slot(it0) : -1ll;
     while (v0 && !aborted) {
       const int g2 = bcast(g2raw);
       g2raw = grab();
       WorkItem it2{};
       const bool v2 = v1 && locate(g2 / a.Hkv, it2);
       const int tb1 = v1 ? load_table(it1, 0) : -1;
+      const long long sl1 = v1 ? load_slot(it1) : -1ll;
 
       const int kvh = g0 % a.Hkv;
       const int tok_begin = it0.p * a.part;
@@ -442,6 +465,21 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
         const bool valid = lane < nb && phys >= 0 && phys < a.NB;
         if (lane < nb && !valid) raise_error(a.err, kErrBlock);
         const unsigned mask = __ballot_sync(0xffffffffu, valid);
+        // Fused step: the block holding the sequence's last position takes that
+        // row from k_new / v_new, provided its slot is the one the table gives.
+        bool new_here = false;
+        if (fused && valid && tok + rows == it0.tok_end && it0.p == it0.nparts - 1) {
+          const long long table_slot = (long long)phys * kBlockSize + (rows - 1);
+          if (sl0 == table_slot) {
+            new_here = true;
+          } else {
+            raise_error(a.err, kErrSlot);
+          }
+        }
+        const unsigned new_mask = __ballot_sync(0xffffffffu, new_here);
+        const int new_lane = new_mask ? __ffs(new_mask) - 1 : -1;
+        const int new_phys = __shfl_sync(0xffffffffu, phys, new_lane >= 0 ? new_lane : 0);
+        const int new_rows = __shfl_sync(0xffffffffu, rows, new_lane >= 0 ? new_lane : 0);
         int bytes = valid ? 2 * rows * D * (int)sizeof(T) : 0;
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
@@ -456,6 +494,10 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
           h.blk0 = blk0 + k0;
           h.nblk = nb;
           h.flags = (first ? kFirst : 0) | (k0 + NC >= nblk ? kLast : 0) | (int)(mask << 8);
+          h.new_warp = new_lane;
+          h.new_phys = new_lane >= 0 ? new_phys : -1;
+          h.new_row = new_lane >= 0 ? new_rows - 1 : -1;
+          h.pad = 0;
           hdr[slot] = h;
           mbar_arrive_expect_tx(&full[slot], (uint32_t)(bytes + (first ? PC::kQBytes : 0)));
         }
@@ -463,9 +505,20 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
         unsigned char* stage = smem + PC::kOffKV + slot * PC::kStageBytes;
         if (valid) {
           const size_t src = (size_t)phys * a.Hkv * PC::kBlockElems + head_off;
-          const uint32_t nbytes = (uint32_t)(rows * D * (int)sizeof(T));
-          bulk_copy_g2s(stage + lane * PC::kBlockBytes, kpool + src, nbytes, &full[slot]);
-          bulk_copy_g2s(stage + (NC + lane) * PC::kBlockBytes, vpool + src, nbytes, &full[slot]);
+          const int cache_rows = new_here ? rows - 1 : rows;
+          const uint32_t nbytes = (uint32_t)(cache_rows * D * (int)sizeof(T));
+          if (nbytes) {
+            bulk_copy_g2s(stage + lane * PC::kBlockBytes, kpool + src, nbytes, &full[slot]);
+            bulk_copy_g2s(stage + (NC + lane) * PC::kBlockBytes, vpool + src, nbytes, &full[slot]);
+          }
+          if (new_here) {
+            const size_t nsrc = ((size_t)it0.b * a.Hkv + kvh) * D;
+            const uint32_t rb = (uint32_t)(D * (int)sizeof(T));
+            bulk_copy_g2s(stage + lane * PC::kBlockBytes + nbytes,
+                          static_cast<const T*>(a.k_new) + nsrc, rb, &full[slot]);
+            bulk_copy_g2s(stage + (NC + lane) * PC::kBlockBytes + nbytes,
+                          static_cast<const T*>(a.v_new) + nsrc, rb, &full[slot]);
+          }
         }
         if (first && lane == 0)
           bulk_copy_g2s(smem + PC::kOffQ + slot * PC::kQStride,
@@ -480,6 +533,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
       it0 = it1;
       v0 = v1;
       tb0 = tb1;
+      sl0 = sl1;
       g1 = g2;
       it1 = it2;
       v1 = v2;
@@ -514,9 +568,10 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
   // ================================================================== consumers
   float qf[G][C::kEPL];
   float m[G], l[G], o[G][C::kEPL];
-  float* pm = reinterpret_cast<float*>(smem + PC::kOffPm);
-  float* pl = reinterpret_cast<float*>(smem + PC::kOffPl);
-  float* po = reinterpret_cast<float*>(smem + PC::kOffPo);
+  float* const pm_buf = reinterpret_cast<float*>(smem + PC::kOffPm);
+  float* const pl_buf = reinterpret_cast<float*>(smem + PC::kOffPl);
+  float* const po_buf = reinterpret_cast<float*>(smem + PC::kOffPo);
+  int parity = 0;  // which partial buffer this item's end uses
   const int c = lane & 7, tg = lane >> 3;
   const int ctid = threadIdx.x;  // 0 .. NC*32-1
   uint32_t st = 0, sync_phase = 0;
@@ -561,13 +616,35 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
       const int n_valid = min(kBlockSize, h.tok_end - (h.blk0 + warp) * kBlockSize);
       attend_block<T, D, G>(stage + warp * PC::kBlockElems, stage + (NC + warp) * PC::kBlockElems,
                             n_valid, qf, m, l, o, lane);
+      if (warp == h.new_warp) {
+        // fused step: this block's row new_row is the new token; store it
+        constexpr int kRowChunks = D * (int)sizeof(T) / 16;
+        constexpr int kPerChunk = 16 / (int)sizeof(T);
+        const size_t dst = (((size_t)h.new_phys * a.Hkv + h.kvh) * kBlockSize + h.new_row) * D;
+        const T* krow = stage + warp * PC::kBlockElems + h.new_row * D;
+        const T* vrow = stage + (NC + warp) * PC::kBlockElems + h.new_row * D;
+        for (int i = lane; i < 2 * kRowChunks; i += 32) {
+          const bool is_v = i >= kRowChunks;
+          const int ch = is_v ? i - kRowChunks : i;
+          const uint4 val = *reinterpret_cast<const uint4*>((is_v ? vrow : krow) + ch * kPerChunk);
+          T* cache = static_cast<T*>(is_v ? a.v_cache_w : a.k_cache_w);
+          *reinterpret_cast<uint4*>(cache + dst + ch * kPerChunk) = val;
+        }
+      }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[slot]);
     ++st;
     if (!(h.flags & kLast)) continue;
 
-    // ---- end of the item: combine the warps' (m, l, o)
+    // ---- end of the item: combine the warps' (m, l, o).  The buffers
+    // alternate between items, so one barrier per item suffices: a warp can
+    // only come back to this buffer after every warp has passed the next
+    // item's barrier, i.e. finished reading it here.
+    float* const pm = pm_buf + parity * NC * G;
+    float* const pl = pl_buf + parity * NC * G;
+    float* const po = po_buf + parity * NC * G * D;
+    parity ^= 1;
 #pragma unroll
     for (int g = 0; g < G; ++g) {
       l[g] += __shfl_xor_sync(0xffffffffu, l[g], 8);
@@ -624,11 +701,6 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
           a.ws_l[row] = L;
         }
       }
-    }
-    // the partial buffers are rewritten at the next item's end
-    if (!consumer_sync(sync, sync_phase, lane)) {
-      fail();
-      return;
     }
 #ifdef PHOTON_PROBE
     if (ctid == 0) PROBE_SET(9 + 2 * items_seen, global_timer_ns());

@@ -197,11 +197,19 @@ photon_status_t photon_paged_decode_plan(const photon_paged_shape_t* shape,
   return PHOTON_OK;
 }
 
-photon_status_t photon_paged_decode(const void* q, const void* k_cache, const void* v_cache,
-                                    const int32_t* block_tables, const int32_t* context_lens,
-                                    float scale, void* out, void* workspace,
-                                    size_t workspace_bytes, const photon_paged_shape_t* shape,
-                                    photon_stream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Shared body of photon_paged_decode and photon_paged_decode_step: checks the
+// decode arguments, carves the workspace and launches.  k_new == nullptr means
+// a plain decode.
+photon_status_t decode_common(const void* q, const void* k_cache, const void* v_cache,
+                              const int32_t* block_tables, const int32_t* context_lens,
+                              float scale, void* out, void* workspace, size_t workspace_bytes,
+                              const photon_paged_shape_t* shape, photon_stream_t stream,
+                              const void* k_new, const void* v_new,
+                              const int64_t* slot_mapping) {
   photon_status_t st = check_shape(shape);
   if (st != PHOTON_OK) return st;
   if (!std::isfinite(scale)) return PHOTON_ERR_INVALID_ARG;
@@ -234,6 +242,11 @@ photon_status_t photon_paged_decode(const void* q, const void* k_cache, const vo
   a.ws_o = reinterpret_cast<float*>(ws + wl.off_o);
   a.ws_ctrl = reinterpret_cast<unsigned long long*>(ws + wl.off_ctrl);
   a.num_sms = sms;
+  a.k_new = k_new;
+  a.v_new = v_new;
+  a.slot_mapping = slot_mapping;
+  a.k_cache_w = k_new ? const_cast<void*>(k_cache) : nullptr;
+  a.v_cache_w = k_new ? const_cast<void*>(v_cache) : nullptr;
   a.err = err;
   a.qscale = (float)((double)scale * 1.4426950408889634);  // scale * log2(e)
   a.B = shape->num_seqs;
@@ -256,6 +269,37 @@ photon_status_t photon_paged_decode(const void* q, const void* k_cache, const vo
     default: e = photon::launch_paged_decode_bf16(a, s); break;
   }
   return e == cudaSuccess ? PHOTON_OK : PHOTON_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+photon_status_t photon_paged_decode(const void* q, const void* k_cache, const void* v_cache,
+                                    const int32_t* block_tables, const int32_t* context_lens,
+                                    float scale, void* out, void* workspace,
+                                    size_t workspace_bytes, const photon_paged_shape_t* shape,
+                                    photon_stream_t stream) {
+  return decode_common(q, k_cache, v_cache, block_tables, context_lens, scale, out, workspace,
+                       workspace_bytes, shape, stream, nullptr, nullptr, nullptr);
+}
+
+photon_status_t photon_paged_decode_step(const void* k_new, const void* v_new,
+                                         const int64_t* slot_mapping, const void* q,
+                                         void* k_cache, void* v_cache,
+                                         const int32_t* block_tables,
+                                         const int32_t* context_lens, float scale, void* out,
+                                         void* workspace, size_t workspace_bytes,
+                                         const photon_paged_shape_t* shape,
+                                         photon_stream_t stream) {
+  photon_status_t st = check_shape(shape);
+  if (st != PHOTON_OK) return st;
+  if (shape->num_seqs == 0) return PHOTON_OK;
+  if (!k_new || !v_new || !slot_mapping) return PHOTON_ERR_INVALID_ARG;
+  if (!aligned16(k_new) || !aligned16(v_new) || (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
+    return PHOTON_ERR_MISALIGNED;
+  return decode_common(q, k_cache, v_cache, block_tables, context_lens, scale, out, workspace,
+                       workspace_bytes, shape, stream, k_new, v_new, slot_mapping);
 }
 
 photon_status_t photon_paged_gather(const void* k_cache, const void* v_cache,

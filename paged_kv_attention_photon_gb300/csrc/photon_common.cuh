@@ -92,6 +92,14 @@ struct DecodeArgs {
   float* ws_l;        // [B][Hq][pmax]    sum of weights per partition
   float* ws_o;        // [B][Hq][pmax][D] unnormalised weighted V sum per partition
   unsigned long long* ws_ctrl;  // work-queue control: [0] guard word, [1] queue counter
+  // Fused step only (all null otherwise): row b of k_new / v_new is sequence
+  // b's new token at position ctx_b - 1; the attention kernel attends over it
+  // and writes it to its cache slot.
+  const void* k_new;
+  const void* v_new;
+  const int64_t* slot_mapping;
+  void* k_cache_w;
+  void* v_cache_w;
   uint32_t* err;      // sticky device error word
   float qscale;       // scale * log2(e): scores are kept in the log2 domain
   int B, Hq, Hkv, D, NB, MBS, part, pmax;
@@ -227,6 +235,11 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
           smem_addr(dst)),
       "l"(src), "r"(bytes), "r"(smem_addr(bar))
       : "memory");
+}
+
+// Hint: bring a line into L2 (no architectural effect on values).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
 // Programmatic dependent launch controls (no-ops without the launch attribute).

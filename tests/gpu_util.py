@@ -69,6 +69,13 @@ class DeviceWorkload:
                              self.wl.slot_mapping.shape[0], self.k_cache, self.v_cache,
                              self.shape, stream)
 
+    def step(self, stream=None) -> None:
+        """Fused cache write + decode (photon_paged_decode_step)."""
+        P.photon_paged_decode_step(self.k_new, self.v_new, self.slot_mapping, self.q,
+                                   self.k_cache, self.v_cache, self.block_tables,
+                                   self.context_lens, self.wl.scale, self.out, self.ws,
+                                   self.ws_bytes, self.shape, stream)
+
     def decode(self, scale=None, stream=None) -> None:
         P.photon_paged_decode(self.q, self.k_cache, self.v_cache, self.block_tables,
                               self.context_lens, self.wl.scale if scale is None else scale,

@@ -148,6 +148,55 @@ def test_step_matches_oracle(name):
     assert_close(d.out_f64(), want, wl.dtype, name)
 
 
+@pytest.mark.parametrize("name", sorted(CASES) + ["qwen_b64", "mix_b256"])
+def test_fused_step_matches_oracle_and_separate_calls(name):
+    """photon_paged_decode_step == cache write then decode: output against the
+    oracle, the written rows bit for bit, and bit-identical to the two
+    separate calls."""
+    wl = {"qwen_b64": W.qwen_b64, "mix_b256": W.mix_b256}.get(name, CASES.get(name))()
+    kc, vc, want = _oracle_step(wl)
+    fused = DeviceWorkload(wl)
+    fused.step()
+    sep = DeviceWorkload(wl)
+    sep.cache_write()
+    sep.decode()
+    torch.cuda.synchronize()
+    _no_device_error()
+    assert_close(fused.out_f64(), want, wl.dtype, name)
+    assert fused.out.view(torch.int16).equal(sep.out.view(torch.int16))
+    live = wl.slot_mapping >= 0
+    blk = wl.slot_mapping[live] // wl.block_size
+    off = wl.slot_mapping[live] % wl.block_size
+    ib, io = torch.from_numpy(blk).cuda(), torch.from_numpy(off).cuda()
+    for dev_pool, host_pool in ((fused.k_cache, kc), (fused.v_cache, vc)):
+        got = dev_pool[ib, :, io].cpu().numpy()
+        assert got.tobytes() == host_pool[blk, :, off].tobytes()
+    if wl.k_cache.nbytes < (64 << 20):   # small pools: every other byte unchanged too
+        assert host(fused.k_cache, kc).tobytes() == kc.tobytes()
+        assert host(fused.v_cache, vc).tobytes() == vc.tobytes()
+
+
+def test_fused_step_flags_a_slot_that_disagrees_with_the_table():
+    wl = W.random_small(56, batch=4, num_q_heads=8, num_kv_heads=2, head_dim=64, max_ctx=70,
+                        dtype=W.DTYPE_F16, context_lens=[20, 33, 64, 70], extra_blocks=4)
+    slots = wl.slot_mapping.copy()
+    slots[2] = slots[2] - 1                      # not the slot of position ctx-1
+    d = DeviceWorkload(wl)
+    d.slot_mapping = dev(slots)
+    d.step()
+    st, bits = P.photon_get_last_device_error()
+    assert st == 6 and bits & 2
+    # sequence 2 attends over the cache as it was; the others over their new rows
+    kc, vc = wl.k_cache.copy(), wl.v_cache.copy()
+    good = wl.slot_mapping.copy()
+    good[2] = -1
+    oracle.cache_write(wl.k_new, wl.v_new, good, kc, vc, block_size=wl.block_size)
+    want = oracle.paged_decode(wl.q, kc, vc, wl.block_tables, wl.context_lens, wl.scale,
+                               dtype=wl.dtype)
+    assert_close(d.out_f64(), want, wl.dtype)
+    assert host(d.k_cache, kc).tobytes() == kc.tobytes()
+
+
 @pytest.mark.parametrize("part", [16, 32, 48, 128, 512, 4096])
 def test_partition_size_invariance(part):
     wl = W.random_small(51, batch=6, num_q_heads=16, num_kv_heads=8, head_dim=128,
