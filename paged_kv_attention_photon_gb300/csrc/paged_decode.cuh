@@ -262,59 +262,11 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
   // The merge kernel may be scheduled as CTAs retire; it waits for this grid.
   pdl_launch_dependents();
 
-  // Number of full partitions over the batch, counted by the whole CTA.
   const int span = a.MBS * kBlockSize;
   auto ctx_of = [&](int b) -> int {
     const int c = b < a.B ? __ldg(a.context_lens + b) : 0;
     return (c < 0 || c > span) ? 0 : c;  // rejected lengths count as empty
   };
-  // Run sizes of the work list, counted by the whole CTA: run 0 holds the
-  // full partitions, run 1 + k the tail partitions of class k, where a tail of
-  // nb blocks (of P16 = part / 16 per partition) has class
-  // floor(log2(floor(P16 / nb))): halves of the partition size, largest first.
-  const int P16 = a.part / kBlockSize;
-  const int nclass = 32 - __clz(P16);  // classes 0 .. log2(P16)
-  auto tail_class = [&](int ctxv) -> int {
-    const int tail = ctxv % a.part;
-    if (!tail) return -1;
-    const int nb = (tail + kBlockSize - 1) / kBlockSize;
-    return 31 - __clz(P16 / nb);
-  };
-  int* run_start = reinterpret_cast<int*>(smem + PC::kOffRuns);  // pairs before run r
-  bool dynamic = false;
-  {
-    int cnt[kMaxRuns];
-#pragma unroll
-    for (int r = 0; r < kMaxRuns; ++r) cnt[r] = 0;
-    for (int b = threadIdx.x; b < a.B; b += PC::kThreads) {
-      const int c = ctx_of(b);
-      cnt[0] += c / a.part;
-      const int k = tail_class(c);
-#pragma unroll
-      for (int r = 1; r < kMaxRuns; ++r) cnt[r] += (k == r - 1) ? 1 : 0;
-    }
-    int* red = reinterpret_cast<int*>(smem + PC::kOffPo);  // scratch until the first item ends
-#pragma unroll
-    for (int r = 0; r < kMaxRuns; ++r) {
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) cnt[r] += __shfl_xor_sync(0xffffffffu, cnt[r], o);
-      if (lane == 0) red[r * (NC + 1) + warp] = cnt[r];
-    }
-    if (threadIdx.x == 0) red[kMaxRuns * (NC + 1)] = a.ws_ctrl[0] == kQueueReady ? 1 : 0;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      int acc = 0;
-      for (int r = 0; r < kMaxRuns; ++r) {
-        run_start[r] = acc;
-        for (int w = 0; w < NC + 1; ++w) acc += red[r * (NC + 1) + w];
-      }
-      run_start[kMaxRuns] = acc;
-    }
-    dynamic = red[kMaxRuns * (NC + 1)] != 0;
-    __syncthreads();
-  }
-  (void)nclass;
-
   auto fail = [&](void) {
     if (lane == 0) {
       raise_error(a.err, kErrTimeout);
@@ -338,6 +290,49 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
     // copy stream: while item i's stages are issued, the block-table slice of
     // item i+1 is in flight and item i+2 is located.
     PROBE_SET(0, global_timer_ns());
+    // Run sizes of the work list, counted by this warp: run 0 holds the full
+    // partitions, run 1 + k the tail partitions of class k, where a tail of nb
+    // blocks (of P16 = part / 16 per partition) has class
+    // floor(log2(floor(P16 / nb))): halves of the partition size, largest
+    // first.  Only this warp needs them, so the consumers never wait for it.
+    const int P16 = a.part / kBlockSize;
+    auto tail_class = [&](int ctxv) -> int {
+      const int tail = ctxv % a.part;
+      if (!tail) return -1;
+      const int nb = (tail + kBlockSize - 1) / kBlockSize;
+      return 31 - __clz(P16 / nb);
+    };
+    int* run_start = reinterpret_cast<int*>(smem + PC::kOffRuns);  // pairs before run r
+    // The first two windows of context lengths are loaded once, up front, and
+    // serve both this count and the walk below (a batch of up to 64 sequences
+    // needs no other load).
+    const int ctx_w0 = ctx_of(lane), ctx_w1 = ctx_of(32 + lane);
+    const bool dynamic =
+        __shfl_sync(0xffffffffu, lane == 0 && a.ws_ctrl[0] == kQueueReady ? 1 : 0, 0) != 0;
+    {
+      int cnt[kMaxRuns];
+#pragma unroll
+      for (int r = 0; r < kMaxRuns; ++r) cnt[r] = 0;
+      auto count = [&](int c) {
+        cnt[0] += c / a.part;
+        const int k = tail_class(c);
+#pragma unroll
+        for (int r = 1; r < kMaxRuns; ++r) cnt[r] += (k == r - 1) ? 1 : 0;
+      };
+      count(ctx_w0);
+      count(ctx_w1);
+      for (int b = 64 + lane; b < a.B; b += 32) count(ctx_of(b));
+      int acc = 0;
+#pragma unroll
+      for (int r = 0; r < kMaxRuns; ++r) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) cnt[r] += __shfl_xor_sync(0xffffffffu, cnt[r], o);
+        if (lane == 0) run_start[r] = acc;
+        acc += cnt[r];
+      }
+      if (lane == 0) run_start[kMaxRuns] = acc;
+      __syncwarp();
+    }
     const T* kpool = static_cast<const T*>(a.k_cache);
     const T* vpool = static_cast<const T*>(a.v_cache);
     const T* qbase = static_cast<const T*>(a.q);
@@ -361,7 +356,6 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
     };
     // The first two windows stay in registers: a batch of up to 64 sequences
     // never reloads context lengths when a new run starts.
-    const int ctx_w0 = ctx_of(lane), ctx_w1 = ctx_of(32 + lane);
     set_window(ctx_w0);
     int pre_ctx = ctx_w1;
     // (sequence, partition) of pair index `pair`; false past the last pair.
@@ -719,6 +713,9 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
 // together with the (m, l) pairs (lane p holds those of partition p), so a
 // sequence with <= 32 partitions costs one round trip to L2.
 constexpr int kMergeWarps = 4;
+// Partial rows loaded at once per lane: one round trip for up to 32
+// partitions.
+constexpr int kMergeRows = 32;
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kMergeWarps * 32) paged_decode_merge_kernel(const DecodeArgs a) {
@@ -756,9 +753,9 @@ __global__ void __launch_bounds__(kMergeWarps * 32) paged_decode_merge_kernel(co
   float M = -INFINITY, L = 0.f;
   for (int p0 = 0; p0 < nparts; p0 += 32) {
     const int n = min(32, nparts - p0);
-    float v[32][EPL];
+    float v[kMergeRows][EPL];
 #pragma unroll
-    for (int u = 0; u < 32; ++u)
+    for (int u = 0; u < kMergeRows; ++u)
 #pragma unroll
       for (int e = 0; e < EPL; ++e) v[u][e] = u < n ? po[(size_t)(p0 + u) * D + e] : 0.f;
     const float lp = lane < n ? pl[p0 + lane] : 0.f;
@@ -778,10 +775,25 @@ __global__ void __launch_bounds__(kMergeWarps * 32) paged_decode_merge_kernel(co
 #pragma unroll
     for (int e = 0; e < EPL; ++e) O[e] *= scale_old;
 #pragma unroll
-    for (int u = 0; u < 32; ++u) {
+    for (int u = 0; u < kMergeRows; ++u) {
       const float wu = __shfl_sync(0xffffffffu, w, u);
 #pragma unroll
       for (int e = 0; e < EPL; ++e) O[e] = fmaf(wu, v[u][e], O[e]);
+    }
+#pragma unroll
+    for (int u0 = kMergeRows; u0 < 32; u0 += kMergeRows) {  // rest of the chunk, if any
+      if (u0 >= n) break;
+#pragma unroll
+      for (int u = 0; u < kMergeRows; ++u)
+#pragma unroll
+        for (int e = 0; e < EPL; ++e)
+          v[u][e] = u0 + u < n ? po[(size_t)(p0 + u0 + u) * D + e] : 0.f;
+#pragma unroll
+      for (int u = 0; u < kMergeRows; ++u) {
+        const float wu = __shfl_sync(0xffffffffu, w, u0 + u);
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) O[e] = fmaf(wu, v[u][e], O[e]);
+      }
     }
     M = Mn;
   }

@@ -26,10 +26,10 @@ std::atomic<cudaEvent_t> g_ev_start{nullptr};
 std::atomic<cudaEvent_t> g_ev_stop{nullptr};
 
 constexpr int kMaxPartition = 4096;
-// Default partition: about 128 KB of K+V per (partition, KV head) work item,
+// Default partition: about 192 KB of K+V per (partition, KV head) work item,
 // i.e. a few microseconds of one SM's share of HBM bandwidth, so the last
 // items of the persistent grid finish close together.
-constexpr int kItemBytes = 128 * 1024;
+constexpr int kItemBytes = 192 * 1024;
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
