@@ -286,9 +286,9 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
     // window of 32 sequences (lane j: sequence wb + j's context length, its
     // pair count in the current run and the pairs before it) and slides it
     // forward as its items advance, with the next window's lengths already
-    // loaded.  A three-deep software pipeline keeps every round trip off the
-    // copy stream: while item i's stages are issued, the block-table slice of
-    // item i+1 is in flight and item i+2 is located.
+    // loaded.  A software pipeline keeps every round trip off the copy
+    // stream: while item i's stages are issued, the block-table slice of item
+    // i+1 is in flight and the index of item i+2 is taken (then located).
     PROBE_SET(0, global_timer_ns());
     // Run sizes of the work list, counted by this warp: run 0 holds the full
     // partitions, run 1 + k the tail partitions of class k, where a tail of nb
@@ -416,7 +416,6 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
     };
     auto bcast = [&](int raw) -> int { return dynamic ? __shfl_sync(0xffffffffu, raw, 0) : raw; };
     int g0 = blockIdx.x, g1 = g0 + N;
-    int g2raw = grab();
     WorkItem it0{}, it1{};
     bool v0 = locate(g0 / a.Hkv, it0);
     bool v1 = v0 && locate(g1 / a.Hkv, it1);
@@ -428,12 +427,12 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
     };
     long long sl0 = v0 ? load_slot(it0) : -1ll;
     while (v0 && !aborted) {
-      const int g2 = bcast(g2raw);
-      g2raw = grab();
-      WorkItem it2{};
-      const bool v2 = v1 && locate(g2 / a.Hkv, it2);
+      // The next item's table slice and slot load while this item's stages
+      // are issued; the item after it is taken from the queue now and
+      // located once they are, so a CTA commits to at most two items ahead.
       const int tb1 = v1 ? load_table(it1, 0) : -1;
       const long long sl1 = v1 ? load_slot(it1) : -1ll;
+      const int g2raw = grab();
 
       const int kvh = g0 % a.Hkv;
       const int tok_begin = it0.p * a.part;
@@ -522,6 +521,9 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
         if (first && lane == 0) PROBE_SET(8 + 2 * items_done, global_timer_ns());
         ++st;
       }
+      const int g2 = bcast(g2raw);
+      WorkItem it2{};
+      const bool v2 = v1 && locate(g2 / a.Hkv, it2);
       ++items_done;
       g0 = g1;
       it0 = it1;
@@ -712,7 +714,13 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
 // partial rows of up to 32 partitions are loaded unconditionally and at once,
 // together with the (m, l) pairs (lane p holds those of partition p), so a
 // sequence with <= 32 partitions costs one round trip to L2.
-constexpr int kMergeWarps = 4;
+// Two warps per CTA: small enough (64 threads) for a merge CTA to be resident
+// next to two attention CTAs, so merges start as soon as the attention grid
+// completes.
+#ifndef PHOTON_MERGE_WARPS
+#define PHOTON_MERGE_WARPS 2
+#endif
+constexpr int kMergeWarps = PHOTON_MERGE_WARPS;
 // Partial rows loaded at once per lane: one round trip for up to 32
 // partitions.
 constexpr int kMergeRows = 32;
