@@ -45,6 +45,7 @@ import workloads as W  # noqa: E402
 METRIC = "paged-decode KV GB/s and fraction of GB300 HBM peak; decode tokens/s per layer"
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 512 << 20
+ROPE_BASE = 1.0e6          # rotary base of the Qwen family (the side measurement only)
 L2_CLEAN_BYTES = 256 << 20
 
 
@@ -58,6 +59,8 @@ def parse():
     ap.add_argument("--partition", type=int, default=0, help="tokens per partition; 0 = default")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-rope", action="store_true",
+                    help="skip the side measurement of the step with RoPE fused in")
     ap.add_argument("--json-out", default="")
     return ap.parse_args()
 
@@ -431,6 +434,37 @@ def run_ours(args):
                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h)}
 
+    # ---- side measurement: the same step with the rotary embedding fused in
+    rope = None
+    if not args.no_rope:
+        max_pos = wl.max_blocks_per_seq * wl.block_size
+        table = torch.empty((max_pos, wl.head_dim // 2, 2), dtype=torch.float32, device="cuda")
+        P.photon_rope_cos_sin(ROPE_BASE, max_pos, wl.head_dim, table, stream)
+
+        def rope_step():
+            P.photon_paged_decode_step_rope(kn, vn, sm, q, kc, vc, bt, cl, table, max_pos,
+                                            wl.scale, out, ws, ws_bytes, shape, stream)
+
+        for _ in range(3):
+            flush_l2()
+            rope_step()
+        re = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(K)]
+        for i in range(K):
+            flush_l2()
+            re[i][0].record(stream)
+            rope_step()
+            re[i][1].record(stream)
+        torch.cuda.synchronize()
+        st, bits = P.photon_get_last_device_error(stream)
+        if st != 0:
+            raise RuntimeError(f"device error word {bits} during the RoPE steps")
+        rope_ms = sum(a.elapsed_time(b) for a, b in re) / K
+        rope = {"ms_per_step": round(rope_ms, 5),
+                "value": round(step_bytes / (rope_ms / 1e3) / 1e9, 2), "unit": "GB/s",
+                "rope_base": ROPE_BASE, "table_positions": max_pos,
+                "time_vs_plain_step": round(rope_ms / ms, 4)}
+
     peak, peak_kind = measured_peaks()
     if peak is None:
         peak = FALLBACK_HBM_GBS
@@ -467,6 +501,7 @@ def run_ours(args):
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": e2e,
+            "rope_step": rope,
             "gpu_launches": K * plan["kernels_per_call"],
             "clocks": clocks,
             "wall_ms_per_step_incl_flush": round(1e3 * t_wall / K, 4),

@@ -153,6 +153,41 @@ photon_status_t photon_paged_decode_step(const void* k_new, const void* v_new,
                                          const photon_paged_shape_t* shape,
                                          photon_stream_t stream);
 
+/* Rotary position embedding table for photon_paged_decode_step_rope (README
+ * "Key features / GPU-optimized kernels": batched RoPE among the fused
+ * kernels).  Writes table[pos][k] = (cos theta, sin theta) as two fp32 values,
+ * theta = pos * base^(-2k / head_dim), for 0 <= pos < max_positions and
+ * 0 <= k < head_dim / 2; angles are formed and evaluated in double and
+ * rounded once to fp32.  `table` (device, 8-byte aligned, owned by the caller)
+ * holds max_positions * head_dim / 2 float pairs = max_positions * head_dim * 4
+ * bytes.  base must be finite and > 1, head_dim even and > 0, max_positions
+ * > 0 with max_positions * head_dim / 2 <= 2^31; otherwise
+ * PHOTON_ERR_INVALID_ARG.  Build it once per model; it is read-only to the
+ * decode step. */
+photon_status_t photon_rope_cos_sin(double base, int32_t max_positions, int32_t head_dim,
+                                    void* table, photon_stream_t stream);
+
+/* photon_paged_decode_step with the rotary embedding of the step's new token
+ * fused in.  q and k_new arrive unrotated; for sequence b at position
+ * pos = context_lens[b] - 1, every q head row and every k_new head row is
+ * turned pairwise (rotate-half form): for k < d/2,
+ *   y[k]       = x[k] cos(theta) - x[k + d/2] sin(theta)
+ *   y[k + d/2] = x[k + d/2] cos(theta) + x[k] sin(theta)
+ * with (cos, sin) = rope_cos_sin[pos][k] from photon_rope_cos_sin for the same
+ * head_dim.  The cache is assumed to hold already-rotated keys (every earlier
+ * step stored its key rotated); values are never rotated.  The rotated new key
+ * row, rounded to the stored dtype, is what is attended and what is stored at
+ * slot_mapping[b]; the rotated q row stays fp32 for the scores.  A position
+ * >= max_positions (rows of the table) sets device error bit 16 and that
+ * sequence is attended and stored unrotated.  Everything else -- layouts,
+ * slot precondition, workspace, errors -- as photon_paged_decode_step;
+ * rope_cos_sin must be 8-byte aligned and max_positions > 0. */
+photon_status_t photon_paged_decode_step_rope(
+    const void* k_new, const void* v_new, const int64_t* slot_mapping, const void* q,
+    void* k_cache, void* v_cache, const int32_t* block_tables, const int32_t* context_lens,
+    const void* rope_cos_sin, int32_t max_positions, float scale, void* out, void* workspace,
+    size_t workspace_bytes, const photon_paged_shape_t* shape, photon_stream_t stream);
+
 /* photon_paged_decode without a caller-provided workspace.  The pages have no
  * counterpart of this call; it exists for callers that cannot allocate device
  * memory for the decode: an engine that reserved nearly all of HBM for its KV
@@ -192,8 +227,11 @@ photon_status_t photon_paged_gather(const void* k_cache, const void* v_cache,
  * error word.  Returns PHOTON_ERR_DEVICE_BOUNDS if any kernel of this library
  * skipped an out-of-range index since the last call, PHOTON_ERR_CUDA if the
  * synchronisation itself failed, PHOTON_OK otherwise.  If `bits` is not NULL
- * it receives the word: 1 = block id out of range, 2 = slot out of range,
- * 4 = context length out of range. */
+ * it receives the word: 1 = block id out of range, 2 = slot out of range (or,
+ * in the fused step, not the block table's slot for the new position),
+ * 4 = context length out of range, 8 = a bounded wait inside a kernel ran out
+ * (the call's output is then incomplete), 16 = a RoPE position outside the
+ * cos/sin table. */
 photon_status_t photon_get_last_device_error(photon_stream_t stream, uint32_t* bits);
 
 /* Static text for a status code (never NULL). */

@@ -5,7 +5,8 @@ baseline leg may import this package.  The product path (the CUDA library and
 its Python binding) never touches it and shares no code with it.
 
 The arithmetic lives in ``paged_ref.c`` (plain loops in double); this module
-builds it with gcc and wraps it with ctypes and numpy.  Every function states
+builds it with gcc and wraps it with ctypes and numpy.  ``scheduler.py`` holds
+the plain-Python oracle of the host scheduler (integer bookkeeping only).  Every function states
 which passage of the PhotonInfer README it restates; see the C file's header
 for the formula and the layouts.
 """
@@ -58,6 +59,10 @@ def _load():
     lib.ref_merge.restype = None
     lib.ref_widen.argtypes = [P, ctypes.c_size_t, i32, P]
     lib.ref_widen.restype = None
+    lib.ref_rope.argtypes = [P, i32, i64, f64, P]
+    lib.ref_rope.restype = None
+    lib.ref_paged_decode_q64.argtypes = [P, P, P, P, P, f64, P] + [i32] * 9
+    lib.ref_paged_decode_q64.restype = ctypes.c_int
     for fn in (lib.ref_cache_write, lib.ref_gather, lib.ref_paged_decode,
                lib.ref_paged_decode_row, lib.ref_attend_range):
         fn.restype = ctypes.c_int
@@ -179,4 +184,81 @@ def widen(a: np.ndarray, dtype: Optional[int] = None) -> np.ndarray:
     a = np.ascontiguousarray(a)
     out = np.empty(a.shape, np.float64)
     lib.ref_widen(_ptr(a), a.size, _dtype_code(a, dtype), _ptr(out))
+    return out
+
+
+def rope(x, pos: int, base: float) -> np.ndarray:
+    """Rotate-half rotary position embedding of the last axis of x (float64),
+    every row at position pos (the README lists batched RoPE among its fused
+    operations)."""
+    lib = _load()
+    x = np.ascontiguousarray(x, np.float64)
+    d = x.shape[-1]
+    flat = x.reshape(-1, d)
+    out = np.empty_like(flat)
+    for r in range(flat.shape[0]):
+        lib.ref_rope(_ptr(flat[r]), d, int(pos), float(base), out[r].ctypes.data)
+    return out.reshape(x.shape)
+
+
+def rope_cos_sin(base: float, max_positions: int, head_dim: int) -> np.ndarray:
+    """(cos, sin) of every position and pair, float64 [max_positions][d/2][2]:
+    the rotation of the vector with ones in its lower half and zeros in its
+    upper half has cos theta_k at k and sin theta_k at k + d/2."""
+    half = head_dim // 2
+    x = np.concatenate([np.ones(half), np.zeros(half)])
+    out = np.empty((max_positions, half, 2))
+    for pos in range(max_positions):
+        y = rope(x, pos, base)
+        out[pos, :, 0] = y[:half]
+        out[pos, :, 1] = y[half:]
+    return out
+
+
+def rope_step(wl, base: float, num_threads: int = 1):
+    """Oracle of the decode step with RoPE: the q rows and the new K rows are
+    rotated (rope) by the new token's position, context_len - 1; the rotated K
+    rows are stored in the storage dtype (round to nearest even) by the cache
+    write; the decode then attends with the rotated q rows, kept in double.
+    Returns (k_cache, v_cache, out float64 [B][Hq][d])."""
+    B = wl.num_seqs
+    q64 = widen(wl.q, wl.dtype)
+    k64 = widen(wl.k_new, wl.dtype)
+    q_rot = np.empty_like(q64)
+    k_rot = np.empty_like(k64)
+    for b in range(B):
+        pos = max(int(wl.context_lens[b]) - 1, 0)
+        q_rot[b] = rope(q64[b], pos, base)
+        k_rot[b] = rope(k64[b], pos, base)
+    kc, vc = wl.k_cache.copy(), wl.v_cache.copy()
+    cache_write(narrow(k_rot, wl.dtype), wl.v_new, wl.slot_mapping, kc, vc,
+                block_size=wl.block_size, dtype=wl.dtype)
+    out = paged_decode_q64(q_rot, kc, vc, wl.block_tables, wl.context_lens, wl.scale,
+                           dtype=wl.dtype, num_threads=num_threads)
+    return kc, vc, out
+
+
+def narrow(x64: np.ndarray, dtype: int) -> np.ndarray:
+    """float64 -> storage dtype, round to nearest even (bf16 through fp32)."""
+    if dtype == 0:
+        return x64.astype(np.float32)
+    if dtype == 1:
+        return x64.astype(np.float16)
+    b = x64.astype(np.float32).view(np.uint32)
+    return ((b + np.uint32(0x7FFF) + ((b >> np.uint32(16)) & np.uint32(1))) >> np.uint32(16)
+            ).astype(np.uint16)
+
+
+def paged_decode_q64(q64, k_cache, v_cache, block_tables, context_lens, scale: float, *,
+                     dtype: int, num_threads: int = 1) -> np.ndarray:
+    """paged_decode with the query rows given in float64 (already widened)."""
+    lib = _load()
+    q64 = np.ascontiguousarray(q64, np.float64)
+    B, Hq, d = q64.shape
+    NB, Hkv, bs, _ = k_cache.shape
+    MBS = block_tables.shape[1]
+    out = np.empty((B, Hq, d), dtype=np.float64)
+    _check(lib.ref_paged_decode_q64(_ptr(q64), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables),
+                                    _ptr(context_lens), float(scale), _ptr(out), B, Hq, Hkv, d,
+                                    bs, NB, MBS, int(dtype), int(num_threads)))
     return out

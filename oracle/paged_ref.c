@@ -11,7 +11,10 @@
  *   - "Key features / GPU-optimized kernels": batched paged attention over a
  *     block-wise KV cache, softmax computed in a numerically stable way;
  *   - "Technical details / Paged attention": block-wise KV cache, per-sequence
- *     cache offsets, one batched cache-write operation for many sequences.
+ *     cache offsets, one batched cache-write operation for many sequences;
+ *   - "Key features / GPU-optimized kernels": batched RoPE among the fused
+ *     operations (ref_rope: rotate-half form, theta_k = pos * base^(-2k/d),
+ *     the plain reading of the rotary embedding; the page names no variant).
  * The page prints no formula.  Its plain reading, used here, is scaled
  * dot-product attention of one query row per sequence over that sequence's
  * cached keys/values, with grouped query heads:
@@ -149,6 +152,7 @@ int ref_gather(const void* k_cache, const void* v_cache, const int32_t* block_ta
 /* ---------------------------------------------------------------- attention */
 typedef struct {
   const void *q, *k_cache, *v_cache;
+  const double* q64;  /* optional: query rows already in double (then q is unused) */
   const int32_t *block_tables, *context_lens;
   double scale;
   int32_t B, Hq, Hkv, d, bs, NB, MBS, dtype;
@@ -177,8 +181,10 @@ static int attend_range(const ref_problem* P, int32_t b, int32_t h, int64_t j0, 
     int64_t r = row_offset(P, b, kvh, j);
     if (r < 0) return REF_BAD_BLOCK;
     double dot = 0.0;
-    for (int32_t i = 0; i < d; ++i)
-      dot += load(P->q, qoff + i, P->dtype) * load(P->k_cache, (size_t)r + i, P->dtype);
+    for (int32_t i = 0; i < d; ++i) {
+      const double qi = P->q64 ? P->q64[qoff + i] : load(P->q, qoff + i, P->dtype);
+      dot += qi * load(P->k_cache, (size_t)r + i, P->dtype);
+    }
     s[j - j0] = P->scale * dot;
     if (s[j - j0] > m) m = s[j - j0];
   }
@@ -248,7 +254,7 @@ int ref_paged_decode(const void* q, const void* k_cache, const void* v_cache,
                      double* out, int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                      int32_t head_dim, int32_t block_size, int32_t num_blocks,
                      int32_t max_blocks_per_seq, int32_t dtype, int32_t num_threads) {
-  ref_problem P = {q, k_cache, v_cache, block_tables, context_lens, scale, num_seqs,
+  ref_problem P = {q, k_cache, v_cache, NULL, block_tables, context_lens, scale, num_seqs,
                    num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
                    max_blocks_per_seq, dtype};
   int rc = check_problem(&P);
@@ -288,7 +294,7 @@ int ref_paged_decode_row(const void* q, const void* k_cache, const void* v_cache
                          int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                          int32_t block_size, int32_t num_blocks, int32_t max_blocks_per_seq,
                          int32_t dtype) {
-  ref_problem P = {q, k_cache, v_cache, block_tables, context_lens, scale, num_seqs,
+  ref_problem P = {q, k_cache, v_cache, NULL, block_tables, context_lens, scale, num_seqs,
                    num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
                    max_blocks_per_seq, dtype};
   int rc = check_problem(&P);
@@ -308,7 +314,7 @@ int ref_attend_range(const void* q, const void* k_cache, const void* v_cache,
                      double* o, int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
                      int32_t head_dim, int32_t block_size, int32_t num_blocks,
                      int32_t max_blocks_per_seq, int32_t dtype) {
-  ref_problem P = {q, k_cache, v_cache, block_tables, context_lens, scale, num_seqs,
+  ref_problem P = {q, k_cache, v_cache, NULL, block_tables, context_lens, scale, num_seqs,
                    num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
                    max_blocks_per_seq, dtype};
   int rc = check_problem(&P);
@@ -349,4 +355,59 @@ void ref_merge(int32_t num_parts, const double* m, const double* l, const double
  * pools without relying on any other decoder). */
 void ref_widen(const void* src, size_t n, int32_t dtype, double* dst) {
   for (size_t i = 0; i < n; ++i) dst[i] = load(src, i, dtype);
+}
+
+/* ---------------------------------------------------------------- RoPE
+ * Rotary position embedding, rotate-half form (the Llama / Qwen convention;
+ * the README's "Key features / GPU-optimized kernels" lists batched RoPE among
+ * the fused operations, without a formula).  For k < d/2, with
+ * theta_k = pos * base^(-2k/d):
+ *   y[k]       = x[k] cos(theta_k) - x[k + d/2] sin(theta_k)
+ *   y[k + d/2] = x[k + d/2] cos(theta_k) + x[k] sin(theta_k)
+ * In double, on already-widened values. */
+void ref_rope(const double* x, int32_t head_dim, int64_t pos, double base, double* y) {
+  const int32_t half = head_dim / 2;
+  for (int32_t k = 0; k < half; ++k) {
+    const double theta = (double)pos * pow(base, -2.0 * (double)k / (double)head_dim);
+    const double c = cos(theta), s = sin(theta);
+    const double a = x[k], b = x[k + half];
+    y[k] = a * c - b * s;
+    y[k + half] = b * c + a * s;
+  }
+}
+
+/* ref_paged_decode with the query rows given in double (used for rotated
+ * queries, which are never stored). */
+int ref_paged_decode_q64(const double* q64, const void* k_cache, const void* v_cache,
+                         const int32_t* block_tables, const int32_t* context_lens, double scale,
+                         double* out, int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                         int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                         int32_t max_blocks_per_seq, int32_t dtype, int32_t num_threads) {
+  ref_problem P = {NULL, k_cache, v_cache, q64, block_tables, context_lens, scale, num_seqs,
+                   num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                   max_blocks_per_seq, dtype};
+  int rc = check_problem(&P);
+  if (rc) return rc;
+  if (num_threads < 1) num_threads = 1;
+  if (num_threads > 256) num_threads = 256;
+  pthread_t tid[256];
+  worker_arg args[256];
+  for (int32_t t = 0; t < num_threads; ++t) {
+    args[t].P = &P;
+    args[t].out = out;
+    args[t].first = t;
+    args[t].stride = num_threads;
+    args[t].rc = REF_OK;
+  }
+  int32_t started = 0;
+  for (int32_t t = 1; t < num_threads; ++t) {
+    if (pthread_create(&tid[t], NULL, worker, &args[t]) != 0) break;
+    ++started;
+  }
+  worker(&args[0]);
+  for (int32_t t = 1 + started; t < num_threads; ++t) worker(&args[t]);
+  for (int32_t t = 1; t <= started; ++t) pthread_join(tid[t], NULL);
+  for (int32_t t = 0; t < num_threads; ++t)
+    if (args[t].rc) return args[t].rc;
+  return REF_OK;
 }

@@ -27,6 +27,7 @@ __all__ = [
     "photon_paged_gather", "photon_get_last_device_error", "photon_status_string",
     "photon_paged_decode_plan", "photon_debug_set_attention_events",
     "photon_paged_decode_noalloc", "photon_paged_decode_step",
+    "photon_rope_cos_sin", "photon_paged_decode_step_rope", "Scheduler",
     "F32", "F16", "BF16", "STATUS",
 ]
 
@@ -95,20 +96,42 @@ def _load() -> ctypes.CDLL:
     lib.photon_paged_decode_noalloc.argtypes = [P, P, P, P, P, ctypes.c_float, P, SP, P]
     lib.photon_paged_decode_step.argtypes = [P, P, P, P, P, P, P, P, ctypes.c_float, P, P, SZ,
                                              SP, P]
+    lib.photon_rope_cos_sin.argtypes = [ctypes.c_double, I32, I32, P, P]
+    lib.photon_paged_decode_step_rope.argtypes = [P, P, P, P, P, P, P, P, P, I32,
+                                                  ctypes.c_float, P, P, SZ, SP, P]
+    # host scheduler (include/photon_scheduler.h)
+    lib.photon_scheduler_create.argtypes = [P, ctypes.POINTER(P)]
+    lib.photon_scheduler_destroy.argtypes = [P]
+    lib.photon_scheduler_destroy.restype = None
+    lib.photon_scheduler_add_request.argtypes = [P, ctypes.c_int64, I32, I32]
+    lib.photon_scheduler_schedule.argtypes = [P, P, P, P, P, P, P]
+    lib.photon_scheduler_update.argtypes = [P, P, P, P]
+    lib.photon_scheduler_stats.argtypes = [P, P, P, P, P]
+    lib.photon_scheduler_request_state.argtypes = [P, ctypes.c_int64, P, P, P, P]
+    for fn in ("photon_scheduler_create", "photon_scheduler_add_request",
+               "photon_scheduler_schedule", "photon_scheduler_update",
+               "photon_scheduler_stats", "photon_scheduler_request_state"):
+        getattr(lib, fn).restype = ctypes.c_int
     for fn in ("photon_cache_write", "photon_paged_decode", "photon_paged_gather",
                "photon_get_last_device_error", "photon_paged_decode_plan",
                "photon_debug_set_attention_events", "photon_paged_decode_noalloc",
-               "photon_paged_decode_step"):
+               "photon_paged_decode_step", "photon_rope_cos_sin",
+               "photon_paged_decode_step_rope"):
         getattr(lib, fn).restype = ctypes.c_int
     _lib = lib
     return lib
 
 
+HEADERS = ("photon_paged.h", "photon_scheduler.h")
+
+
 def exported_symbols() -> Tuple[str, ...]:
-    """Names of the functions declared in include/photon_paged.h."""
-    hdr = os.path.join(_build.INCLUDE, "photon_paged.h")
-    text = open(hdr).read()
-    return tuple(sorted(set(re.findall(r"^\S.*?\b(photon_\w+)\(", text, re.M))))
+    """Names of the functions declared in the library's public headers."""
+    names = set()
+    for h in HEADERS:
+        text = open(os.path.join(_build.INCLUDE, h)).read()
+        names.update(re.findall(r"^\S.*?\b(photon_\w+)\(", text, re.M))
+    return tuple(sorted(names))
 
 
 def _string(status: int) -> str:
@@ -177,6 +200,27 @@ def photon_paged_decode_step(k_new, v_new, slot_mapping, q, k_cache, v_cache, bl
                                             _stream(stream)), "photon_paged_decode_step")
 
 
+def photon_rope_cos_sin(base: float, max_positions: int, head_dim: int, table,
+                        stream=None) -> None:
+    """Fills table ([max_positions][head_dim/2] pairs of fp32) with the rotary
+    embedding's (cos, sin) for every position and pair."""
+    _check(_load().photon_rope_cos_sin(float(base), int(max_positions), int(head_dim),
+                                       _ptr(table), _stream(stream)), "photon_rope_cos_sin")
+
+
+def photon_paged_decode_step_rope(k_new, v_new, slot_mapping, q, k_cache, v_cache,
+                                  block_tables, context_lens, rope_cos_sin, max_positions: int,
+                                  scale: float, out, workspace, workspace_bytes: int,
+                                  shape: PagedShape, stream=None) -> None:
+    """photon_paged_decode_step with q and the new K rows rotated by RoPE at
+    position context_len - 1."""
+    _check(_load().photon_paged_decode_step_rope(
+        _ptr(k_new), _ptr(v_new), _ptr(slot_mapping), _ptr(q), _ptr(k_cache), _ptr(v_cache),
+        _ptr(block_tables), _ptr(context_lens), _ptr(rope_cos_sin), int(max_positions),
+        float(scale), _ptr(out), _ptr(workspace), int(workspace_bytes), ctypes.byref(shape),
+        _stream(stream)), "photon_paged_decode_step_rope")
+
+
 def photon_paged_decode_noalloc(q, k_cache, v_cache, block_tables, context_lens, scale: float,
                                 out, shape: PagedShape, stream=None) -> None:
     """photon_paged_decode with the library's built-in 32 MiB scratch instead of a
@@ -219,3 +263,6 @@ def photon_debug_set_attention_events(start_event=None, stop_event=None) -> None
         return ev.cuda_event if hasattr(ev, "cuda_event") else int(ev)
     _check(_load().photon_debug_set_attention_events(raw(start_event), raw(stop_event)),
            "photon_debug_set_attention_events")
+
+
+from .scheduler import Scheduler  # noqa: E402  (needs _load and PhotonError above)

@@ -35,7 +35,9 @@ def nvcc_path() -> str:
 
 
 def sources() -> List[str]:
-    return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    """CUDA translation units and the plain host C++ ones (compiled by nvcc too,
+    which hands .cpp files to the host compiler)."""
+    return sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
 
 
 def _deps() -> List[str]:
@@ -61,7 +63,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False,
         flags = flags + ["-Xptxas", "-v"]
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(BUILD_DIR, os.path.splitext(os.path.basename(src))[0] + ".o")
         cmd = [nvcc] + flags + ["-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:

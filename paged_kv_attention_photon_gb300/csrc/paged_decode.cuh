@@ -86,7 +86,8 @@ struct StageHdr {
   int flags;           // kFirst | kLast | kDone, valid-block mask << 8
   // fused step: the stage block (new_warp) whose row new_row is this
   // sequence's new token, to be stored at physical block new_phys; -1 if none
-  int new_warp, new_phys, new_row, pad;
+  int new_warp, new_phys, new_row;
+  int pos;             // the sequence's new-token position, ctx - 1 (RoPE angle)
 };
 enum : int { kFirst = 1, kLast = 2, kDone = 4 };
 
@@ -199,6 +200,73 @@ __device__ __forceinline__ void attend_block(const T* __restrict__ ks, const T* 
   }
 }
 
+// ------------------------------------------------------------------ RoPE
+// Rotate-half rotary embedding: for k < D/2 the pair (x[k], x[k + D/2]) turns
+// by the table's (cos, sin) for (pos, k).  Positions outside the table are
+// flagged and left unrotated.
+//
+// q rows, in the lane's registers: lane c of a row group holds chunks
+// c, c + 8, ... of each row; a pair's partner sits in the same lane when the
+// chunk distance D/2/kChunk is a multiple of 8, otherwise (16-bit D = 64) in
+// lane c ^ 4 of the same row group.
+template <typename T, int D, int G>
+__device__ __forceinline__ void rope_q(float (&qf)[G][DecodeCfg<T, D, G>::kEPL],
+                                       const float2* __restrict__ cs, int max_pos, int pos,
+                                       int c, uint32_t* err, int ctid) {
+  using C = DecodeCfg<T, D, G>;
+  constexpr int kHalfChunks = (D / 2) / C::kChunk;
+  constexpr bool kInLane = kHalfChunks % 8 == 0;
+  constexpr int kSlotShift = kInLane ? (kHalfChunks / 8) * C::kChunk : 0;
+  if (pos < 0 || pos >= max_pos) {
+    if (ctid == 0) raise_error(err, kErrPosition);
+    return;
+  }
+  const float2* row = cs + (size_t)pos * (D / 2);
+  if constexpr (kInLane) {
+    // slots of the lower half are the first kEPL/2; each one's partner is
+    // kSlotShift further on in the same lane
+#pragma unroll
+    for (int s = 0; s < C::kEPL / 2; ++s) {
+      const int e = (c + 8 * (s / C::kChunk)) * C::kChunk + s % C::kChunk;
+      const float2 t = __ldg(row + e);
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const float x0 = qf[g][s], x1 = qf[g][s + kSlotShift];
+        qf[g][s] = x0 * t.x - x1 * t.y;
+        qf[g][s + kSlotShift] = x1 * t.x + x0 * t.y;
+      }
+    }
+  } else {
+    const bool lower = c < 4;
+#pragma unroll
+    for (int s = 0; s < C::kEPL; ++s) {
+      const int e = (c + 8 * (s / C::kChunk)) * C::kChunk + s % C::kChunk;
+      const float2 t = __ldg(row + (lower ? e : e - D / 2));
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const float x = qf[g][s];
+        const float partner = __shfl_xor_sync(0xffffffffu, x, 4);
+        qf[g][s] = lower ? x * t.x - partner * t.y : x * t.x + partner * t.y;
+      }
+    }
+  }
+}
+
+// One row of D elements in shared memory, rotated in place by a warp and
+// rounded back to the storage type.
+template <typename T, int D>
+__device__ __forceinline__ void rope_row(T* row, const float2* __restrict__ cs, int max_pos,
+                                         int pos, int lane) {
+  if (pos < 0 || pos >= max_pos) return;  // flagged by rope_q of the same item
+  const float2* t = cs + (size_t)pos * (D / 2);
+  for (int k = lane; k < D / 2; k += 32) {
+    const float2 w = __ldg(t + k);
+    const float x0 = Elem<T>::to_f32(row[k]), x1 = Elem<T>::to_f32(row[k + D / 2]);
+    row[k] = Elem<T>::narrow(x0 * w.x - x1 * w.y);
+    row[k + D / 2] = Elem<T>::narrow(x1 * w.x + x0 * w.y);
+  }
+}
+
 // Arrive-and-wait of the NC consumer warps on `bar` (bounded).
 __device__ __forceinline__ bool consumer_sync(uint64_t* bar, uint32_t& phase, int lane) {
   __syncwarp();
@@ -222,7 +290,10 @@ static __device__ unsigned long long g_probe[kProbeCtas][kProbeSlots];
 #endif
 
 // ------------------------------------------------------------------ attention kernel
-template <typename T, int D, int G, int NC, int S>
+// kRope: the fused step with the rotary embedding (q rows and the new K row
+// turn by the token's position); a separate instantiation, so the plain path
+// carries none of it.
+template <typename T, int D, int G, int NC, int S, bool kRope>
 __global__ void __launch_bounds__((NC + 1) * 32, 1)
     paged_decode_attention_kernel(const DecodeArgs a) {
   using PC = PersistCfg<T, D, G, NC, S>;
@@ -389,6 +460,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
       it.p = run == 0 ? rel - excl : nfull;
       it.tok_end = run == 0 ? (it.p + 1) * a.part : ctxj;
       it.nparts = nfull + (ctxj % a.part != 0 ? 1 : 0);
+      if constexpr (kRope) it.ctx = ctxj;
       return true;
     };
     // Lane j holds the physical block of logical block (chunk*32 + j) of the item.
@@ -490,7 +562,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
           h.new_warp = new_lane;
           h.new_phys = new_lane >= 0 ? new_phys : -1;
           h.new_row = new_lane >= 0 ? new_rows - 1 : -1;
-          h.pad = 0;
+          h.pos = kRope ? it0.ctx - 1 : 0;
           hdr[slot] = h;
           mbar_arrive_expect_tx(&full[slot], (uint32_t)(bytes + (first ? PC::kQBytes : 0)));
         }
@@ -601,15 +673,30 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
           Elem<T>::widen(raw, t);
 #pragma unroll
           for (int e = 0; e < C::kChunk; ++e) {
-            qf[g][i * C::kChunk + e] = t[e] * a.qscale;
+            qf[g][i * C::kChunk + e] = kRope ? t[e] : t[e] * a.qscale;
             o[g][i * C::kChunk + e] = 0.f;
           }
         }
+      }
+      if constexpr (kRope) {
+        // turn the raw rows first, then scale them like the plain path
+        rope_q<T, D, G>(qf, a.rope_cs, a.rope_max_pos, h.pos, c, a.err, ctid);
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+#pragma unroll
+          for (int e = 0; e < C::kEPL; ++e) qf[g][e] *= a.qscale;
       }
     }
     if (warp < h.nblk && ((h.flags >> (8 + warp)) & 1)) {
       const T* stage = reinterpret_cast<const T*>(smem + PC::kOffKV + slot * PC::kStageBytes);
       const int n_valid = min(kBlockSize, h.tok_end - (h.blk0 + warp) * kBlockSize);
+      if (kRope && warp == h.new_warp) {
+        // fused step with RoPE: turn the new K row by its position, in place,
+        // before it is attended and stored
+        rope_row<T, D>(const_cast<T*>(stage) + warp * PC::kBlockElems + h.new_row * D, a.rope_cs,
+                       a.rope_max_pos, h.pos, lane);
+        __syncwarp();
+      }
       attend_block<T, D, G>(stage + warp * PC::kBlockElems, stage + (NC + warp) * PC::kBlockElems,
                             n_valid, qf, m, l, o, lane);
       if (warp == h.new_warp) {
@@ -812,7 +899,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) paged_decode_merge_kernel(co
 
 // Resident CTAs per SM of an attention-kernel instantiation (queried once per
 // device, after raising its dynamic shared-memory limit).
-template <typename T, int D, int G, int NC, int S>
+template <typename T, int D, int G, int NC, int S, bool kRope>
 int attention_ctas_per_sm() {
   using PC = PersistCfg<T, D, G, NC, S>;
   constexpr int kMaxDev = 64;
@@ -820,7 +907,7 @@ int attention_ctas_per_sm() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
   if (cache[dev] > 0) return cache[dev];
-  auto kern = paged_decode_attention_kernel<T, D, G, NC, S>;
+  auto kern = paged_decode_attention_kernel<T, D, G, NC, S, kRope>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PC::kSmemBytes) !=
       cudaSuccess)
     return 0;
@@ -859,13 +946,18 @@ cudaError_t launch_decode_impl(const DecodeArgs& a0, cudaStream_t stream) {
   if (!a.q || !a.k_cache || !a.v_cache || !a.block_tables || !a.context_lens || !a.out ||
       !a.ws_m || !a.ws_l || !a.ws_o || !a.ws_ctrl || !a.err)
     return cudaErrorInvalidValue;
-  const int per_sm = attention_ctas_per_sm<T, D, G, NC, S>();
+  const bool rope = a.rope_cs != nullptr;
+  const int per_sm = rope ? attention_ctas_per_sm<T, D, G, NC, S, true>()
+                          : attention_ctas_per_sm<T, D, G, NC, S, false>();
   if (per_sm <= 0) return cudaErrorInvalidConfiguration;
   const int grid = per_sm * a.num_sms;
 
   if (a.ev_start) cudaEventRecord(a.ev_start, stream);
-  cudaError_t err = launch_pdl(paged_decode_attention_kernel<T, D, G, NC, S>, dim3(grid),
-                               dim3(PC::kThreads), PC::kSmemBytes, stream, a);
+  cudaError_t err =
+      rope ? launch_pdl(paged_decode_attention_kernel<T, D, G, NC, S, true>, dim3(grid),
+                        dim3(PC::kThreads), PC::kSmemBytes, stream, a)
+           : launch_pdl(paged_decode_attention_kernel<T, D, G, NC, S, false>, dim3(grid),
+                        dim3(PC::kThreads), PC::kSmemBytes, stream, a);
   if (err != cudaSuccess) return err;
   const int items = a.B * a.Hq;
   err = launch_pdl(paged_decode_merge_kernel<T, D>, dim3((items + kMergeWarps - 1) / kMergeWarps),

@@ -209,7 +209,8 @@ photon_status_t decode_common(const void* q, const void* k_cache, const void* v_
                               float scale, void* out, void* workspace, size_t workspace_bytes,
                               const photon_paged_shape_t* shape, photon_stream_t stream,
                               const void* k_new, const void* v_new,
-                              const int64_t* slot_mapping) {
+                              const int64_t* slot_mapping, const void* rope_cos_sin,
+                              int32_t rope_max_positions) {
   photon_status_t st = check_shape(shape);
   if (st != PHOTON_OK) return st;
   if (!std::isfinite(scale)) return PHOTON_ERR_INVALID_ARG;
@@ -247,6 +248,8 @@ photon_status_t decode_common(const void* q, const void* k_cache, const void* v_
   a.slot_mapping = slot_mapping;
   a.k_cache_w = k_new ? const_cast<void*>(k_cache) : nullptr;
   a.v_cache_w = k_new ? const_cast<void*>(v_cache) : nullptr;
+  a.rope_cs = static_cast<const float2*>(rope_cos_sin);
+  a.rope_max_pos = rope_cos_sin ? rope_max_positions : 0;
   a.err = err;
   a.qscale = (float)((double)scale * 1.4426950408889634);  // scale * log2(e)
   a.B = shape->num_seqs;
@@ -281,7 +284,7 @@ photon_status_t photon_paged_decode(const void* q, const void* k_cache, const vo
                                     size_t workspace_bytes, const photon_paged_shape_t* shape,
                                     photon_stream_t stream) {
   return decode_common(q, k_cache, v_cache, block_tables, context_lens, scale, out, workspace,
-                       workspace_bytes, shape, stream, nullptr, nullptr, nullptr);
+                       workspace_bytes, shape, stream, nullptr, nullptr, nullptr, nullptr, 0);
 }
 
 photon_status_t photon_paged_decode_step(const void* k_new, const void* v_new,
@@ -299,7 +302,39 @@ photon_status_t photon_paged_decode_step(const void* k_new, const void* v_new,
   if (!aligned16(k_new) || !aligned16(v_new) || (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
     return PHOTON_ERR_MISALIGNED;
   return decode_common(q, k_cache, v_cache, block_tables, context_lens, scale, out, workspace,
-                       workspace_bytes, shape, stream, k_new, v_new, slot_mapping);
+                       workspace_bytes, shape, stream, k_new, v_new, slot_mapping, nullptr, 0);
+}
+
+photon_status_t photon_rope_cos_sin(double base, int32_t max_positions, int32_t head_dim,
+                                    void* table, photon_stream_t stream) {
+  if (!(base > 1.0) || !std::isfinite(base) || max_positions <= 0 || head_dim <= 0 ||
+      head_dim % 2 != 0)
+    return PHOTON_ERR_INVALID_ARG;
+  if ((long long)max_positions * (head_dim / 2) > (1ll << 31)) return PHOTON_ERR_INVALID_ARG;
+  if (!table) return PHOTON_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(table) & 7u) return PHOTON_ERR_MISALIGNED;
+  return photon::launch_rope_table(base, max_positions, head_dim, static_cast<float2*>(table),
+                                   reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PHOTON_OK
+             : PHOTON_ERR_CUDA;
+}
+
+photon_status_t photon_paged_decode_step_rope(
+    const void* k_new, const void* v_new, const int64_t* slot_mapping, const void* q,
+    void* k_cache, void* v_cache, const int32_t* block_tables, const int32_t* context_lens,
+    const void* rope_cos_sin, int32_t max_positions, float scale, void* out, void* workspace,
+    size_t workspace_bytes, const photon_paged_shape_t* shape, photon_stream_t stream) {
+  photon_status_t st = check_shape(shape);
+  if (st != PHOTON_OK) return st;
+  if (shape->num_seqs == 0) return PHOTON_OK;
+  if (!k_new || !v_new || !slot_mapping || !rope_cos_sin || max_positions <= 0)
+    return PHOTON_ERR_INVALID_ARG;
+  if (!aligned16(k_new) || !aligned16(v_new) || (reinterpret_cast<uintptr_t>(slot_mapping) & 7u) ||
+      (reinterpret_cast<uintptr_t>(rope_cos_sin) & 7u))
+    return PHOTON_ERR_MISALIGNED;
+  return decode_common(q, k_cache, v_cache, block_tables, context_lens, scale, out, workspace,
+                       workspace_bytes, shape, stream, k_new, v_new, slot_mapping, rope_cos_sin,
+                       max_positions);
 }
 
 photon_status_t photon_paged_gather(const void* k_cache, const void* v_cache,

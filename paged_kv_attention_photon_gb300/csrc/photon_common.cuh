@@ -10,7 +10,7 @@
 namespace photon {
 
 // Bits of the sticky device error word (see photon_get_last_device_error).
-enum : uint32_t { kErrBlock = 1u, kErrSlot = 2u, kErrContext = 4u };
+enum : uint32_t { kErrBlock = 1u, kErrSlot = 2u, kErrContext = 4u, kErrPosition = 16u };
 
 __device__ __forceinline__ void raise_error(uint32_t* word, uint32_t bit) {
   atomicOr(word, bit);
@@ -31,6 +31,7 @@ struct Elem<float> {
     f[3] = __uint_as_float(c.w);
   }
   __device__ __forceinline__ static float narrow(float x) { return x; }
+  __device__ __forceinline__ static float to_f32(float x) { return x; }
 };
 
 template <>
@@ -46,6 +47,7 @@ struct Elem<__half> {
     }
   }
   __device__ __forceinline__ static __half narrow(float x) { return __float2half_rn(x); }
+  __device__ __forceinline__ static float to_f32(__half x) { return __half2float(x); }
 };
 
 template <>
@@ -61,6 +63,7 @@ struct Elem<__nv_bfloat16> {
     }
   }
   __device__ __forceinline__ static __nv_bfloat16 narrow(float x) { return __float2bfloat16_rn(x); }
+  __device__ __forceinline__ static float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
 };
 
 // Streaming 16-byte global load that bypasses L1 allocation: every K/V byte
@@ -78,7 +81,7 @@ __device__ __forceinline__ uint4 ld_stream16(const void* p) {
 // is the exclusive end of the partition's token range, nparts the number of
 // partitions of the sequence.
 struct WorkItem {
-  int b, p, tok_end, nparts;
+  int b, p, tok_end, nparts, ctx;
 };
 
 struct DecodeArgs {
@@ -100,6 +103,10 @@ struct DecodeArgs {
   const int64_t* slot_mapping;
   void* k_cache_w;
   void* v_cache_w;
+  // Fused step with RoPE only (null otherwise): (cos, sin) per position and
+  // pair, [rope_max_pos][D/2]; q rows and the new K rows turn by ctx - 1.
+  const float2* rope_cs;
+  int rope_max_pos;
   uint32_t* err;      // sticky device error word
   float qscale;       // scale * log2(e): scores are kept in the log2 domain
   int B, Hq, Hkv, D, NB, MBS, part, pmax;
@@ -129,6 +136,8 @@ struct GatherArgs {
 };
 
 cudaError_t launch_cache_write(const CacheWriteArgs& a, cudaStream_t stream);
+cudaError_t launch_rope_table(double base, int max_pos, int d, float2* table,
+                              cudaStream_t stream);
 cudaError_t launch_gather(const GatherArgs& a, cudaStream_t stream);
 
 // One entry per storage dtype; each returns cudaErrorInvalidValue for a

@@ -76,6 +76,14 @@ class DeviceWorkload:
                                    self.context_lens, self.wl.scale, self.out, self.ws,
                                    self.ws_bytes, self.shape, stream)
 
+    def step_rope(self, table: torch.Tensor, max_positions: int, stream=None) -> None:
+        """Fused cache write + decode with RoPE (photon_paged_decode_step_rope)."""
+        P.photon_paged_decode_step_rope(self.k_new, self.v_new, self.slot_mapping, self.q,
+                                        self.k_cache, self.v_cache, self.block_tables,
+                                        self.context_lens, table, max_positions,
+                                        self.wl.scale, self.out, self.ws, self.ws_bytes,
+                                        self.shape, stream)
+
     def decode(self, scale=None, stream=None) -> None:
         P.photon_paged_decode(self.q, self.k_cache, self.v_cache, self.block_tables,
                               self.context_lens, self.wl.scale if scale is None else scale,
@@ -83,6 +91,13 @@ class DeviceWorkload:
 
     def out_f64(self) -> np.ndarray:
         return to_float64(self.out, self.wl.dtype)
+
+
+def rope_table(base: float, max_positions: int, head_dim: int) -> torch.Tensor:
+    """Device (cos, sin) table from photon_rope_cos_sin, fp32 [max_positions][d/2][2]."""
+    t = torch.empty((max_positions, head_dim // 2, 2), dtype=torch.float32, device="cuda")
+    P.photon_rope_cos_sin(base, max_positions, head_dim, t)
+    return t
 
 
 def assert_close(got: np.ndarray, want: np.ndarray, dtype: int, what: str = "") -> float:

@@ -110,3 +110,27 @@ def test_workspace_size_and_plan(lib):
 def test_events_hook_argument_check(lib):
     assert lib.photon_debug_set_attention_events(FAKE, None) == 1
     assert lib.photon_debug_set_attention_events(None, None) == 0
+
+
+def test_rope_entry_points_validation(lib):
+    f = lib.photon_rope_cos_sin
+    assert f(1e4, 16, 128, None, None) == 1
+    assert f(1.0, 16, 128, FAKE, None) == 1              # base must be > 1
+    assert f(math.nan, 16, 128, FAKE, None) == 1
+    assert f(math.inf, 16, 128, FAKE, None) == 1
+    assert f(1e4, 0, 128, FAKE, None) == 1
+    assert f(1e4, 16, 127, FAKE, None) == 1              # odd head_dim
+    assert f(1e4, 1 << 30, 128, FAKE, None) == 1         # table too large
+    assert f(1e4, 16, 128, FAKE + 4, None) == 3          # float2 alignment
+    g = lib.photon_paged_decode_step_rope
+    s = _shape()
+    args = lambda **o: [o.get("kn", FAKE), o.get("vn", FAKE), o.get("sm", FAKE), FAKE, FAKE,
+                        FAKE, FAKE, FAKE, o.get("cs", FAKE), o.get("mp", 4096), 0.1, FAKE2,
+                        FAKE2, 1 << 40, ctypes.byref(o.get("shape", s)), None]
+    assert g(*args(cs=None)) == 1
+    assert g(*args(mp=0)) == 1
+    assert g(*args(kn=None)) == 1
+    assert g(*args(cs=FAKE + 4)) == 3
+    assert g(*args(sm=FAKE + 4)) == 3
+    assert g(*args(shape=_shape(head_dim=96))) == 2
+    assert g(*args(shape=_shape(num_seqs=0), cs=None)) == 0    # empty batch: no-op

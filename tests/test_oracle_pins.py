@@ -412,3 +412,135 @@ def test_step_order_cache_write_then_decode():
     out = oracle.paged_decode(wl.q, kc, vc, wl.block_tables, wl.context_lens, 1.0)
     for b in range(3):
         np.testing.assert_allclose(out[b, 0], wl.v_new[b, 0].astype(np.float64), atol=1e-6)
+
+
+# --------------------------------------------------------------- rotary embedding
+# The README lists batched RoPE among the fused operations and names no
+# variant; the oracle takes the rotate-half form with theta_k = pos *
+# base^(-2k/d).  The pins below fix that reading against closed forms and the
+# algebra of rotations, not against the oracle's own formula.
+
+def test_rope_position_zero_is_identity():
+    x = np.random.default_rng(70).standard_normal((3, 128))
+    assert oracle.rope(x, 0, 1e6).tobytes() == x.tobytes()
+
+
+@pytest.mark.parametrize("pos", [1, 3])
+def test_rope_closed_form_base_10000_d8(pos):
+    """base 10000, d = 8: base^(-2k/8) = 10^(-k), so the unit vector e_k turns
+    into cos(pos 10^-k) e_k + sin(pos 10^-k) e_(k+4) and e_(k+4) into
+    -sin(pos 10^-k) e_k + cos(pos 10^-k) e_(k+4).  Pins the pairing (k with
+    k + d/2, not 2k with 2k+1), the exponent 2k/d, the base and the sign."""
+    for k in range(4):
+        ang = pos * 10.0 ** (-k)
+        c, s = math.cos(ang), math.sin(ang)
+        e = np.zeros(8)
+        e[k] = 1.0
+        want = np.zeros(8)
+        want[k], want[k + 4] = c, s
+        np.testing.assert_allclose(oracle.rope(e, pos, 10000.0), want, rtol=0, atol=1e-15)
+        e = np.zeros(8)
+        e[k + 4] = 1.0
+        want = np.zeros(8)
+        want[k], want[k + 4] = -s, c
+        np.testing.assert_allclose(oracle.rope(e, pos, 10000.0), want, rtol=0, atol=1e-15)
+
+
+def test_rope_preserves_every_pair_norm():
+    x = np.random.default_rng(71).standard_normal((5, 64))
+    y = oracle.rope(x, 4321, 5e5)
+    nx = x[:, :32] ** 2 + x[:, 32:] ** 2
+    ny = y[:, :32] ** 2 + y[:, 32:] ** 2
+    np.testing.assert_allclose(ny, nx, rtol=1e-13)
+
+
+def test_rope_scores_depend_only_on_relative_position():
+    """<R(m) q, R(n) k> = <R(m - n) q, k>: the property RoPE exists for."""
+    rng = np.random.default_rng(72)
+    q, k = rng.standard_normal(128), rng.standard_normal(128)
+    for m, n in [(5000, 1234), (17, 17), (8191, 0), (300, 301)]:
+        lhs = oracle.rope(q, m, 1e6) @ oracle.rope(k, n, 1e6)
+        rhs = oracle.rope(q, m - n, 1e6) @ k
+        assert abs(lhs - rhs) <= 1e-11 * (np.abs(q).sum() * np.abs(k).sum()), (m, n)
+
+
+def test_rope_composes_additively():
+    x = np.random.default_rng(73).standard_normal(128)
+    a = oracle.rope(oracle.rope(x, 700, 1e4), 900, 1e4)
+    np.testing.assert_allclose(a, oracle.rope(x, 1600, 1e4), rtol=0, atol=1e-11)
+
+
+def test_rope_d2_is_complex_rotation_by_pos():
+    """d = 2: one pair with frequency 1 whatever the base, i.e. multiplication
+    of x0 + i x1 by e^(i pos)."""
+    for pos in (1, 2, 100):
+        z = complex(0.3, -1.7) * complex(math.cos(pos), math.sin(pos))
+        y = oracle.rope(np.array([0.3, -1.7]), pos, 123.0)
+        np.testing.assert_allclose(y, [z.real, z.imag], rtol=0, atol=1e-14)
+
+
+def test_rope_cos_sin_table_rows():
+    t = oracle.rope_cos_sin(10000.0, 4, 8)
+    assert t.shape == (4, 4, 2)
+    np.testing.assert_array_equal(t[0], np.stack([np.ones(4), np.zeros(4)], -1))
+    for pos in range(4):
+        for k in range(4):
+            ang = pos * 10.0 ** (-k)
+            assert abs(t[pos, k, 0] - math.cos(ang)) <= 1e-15
+            assert abs(t[pos, k, 1] - math.sin(ang)) <= 1e-15
+
+
+@pytest.mark.parametrize("dtype", [W.DTYPE_F32, W.DTYPE_F16, W.DTYPE_BF16])
+def test_narrow_rounds_to_nearest_even_like_torch(dtype):
+    x = np.random.default_rng(74).standard_normal(4096) * 3.0
+    x[:4] = [1.0 + 2.0 ** -11, 1.0 + 3 * 2.0 ** -11, 1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8]  # ties
+    got = oracle.narrow(x, dtype)
+    t = torch.from_numpy(x)
+    if dtype == W.DTYPE_BF16:
+        want = t.to(torch.float32).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    else:
+        want = t.to(torch.float32 if dtype == W.DTYPE_F32 else torch.float16).numpy()
+    assert got.tobytes() == want.tobytes()
+
+
+@pytest.mark.parametrize("dtype", [W.DTYPE_F16, W.DTYPE_BF16])
+def test_decode_with_widened_q_equals_decode(dtype):
+    wl = W.random_small(75, batch=5, num_q_heads=8, num_kv_heads=2, head_dim=64, max_ctx=90,
+                        dtype=dtype)
+    a = oracle.paged_decode(wl.q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens,
+                            wl.scale, dtype=dtype)
+    b = oracle.paged_decode_q64(_to_f64(wl.q, dtype), wl.k_cache, wl.v_cache, wl.block_tables,
+                                wl.context_lens, wl.scale, dtype=dtype)
+    assert a.tobytes() == b.tobytes()
+
+
+def test_rope_step_at_position_zero_is_the_plain_step():
+    """Every context 1: the new token sits at position 0, where RoPE is the
+    identity, so the RoPE step equals cache write + decode bit for bit (a step
+    that turned by context_len instead of context_len - 1 would not)."""
+    wl = W.random_small(76, batch=6, num_q_heads=4, num_kv_heads=2, head_dim=64, max_ctx=1,
+                        dtype=W.DTYPE_F16, context_lens=[1] * 6)
+    kc, vc, out = oracle.rope_step(wl, 1e4)
+    kc2, vc2 = wl.k_cache.copy(), wl.v_cache.copy()
+    oracle.cache_write(wl.k_new, wl.v_new, wl.slot_mapping, kc2, vc2,
+                       block_size=wl.block_size, dtype=wl.dtype)
+    out2 = oracle.paged_decode(wl.q, kc2, vc2, wl.block_tables, wl.context_lens, wl.scale,
+                               dtype=wl.dtype)
+    assert kc.tobytes() == kc2.tobytes() and vc.tobytes() == vc2.tobytes()
+    assert out.tobytes() == out2.tobytes()
+
+
+def test_rope_step_stores_rotated_keys_and_plain_values():
+    """The stored K row of each sequence keeps the pair norms of k_new (a
+    rotation), differs from k_new (it did turn: positions > 0), and the V row
+    is stored unchanged."""
+    wl = W.random_small(77, batch=4, num_q_heads=4, num_kv_heads=2, head_dim=64, max_ctx=64,
+                        dtype=W.DTYPE_F32, context_lens=[5, 17, 33, 64])
+    kc, vc, _ = oracle.rope_step(wl, 1e4)
+    blk, off = wl.slot_mapping // wl.block_size, wl.slot_mapping % wl.block_size
+    k_st = kc[blk, :, off].astype(np.float64)
+    k_in = wl.k_new.astype(np.float64)
+    norm = lambda x: x[..., :32] ** 2 + x[..., 32:] ** 2
+    np.testing.assert_allclose(norm(k_st), norm(k_in), rtol=1e-6, atol=1e-6)
+    assert not np.allclose(k_st, k_in)
+    assert vc[blk, :, off].tobytes() == wl.v_new.tobytes()

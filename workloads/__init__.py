@@ -23,7 +23,7 @@ from __future__ import annotations
 
 import dataclasses
 import math
-from typing import Dict, List, Optional
+from typing import Tuple, Dict, List, Optional
 
 import numpy as np
 
@@ -291,6 +291,49 @@ def random_small(seed: int, *, batch: int, num_q_heads: int, num_kv_heads: int,
                  head_dim=head_dim, context_lens=ctx, num_blocks=max(nb, 1), dtype=dtype,
                  scale=(1.0 / math.sqrt(head_dim)) if scale is None else scale, rng=rng,
                  block_size=block_size, max_blocks_per_seq=mbs, seed=seed)
+
+
+def request_trace(seed: int, num_requests: int, *, max_prompt: int, max_new: int,
+                  pool_tokens: int, long_frac: float = 0.2,
+                  arrivals_per_step: float = 1.0) -> List[tuple]:
+    """Seeded serving trace for the scheduler: (arrival_step, request_id,
+    prompt_len, max_new_tokens), arrival order.  The prompt mix follows the
+    batch-256 serving step: long_frac of the prompts are long (uniform in
+    [max_prompt/4, max_prompt]), the rest short (uniform in [1, max_prompt/8]);
+    output lengths are uniform in [1, max_new]; arrivals are a Poisson stream
+    of arrivals_per_step per step.  Every request fits max_prompt + max_new - 1
+    tokens and the pool (pool_tokens)."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    out, t = [], 0.0
+    for i in range(num_requests):
+        t += rng.exponential(1.0 / arrivals_per_step)
+        if rng.uniform() < long_frac:
+            prompt = int(rng.integers(max(1, max_prompt // 4), max_prompt, endpoint=True))
+        else:
+            prompt = int(rng.integers(1, max(1, max_prompt // 8), endpoint=True))
+        new = int(rng.integers(1, max_new, endpoint=True))
+        new = max(1, min(new, pool_tokens - prompt + 1))
+        out.append((int(t), 1000 + i, prompt, new))
+    return out
+
+
+def request_rows(seed: int, request_id: int, num_tokens: int, num_kv_heads: int,
+                 head_dim: int, dtype: int) -> Tuple[np.ndarray, np.ndarray]:
+    """The K and V rows of every position of one request, [num_tokens][Hkv][d],
+    N(0,1) rounded to the storage dtype, a function of (seed, request_id) only:
+    a request that is preempted and recomputed writes the same rows again."""
+    rng = np.random.Generator(np.random.PCG64([seed, request_id]))
+    n = num_tokens * num_kv_heads * head_dim
+    k = _draw_values(rng, n, dtype).reshape(num_tokens, num_kv_heads, head_dim)
+    v = _draw_values(rng, n, dtype).reshape(num_tokens, num_kv_heads, head_dim)
+    return k, v
+
+
+def request_queries(seed: int, request_id: int, position: int, num_q_heads: int,
+                    head_dim: int, dtype: int) -> np.ndarray:
+    """The query rows [Hq][d] of one request at one position."""
+    rng = np.random.Generator(np.random.PCG64([seed, request_id, position, 7]))
+    return _draw_values(rng, num_q_heads * head_dim, dtype).reshape(num_q_heads, head_dim)
 
 
 NAMED = {
