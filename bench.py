@@ -44,6 +44,7 @@ import workloads as W  # noqa: E402
 
 METRIC = "paged-decode KV GB/s and fraction of GB300 HBM peak; decode tokens/s per layer"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 L2_FLUSH_BYTES = 512 << 20
 ROPE_BASE = 1.0e6          # rotary base of the Qwen family (the side measurement only)
 L2_CLEAN_BYTES = 256 << 20
@@ -61,6 +62,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-rope", action="store_true",
                     help="skip the side measurement of the step with RoPE fused in")
+    ap.add_argument("--no-mq", action="store_true",
+                    help="skip the side measurements of multi-query attention")
     ap.add_argument("--json-out", default="")
     return ap.parse_args()
 
@@ -101,6 +104,79 @@ def reduce_over_ranks(pg, ms, attn_ms, step_bytes, seqs, tokens):
     return float(t[0]), float(t[1]), float(tb[0]), float(tb[1]), float(tb[2])
 
 
+def measured_bf16_tflops():
+    """Dense bf16 tensor throughput (burst) from MEASURED_PEAKS.json, else the
+    fallback figure; fp16 runs at the same rate."""
+    try:
+        v = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))).get("bf16_tflops")
+        if isinstance(v, (int, float)):
+            return float(v), "measured"
+    except Exception:
+        pass
+    return FALLBACK_BF16_TFLOPS, "fallback"
+
+
+def multi_query_side(P, torch, stream, flush_l2, K, hbm_peak):
+    """Speculative-verify and chunked-prefill timings of photon_paged_multi_query."""
+    rng = np.random.Generator(np.random.PCG64(2))
+    ctx = W.qwen_context_lens(rng, 64)
+    cases = {
+        "verify_b64x4": (W.multi_query(311, query_lens=[4] * 64, prefix_lens=(ctx - 4).tolist(),
+                                       num_q_heads=16, num_kv_heads=8, head_dim=128,
+                                       dtype=W.DTYPE_F16), "hbm"),
+        "prefill_b16x1024": (W.multi_query(320, query_lens=[1024] * 16,
+                                           prefix_lens=[0] * 8 + [4096] * 8, num_q_heads=16,
+                                           num_kv_heads=8, head_dim=128, dtype=W.DTYPE_F16),
+                             "tensor"),
+    }
+    tpeak, tkind = measured_bf16_tflops()
+    res = {}
+
+    def dev(a):
+        a = np.ascontiguousarray(a)
+        return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).cuda()
+
+    for name, (mq, bound) in cases.items():
+        p = mq.pool
+        shape = P.PagedShape.make(**p.shape_dict())
+        q, kc, vc = dev(mq.q), dev(p.k_cache), dev(p.v_cache)
+        bt, cl, qs = dev(p.block_tables), dev(p.context_lens), dev(mq.query_start)
+        out = torch.empty_like(q)
+
+        def call():
+            P.photon_paged_multi_query(q, kc, vc, bt, cl, qs, mq.num_tokens, mq.max_query_len,
+                                       p.scale, out, shape, stream)
+
+        for _ in range(3):
+            flush_l2()
+            call()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(K)]
+        for i in range(K):
+            flush_l2()
+            ev[i][0].record(stream)
+            call()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        st, bits = P.photon_get_last_device_error(stream)
+        if st != 0:
+            raise RuntimeError(f"device error word {bits} in multi-query {name}")
+        ms = sum(a.elapsed_time(b) for a, b in ev) / K
+        gbs = mq.kv_bytes() / (ms / 1e3) / 1e9
+        tfs = mq.flops() / (ms / 1e3) / 1e12
+        achieved, peak, unit = (gbs, hbm_peak, "GB/s") if bound == "hbm" else \
+            (tfs, tpeak, "TFLOP/s")
+        res[name] = {"ms_per_call": round(ms, 5), "tokens": mq.num_tokens,
+                     "kv_GBps": round(gbs, 1), "TFLOPs": round(tfs, 2),
+                     "roofline": {"bound": bound, "achieved": round(achieved, 2),
+                                  "peak": peak, "unit": unit,
+                                  "frac": round(achieved / peak, 4),
+                                  "peak_source": "measured" if bound == "hbm" else tkind},
+                     "algorithmic_bytes": mq.kv_bytes(), "flops": mq.flops()}
+        del q, kc, vc, bt, cl, qs, out
+    return res
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -121,12 +197,16 @@ def measured_peaks():
     return (v, "measured") if v else (None, "fallback")
 
 
+# The sources the decode attention kernel is compiled from.
+ATTENTION_SOURCES = ("photon_common.cuh", "paged_decode.cuh", "paged_decode_f16.cu",
+                     "paged_decode_bf16.cu", "paged_decode_f32.cu")
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_attention_photon_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh")):
-            h.update(open(os.path.join(csrc, f), "rb").read())
+    for f in ATTENTION_SOURCES:
+        h.update(open(os.path.join(csrc, f), "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -468,6 +548,9 @@ def run_ours(args):
     peak, peak_kind = measured_peaks()
     if peak is None:
         peak = FALLBACK_HBM_GBS
+    mq_side = None
+    if not args.no_mq:
+        mq_side = multi_query_side(P, torch, stream, flush_l2, K, peak)
     achieved = decode_bytes / (attn_mean_ms / 1e3) / 1e9
     roofline = {"bound": "hbm",
                 "kernel": "paged_decode_attention_kernel + paged_decode_merge_kernel",
@@ -502,6 +585,7 @@ def run_ours(args):
             "cpu_baseline": cpu,
             "e2e": e2e,
             "rope_step": rope,
+            "multi_query": mq_side,
             "gpu_launches": K * plan["kernels_per_call"],
             "clocks": clocks,
             "wall_ms_per_step_incl_flush": round(1e3 * t_wall / K, 4),

@@ -188,6 +188,39 @@ photon_status_t photon_paged_decode_step_rope(
     const void* rope_cos_sin, int32_t max_positions, float scale, void* out, void* workspace,
     size_t workspace_bytes, const photon_paged_shape_t* shape, photon_stream_t stream);
 
+/* Multi-query causal attention over the paged cache (README "Technical
+ * details / Paged attention"; "Roadmap": FlashAttention-2 style attention for
+ * long sequences): the chunked-prefill / speculative-verification form of
+ * photon_paged_decode.  Sequence b has n_b = query_start[b+1] - query_start[b]
+ * new query tokens, rows query_start[b] .. query_start[b+1]-1 of q; they are
+ * the LAST n_b tokens of its context, so query token i sits at position
+ * p_i = context_lens[b] - n_b + i, and its K/V rows must already be in the
+ * cache (photon_cache_write first).  For every such token and q head h:
+ *     out[query_start[b] + i][h] = sum_{j <= p_i} softmax_j(scale * q . K_j[kvh]) V_j[kvh]
+ * (causal: keys 0 .. p_i of the sequence, kvh = h / G), in fp32 arithmetic
+ * from fp16/bf16 operands on the tensor cores, out rounded to the stored
+ * dtype.  n_b = 1 is exactly the decode row of photon_paged_decode.
+ *   q, out        [num_tokens][num_q_heads][head_dim]
+ *   query_start   int32 [num_seqs + 1], non-decreasing, query_start[0] >= 0,
+ *                 query_start[num_seqs] <= num_tokens
+ *   max_query_len host upper bound of every n_b (sizes the launch)
+ * dtype must be PHOTON_F16 or PHOTON_BF16 (PHOTON_ERR_UNSUPPORTED for f32).
+ * No workspace.  Device-side errors (never a fault): n_b < 0, n_b >
+ * max_query_len or rows outside [0, num_tokens) set bit 32 and that sequence
+ * is skipped (rows past max_query_len are zeroed when they are in range);
+ * n_b > context_lens[b] or a context outside [0, max_blocks_per_seq *
+ * block_size] sets bit 4 and zeroes the sequence's rows; a block id outside
+ * the pool sets bit 1 and its keys read as zeros (that sequence's output is
+ * then not meaningful).  num_seqs == 0, num_tokens == 0 or max_query_len == 0
+ * is a no-op. */
+photon_status_t photon_paged_multi_query(const void* q, const void* k_cache, const void* v_cache,
+                                         const int32_t* block_tables,
+                                         const int32_t* context_lens,
+                                         const int32_t* query_start, int32_t num_tokens,
+                                         int32_t max_query_len, float scale, void* out,
+                                         const photon_paged_shape_t* shape,
+                                         photon_stream_t stream);
+
 /* photon_paged_decode without a caller-provided workspace.  The pages have no
  * counterpart of this call; it exists for callers that cannot allocate device
  * memory for the decode: an engine that reserved nearly all of HBM for its KV
@@ -231,7 +264,8 @@ photon_status_t photon_paged_gather(const void* k_cache, const void* v_cache,
  * in the fused step, not the block table's slot for the new position),
  * 4 = context length out of range, 8 = a bounded wait inside a kernel ran out
  * (the call's output is then incomplete), 16 = a RoPE position outside the
- * cos/sin table. */
+ * cos/sin table, 32 = inconsistent query_start / max_query_len of
+ * photon_paged_multi_query. */
 photon_status_t photon_get_last_device_error(photon_stream_t stream, uint32_t* bits);
 
 /* Static text for a status code (never NULL). */

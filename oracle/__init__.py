@@ -238,6 +238,32 @@ def rope_step(wl, base: float, num_threads: int = 1):
     return kc, vc, out
 
 
+def multi_query(q, k_cache, v_cache, block_tables, context_lens, query_start, scale: float, *,
+                dtype: int, num_threads: int = 1) -> np.ndarray:
+    """Causal multi-query attention (chunked prefill / verification), float64
+    [T][Hq][d].  Sequence b's query rows query_start[b] .. query_start[b+1]-1
+    are its last n_b tokens; token i sits at position context_lens[b] - n_b + i
+    and attends to the keys at positions 0 .. that position.  Written as what
+    it is: one decode row per query token, over the same block table with the
+    context cut at the token's own position."""
+    qs = np.asarray(query_start, dtype=np.int64)
+    B = qs.shape[0] - 1
+    rows_b, rows_ctx = [], []
+    for b in range(B):
+        n = int(qs[b + 1] - qs[b])
+        first = int(context_lens[b]) - n
+        for i in range(n):
+            rows_b.append(b)
+            rows_ctx.append(first + i + 1)
+    if not rows_b:
+        return np.zeros((0,) + tuple(q.shape[1:]))
+    tables = np.ascontiguousarray(np.asarray(block_tables)[rows_b])
+    ctx = np.asarray(rows_ctx, dtype=np.int32)
+    qq = np.ascontiguousarray(q[int(qs[0]):int(qs[-1])])
+    return paged_decode(qq, k_cache, v_cache, tables, ctx, scale, dtype=dtype,
+                        num_threads=num_threads)
+
+
 def narrow(x64: np.ndarray, dtype: int) -> np.ndarray:
     """float64 -> storage dtype, round to nearest even (bf16 through fp32)."""
     if dtype == 0:

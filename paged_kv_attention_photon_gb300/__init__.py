@@ -27,7 +27,8 @@ __all__ = [
     "photon_paged_gather", "photon_get_last_device_error", "photon_status_string",
     "photon_paged_decode_plan", "photon_debug_set_attention_events",
     "photon_paged_decode_noalloc", "photon_paged_decode_step",
-    "photon_rope_cos_sin", "photon_paged_decode_step_rope", "Scheduler",
+    "photon_rope_cos_sin", "photon_paged_decode_step_rope", "photon_paged_multi_query",
+    "Scheduler",
     "F32", "F16", "BF16", "STATUS",
 ]
 
@@ -99,6 +100,9 @@ def _load() -> ctypes.CDLL:
     lib.photon_rope_cos_sin.argtypes = [ctypes.c_double, I32, I32, P, P]
     lib.photon_paged_decode_step_rope.argtypes = [P, P, P, P, P, P, P, P, P, I32,
                                                   ctypes.c_float, P, P, SZ, SP, P]
+    lib.photon_paged_multi_query.argtypes = [P, P, P, P, P, P, I32, I32, ctypes.c_float, P, SP,
+                                             P]
+    lib.photon_paged_multi_query.restype = ctypes.c_int
     # host scheduler (include/photon_scheduler.h)
     lib.photon_scheduler_create.argtypes = [P, ctypes.POINTER(P)]
     lib.photon_scheduler_destroy.argtypes = [P]
@@ -219,6 +223,16 @@ def photon_paged_decode_step_rope(k_new, v_new, slot_mapping, q, k_cache, v_cach
         _ptr(block_tables), _ptr(context_lens), _ptr(rope_cos_sin), int(max_positions),
         float(scale), _ptr(out), _ptr(workspace), int(workspace_bytes), ctypes.byref(shape),
         _stream(stream)), "photon_paged_decode_step_rope")
+
+
+def photon_paged_multi_query(q, k_cache, v_cache, block_tables, context_lens, query_start,
+                             num_tokens: int, max_query_len: int, scale: float, out,
+                             shape: PagedShape, stream=None) -> None:
+    """Causal attention of the last n_b tokens of each sequence over its cache."""
+    _check(_load().photon_paged_multi_query(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
+        _ptr(query_start), int(num_tokens), int(max_query_len), float(scale), _ptr(out),
+        ctypes.byref(shape), _stream(stream)), "photon_paged_multi_query")
 
 
 def photon_paged_decode_noalloc(q, k_cache, v_cache, block_tables, context_lens, scale: float,

@@ -46,13 +46,6 @@
 
 #include "photon_common.cuh"
 
-// PHOTON_FAST_EXP selects the PTX ex2.approx.ftz instruction (relative error
-// about 2^-22; results below 2^-126 flush to zero) for the softmax weights
-// instead of the exp2f library call.
-#ifndef PHOTON_FAST_EXP
-#define PHOTON_FAST_EXP 1
-#endif
-
 namespace photon {
 
 template <typename T, int D, int G>
@@ -66,16 +59,6 @@ struct DecodeCfg {
   static constexpr int kSteps = kBlockSize / kRowsPerStep;    // load steps per block
   static_assert(kRowChunks % kLanesPerRow == 0, "row must split over 8 lanes");
 };
-
-__device__ __forceinline__ float softmax_exp2(float x) {
-#if PHOTON_FAST_EXP
-  float y;
-  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-#else
-  return exp2f(x);
-#endif
-}
 
 // Stage header written by the producer, read by the consumers after the
 // stage's full barrier completes.

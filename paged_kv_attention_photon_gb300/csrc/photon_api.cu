@@ -337,6 +337,52 @@ photon_status_t photon_paged_decode_step_rope(
                        max_positions);
 }
 
+photon_status_t photon_paged_multi_query(const void* q, const void* k_cache, const void* v_cache,
+                                         const int32_t* block_tables,
+                                         const int32_t* context_lens,
+                                         const int32_t* query_start, int32_t num_tokens,
+                                         int32_t max_query_len, float scale, void* out,
+                                         const photon_paged_shape_t* shape,
+                                         photon_stream_t stream) {
+  photon_status_t st = check_shape(shape);
+  if (st != PHOTON_OK) return st;
+  if (shape->dtype == PHOTON_F32) return PHOTON_ERR_UNSUPPORTED;
+  if (!std::isfinite(scale) || num_tokens < 0 || max_query_len < 0) return PHOTON_ERR_INVALID_ARG;
+  if (shape->num_seqs == 0 || num_tokens == 0 || max_query_len == 0) return PHOTON_OK;
+  if (shape->num_seqs > 65535 || shape->num_kv_heads > 65535) return PHOTON_ERR_UNSUPPORTED;
+  if ((int64_t)max_query_len * (shape->num_q_heads / shape->num_kv_heads) > INT_MAX / 2)
+    return PHOTON_ERR_INVALID_ARG;
+  if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !query_start || !out)
+    return PHOTON_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(block_tables) ||
+      !aligned16(context_lens) || !aligned16(query_start) || !aligned16(out))
+    return PHOTON_ERR_MISALIGNED;
+  uint32_t* err = nullptr;
+  if ((st = error_word(&err)) != PHOTON_OK) return st;
+  photon::MultiQueryArgs a{};
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.block_tables = block_tables;
+  a.context_lens = context_lens;
+  a.query_start = query_start;
+  a.out = out;
+  a.err = err;
+  a.qscale = (float)((double)scale * 1.4426950408889634);  // scale * log2(e)
+  a.B = shape->num_seqs;
+  a.Hq = shape->num_q_heads;
+  a.Hkv = shape->num_kv_heads;
+  a.D = shape->head_dim;
+  a.NB = shape->num_blocks;
+  a.MBS = shape->max_blocks_per_seq;
+  a.max_query_len = max_query_len;
+  a.num_tokens = num_tokens;
+  a.dtype = shape->dtype;
+  return photon::launch_multi_query(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PHOTON_OK
+             : PHOTON_ERR_CUDA;
+}
+
 photon_status_t photon_paged_gather(const void* k_cache, const void* v_cache,
                                     const int32_t* block_tables, const int32_t* context_lens,
                                     void* k_dense, void* v_dense,

@@ -10,7 +10,9 @@
 namespace photon {
 
 // Bits of the sticky device error word (see photon_get_last_device_error).
-enum : uint32_t { kErrBlock = 1u, kErrSlot = 2u, kErrContext = 4u, kErrPosition = 16u };
+enum : uint32_t {
+  kErrBlock = 1u, kErrSlot = 2u, kErrContext = 4u, kErrPosition = 16u, kErrQuery = 32u
+};
 
 __device__ __forceinline__ void raise_error(uint32_t* word, uint32_t bit) {
   atomicOr(word, bit);
@@ -65,6 +67,23 @@ struct Elem<__nv_bfloat16> {
   __device__ __forceinline__ static __nv_bfloat16 narrow(float x) { return __float2bfloat16_rn(x); }
   __device__ __forceinline__ static float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
 };
+
+// PHOTON_FAST_EXP selects the PTX ex2.approx.ftz instruction (relative error
+// about 2^-22; results below 2^-126 flush to zero) for the softmax weights
+// instead of the exp2f library call.
+#ifndef PHOTON_FAST_EXP
+#define PHOTON_FAST_EXP 1
+#endif
+
+__device__ __forceinline__ float softmax_exp2(float x) {
+#if PHOTON_FAST_EXP
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+#else
+  return exp2f(x);
+#endif
+}
 
 // Streaming 16-byte global load that bypasses L1 allocation: every K/V byte
 // of a decode step is read exactly once.
@@ -145,6 +164,24 @@ cudaError_t launch_gather(const GatherArgs& a, cudaStream_t stream);
 cudaError_t launch_paged_decode_f32(const DecodeArgs& a, cudaStream_t stream);
 cudaError_t launch_paged_decode_f16(const DecodeArgs& a, cudaStream_t stream);
 cudaError_t launch_paged_decode_bf16(const DecodeArgs& a, cudaStream_t stream);
+
+// Multi-query (causal) paged attention: query_start[b] .. query_start[b+1]-1
+// are sequence b's new query tokens, the last ones of its context.
+struct MultiQueryArgs {
+  const void* q;
+  const void* k_cache;
+  const void* v_cache;
+  const int32_t* block_tables;
+  const int32_t* context_lens;
+  const int32_t* query_start;
+  void* out;
+  uint32_t* err;
+  float qscale;       // scale * log2(e)
+  int B, Hq, Hkv, D, NB, MBS, max_query_len;
+  int num_tokens;     // rows of q and out
+  int dtype;          // 1 = fp16, 2 = bf16
+};
+cudaError_t launch_multi_query(const MultiQueryArgs& a, cudaStream_t stream);
 
 
 // Launch with programmatic stream serialization: the kernel may be scheduled

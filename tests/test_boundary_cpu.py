@@ -134,3 +134,23 @@ def test_rope_entry_points_validation(lib):
     assert g(*args(sm=FAKE + 4)) == 3
     assert g(*args(shape=_shape(head_dim=96))) == 2
     assert g(*args(shape=_shape(num_seqs=0), cs=None)) == 0    # empty batch: no-op
+
+
+def test_multi_query_validation(lib):
+    f = lib.photon_paged_multi_query
+    s = _shape()
+    args = lambda **o: [o.get("q", FAKE), FAKE, FAKE, FAKE, FAKE, o.get("qs", FAKE),
+                        o.get("T", 64), o.get("maxq", 16), o.get("scale", 0.1), o.get("out", FAKE2),
+                        ctypes.byref(o.get("shape", s)), None]
+    assert f(*args(shape=_shape(dtype=P.F32))) == 2            # tensor-core path: 16-bit only
+    assert f(*args(shape=_shape(head_dim=96))) == 2
+    assert f(*args(qs=None)) == 1
+    assert f(*args(q=None)) == 1
+    assert f(*args(T=-1)) == 1
+    assert f(*args(maxq=-1)) == 1
+    assert f(*args(scale=math.nan)) == 1
+    assert f(*args(qs=FAKE + 4)) == 3
+    assert f(*args(out=FAKE2 + 2)) == 3
+    assert f(*args(T=0, q=None, qs=None, out=None)) == 0        # no tokens: no-op
+    assert f(*args(maxq=0, q=None)) == 0
+    assert f(*args(shape=_shape(num_seqs=0), q=None)) == 0

@@ -544,3 +544,63 @@ def test_rope_step_stores_rotated_keys_and_plain_values():
     np.testing.assert_allclose(norm(k_st), norm(k_in), rtol=1e-6, atol=1e-6)
     assert not np.allclose(k_st, k_in)
     assert vc[blk, :, off].tobytes() == wl.v_new.tobytes()
+
+
+# --------------------------------------------------------------- multi-query (causal)
+@pytest.mark.parametrize("dtype", [W.DTYPE_F16, W.DTYPE_BF16, W.DTYPE_F32])
+def test_multi_query_equals_dense_causal_torch(dtype):
+    """A torch float64 causal attention on dense K/V the test pages itself:
+    query token i of sequence b (position first_b + i) sees keys 0..first_b+i,
+    through an explicit upper-triangular -inf mask on the full score matrix."""
+    rng = np.random.default_rng(900 + dtype)
+    Hq, Hkv, d, bs = 8, 2, 16, 16
+    n = np.array([1, 5, 16, 3, 0, 20], np.int32)          # new tokens per sequence
+    prefix = np.array([0, 11, 16, 40, 7, 1], np.int32)
+    ctx = prefix + n
+    B, S = len(ctx), int(ctx.max())
+    dk = _draw(rng, (B, Hkv, S, d), dtype)
+    dv = _draw(rng, (B, Hkv, S, d), dtype)
+    T = int(n.sum())
+    q = _draw(rng, (T, Hq, d), dtype)
+    qs = np.concatenate([[0], np.cumsum(n)]).astype(np.int32)
+    kc, vc, tables = _page(dk, dv, ctx, bs, rng)
+    scale = 0.9 / math.sqrt(d)
+    got = oracle.multi_query(q, kc, vc, tables, ctx, qs, scale, dtype=dtype)
+    q64, k64, v64 = _to_f64(q, dtype), _to_f64(dk, dtype), _to_f64(dv, dtype)
+    G = Hq // Hkv
+    for b in range(B):
+        if n[b] == 0:
+            continue
+        c = int(ctx[b])
+        K = torch.from_numpy(k64[b, :, :c]).repeat_interleave(G, dim=0)     # [Hq][c][d]
+        V = torch.from_numpy(v64[b, :, :c]).repeat_interleave(G, dim=0)
+        Q = torch.from_numpy(q64[qs[b]:qs[b + 1]]).transpose(0, 1)          # [Hq][n][d]
+        s = torch.matmul(Q, K.transpose(1, 2)) * scale                      # [Hq][n][c]
+        i = torch.arange(int(n[b])).unsqueeze(1) + int(prefix[b])
+        j = torch.arange(c).unsqueeze(0)
+        s = s.masked_fill(j > i, float("-inf"))
+        want = torch.matmul(torch.softmax(s, dim=-1), V).transpose(0, 1).numpy()
+        np.testing.assert_allclose(got[qs[b]:qs[b + 1]], want, rtol=0, atol=1e-12)
+
+
+def test_multi_query_with_one_token_is_the_decode():
+    wl = W.random_small(78, batch=6, num_q_heads=8, num_kv_heads=2, head_dim=64, max_ctx=200,
+                        dtype=W.DTYPE_F16, context_lens=[1, 17, 64, 100, 150, 200])
+    qs = np.arange(7, dtype=np.int32)
+    a = oracle.multi_query(wl.q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens, qs,
+                           wl.scale, dtype=wl.dtype)
+    assert a.tobytes() == _decode_wl(wl).tobytes()
+
+
+def test_multi_query_first_token_of_a_fresh_prompt_returns_its_v():
+    """A prompt with no prefix: its first token sees only itself, so its output
+    is its own V row exactly, whatever q and K are."""
+    mq = W.multi_query(79, query_lens=[4, 9], prefix_lens=[0, 0], num_q_heads=4, num_kv_heads=2,
+                       head_dim=64, dtype=W.DTYPE_F32)
+    p = mq.pool
+    out = oracle.multi_query(mq.q, p.k_cache, p.v_cache, p.block_tables, p.context_lens,
+                             mq.query_start, p.scale, dtype=p.dtype)
+    for b in range(2):
+        blk = p.block_tables[b, 0]
+        v0 = p.v_cache[blk, :, 0].astype(np.float64)              # [Hkv][d], position 0
+        np.testing.assert_array_equal(out[mq.query_start[b]], np.repeat(v0, 2, axis=0))

@@ -336,6 +336,59 @@ def request_queries(seed: int, request_id: int, position: int, num_q_heads: int,
     return _draw_values(rng, num_q_heads * head_dim, dtype).reshape(num_q_heads, head_dim)
 
 
+@dataclasses.dataclass
+class MultiQueryWorkload:
+    """A paged pool whose sequences end in query_lens[b] new tokens (their K/V
+    rows already in the pool) plus the query rows of those tokens."""
+    pool: Workload            # pool, block tables, context lengths (= prefix + new)
+    q: np.ndarray             # [T][Hq][d]
+    query_start: np.ndarray   # int32 [B + 1]
+    max_query_len: int
+
+    @property
+    def num_tokens(self) -> int:
+        return int(self.query_start[-1])
+
+    def flops(self) -> int:
+        """Multiply-adds x 2 of QK^T and PV over the causal key ranges."""
+        p = self.pool
+        n = np.diff(self.query_start).astype(np.int64)
+        first = p.context_lens.astype(np.int64) - n
+        keys = (n * first + n * (n + 1) // 2).sum()          # sum over tokens of (pos + 1)
+        return int(4 * keys * p.num_q_heads * p.head_dim)
+
+    def kv_bytes(self) -> int:
+        """K/V rows read once per (sequence, KV head), plus q and out."""
+        p = self.pool
+        kv = int(p.context_lens.astype(np.int64).sum()) * p.num_kv_heads * p.head_dim * \
+            p.elem_bytes * 2
+        return kv + 2 * self.q.nbytes
+
+
+def multi_query(seed: int, *, query_lens, prefix_lens, num_q_heads: int, num_kv_heads: int,
+                head_dim: int, dtype: int, extra_blocks: int = 3,
+                scale: Optional[float] = None) -> MultiQueryWorkload:
+    """Chunked-prefill / speculative-verify input: sequence b has prefix_lens[b]
+    cached tokens followed by query_lens[b] new tokens whose K/V rows are
+    already written; values N(0,1) in the storage dtype, blocks permuted."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    n = np.asarray(query_lens, dtype=np.int32)
+    ctx = (np.asarray(prefix_lens, dtype=np.int64) + n).astype(np.int32)
+    bs = 16
+    mbs = max(1, (int(ctx.max(initial=0)) + bs - 1) // bs)
+    nb = int(((ctx.astype(np.int64) + bs - 1) // bs).sum()) + extra_blocks
+    pool = build(f"mq_s{seed}", num_q_heads=num_q_heads, num_kv_heads=num_kv_heads,
+                 head_dim=head_dim, context_lens=ctx, num_blocks=max(nb, 1), dtype=dtype,
+                 scale=(1.0 / math.sqrt(head_dim)) if scale is None else scale, rng=rng,
+                 block_size=bs, max_blocks_per_seq=mbs, seed=seed)
+    T = int(n.sum())
+    q = _draw_values(rng, T * num_q_heads * head_dim, dtype).reshape(T, num_q_heads, head_dim)
+    qs = np.zeros(n.shape[0] + 1, dtype=np.int32)
+    qs[1:] = np.cumsum(n)
+    return MultiQueryWorkload(pool=pool, q=q, query_start=qs,
+                              max_query_len=int(n.max(initial=0)))
+
+
 NAMED = {
     "tiny": tiny,
     "llama_b16": llama_b16,
