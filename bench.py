@@ -142,26 +142,34 @@ def multi_query_side(P, torch, stream, flush_l2, K, hbm_peak):
         q, kc, vc = dev(mq.q), dev(p.k_cache), dev(p.v_cache)
         bt, cl, qs = dev(p.block_tables), dev(p.context_lens), dev(mq.query_start)
         out = torch.empty_like(q)
+        nws = P.photon_paged_multi_query_workspace_size(shape, mq.num_tokens, mq.max_query_len)
+        ws = torch.empty(max(nws, 16), dtype=torch.uint8, device="cuda")
 
         def call():
             P.photon_paged_multi_query(q, kc, vc, bt, cl, qs, mq.num_tokens, mq.max_query_len,
-                                       p.scale, out, shape, stream)
+                                       p.scale, out, ws, nws, shape, stream)
 
-        for _ in range(3):
-            flush_l2()
-            call()
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(K)]
-        for i in range(K):
-            flush_l2()
-            ev[i][0].record(stream)
-            call()
-            ev[i][1].record(stream)
-        torch.cuda.synchronize()
-        st, bits = P.photon_get_last_device_error(stream)
-        if st != 0:
-            raise RuntimeError(f"device error word {bits} in multi-query {name}")
-        ms = sum(a.elapsed_time(b) for a, b in ev) / K
+        def timed(which):
+            P.photon_debug_set_multi_query_kernel(which)
+            for _ in range(3):
+                flush_l2()
+                call()
+            ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                  for _ in range(K)]
+            for i in range(K):
+                flush_l2()
+                ev[i][0].record(stream)
+                call()
+                ev[i][1].record(stream)
+            torch.cuda.synchronize()
+            P.photon_debug_set_multi_query_kernel(0)
+            st, bits = P.photon_get_last_device_error(stream)
+            if st != 0:
+                raise RuntimeError(f"device error word {bits} in multi-query {name}")
+            return sum(a.elapsed_time(b) for a, b in ev) / K
+
+        ms = timed(0)
+        ms_tc = timed(2)
         gbs = mq.kv_bytes() / (ms / 1e3) / 1e9
         tfs = mq.flops() / (ms / 1e3) / 1e12
         achieved, peak, unit = (gbs, hbm_peak, "GB/s") if bound == "hbm" else \
@@ -172,8 +180,13 @@ def multi_query_side(P, torch, stream, flush_l2, K, hbm_peak):
                                   "peak": peak, "unit": unit,
                                   "frac": round(achieved / peak, 4),
                                   "peak_source": "measured" if bound == "hbm" else tkind},
-                     "algorithmic_bytes": mq.kv_bytes(), "flops": mq.flops()}
-        del q, kc, vc, bt, cl, qs, out
+                     "algorithmic_bytes": mq.kv_bytes(), "flops": mq.flops(),
+                     "split_kv_workspace_bytes": int(nws),
+                     "tcgen05_kernel": {"ms_per_call": round(ms_tc, 5),
+                                        "TFLOPs": round(mq.flops() / (ms_tc / 1e3) / 1e12, 2),
+                                        "kv_GBps": round(mq.kv_bytes() / (ms_tc / 1e3) / 1e9,
+                                                         1)}}
+        del q, kc, vc, bt, cl, qs, out, ws
     return res
 
 

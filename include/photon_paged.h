@@ -158,7 +158,7 @@ photon_status_t photon_paged_decode_step(const void* k_new, const void* v_new,
  * kernels).  Writes table[pos][k] = (cos theta, sin theta) as two fp32 values,
  * theta = pos * base^(-2k / head_dim), for 0 <= pos < max_positions and
  * 0 <= k < head_dim / 2; angles are formed and evaluated in double and
- * rounded once to fp32.  `table` (device, 8-byte aligned, owned by the caller)
+ * rounded once to fp32.  `table` (device, 16-byte aligned, owned by the caller)
  * holds max_positions * head_dim / 2 float pairs = max_positions * head_dim * 4
  * bytes.  base must be finite and > 1, head_dim even and > 0, max_positions
  * > 0 with max_positions * head_dim / 2 <= 2^31; otherwise
@@ -181,7 +181,7 @@ photon_status_t photon_rope_cos_sin(double base, int32_t max_positions, int32_t 
  * >= max_positions (rows of the table) sets device error bit 16 and that
  * sequence is attended and stored unrotated.  Everything else -- layouts,
  * slot precondition, workspace, errors -- as photon_paged_decode_step;
- * rope_cos_sin must be 8-byte aligned and max_positions > 0. */
+ * rope_cos_sin must be 16-byte aligned and max_positions > 0. */
 photon_status_t photon_paged_decode_step_rope(
     const void* k_new, const void* v_new, const int64_t* slot_mapping, const void* q,
     void* k_cache, void* v_cache, const int32_t* block_tables, const int32_t* context_lens,
@@ -205,7 +205,10 @@ photon_status_t photon_paged_decode_step_rope(
  *                 query_start[num_seqs] <= num_tokens
  *   max_query_len host upper bound of every n_b (sizes the launch)
  * dtype must be PHOTON_F16 or PHOTON_BF16 (PHOTON_ERR_UNSUPPORTED for f32).
- * No workspace.  Device-side errors (never a fault): n_b < 0, n_b >
+ * workspace: device scratch of at least
+ * photon_paged_multi_query_workspace_size() bytes (may be NULL when that is
+ * 0), owned by the caller, no initialisation needed, not shared by calls that
+ * may overlap.  Device-side errors (never a fault): n_b < 0, n_b >
  * max_query_len or rows outside [0, num_tokens) set bit 32 and that sequence
  * is skipped (rows past max_query_len are zeroed when they are in range);
  * n_b > context_lens[b] or a context outside [0, max_blocks_per_seq *
@@ -218,8 +221,29 @@ photon_status_t photon_paged_multi_query(const void* q, const void* k_cache, con
                                          const int32_t* context_lens,
                                          const int32_t* query_start, int32_t num_tokens,
                                          int32_t max_query_len, float scale, void* out,
+                                         void* workspace, size_t workspace_bytes,
                                          const photon_paged_shape_t* shape,
                                          photon_stream_t stream);
+
+/* Bytes of device workspace photon_paged_multi_query needs (0: none).  When
+ * the query tiles alone (num_seqs x num_kv_heads x ceil(max_query_len * G /
+ * 64)) give fewer than 1216 CTAs, each tile's keys are split into partitions
+ * of shape->partition_size keys rounded up to a multiple of 64 (512 when 0)
+ * that run in parallel and are merged by their log-sum-exp weights; a nonzero
+ * partition_size forces the split.  The workspace then holds the partials
+ * (m, l, o) of num_tokens x num_q_heads rows x ceil(max_blocks_per_seq *
+ * block_size / partition) partitions.  0 for an invalid shape, f32,
+ * num_tokens <= 0 or max_query_len <= 0. */
+size_t photon_paged_multi_query_workspace_size(const photon_paged_shape_t* shape,
+                                               int32_t num_tokens, int32_t max_query_len);
+
+/* Test and tuning hook: which kernel photon_paged_multi_query runs.
+ * 0 (default) and 1 = the warp-level mma.sync kernel with the key split of
+ * the plan; 2 = the tcgen05/TMEM kernel (128-row tiles, no key split,
+ * workspace unused).  Results
+ * agree within the documented tolerance, not bit for bit.  Process-wide;
+ * PHOTON_ERR_INVALID_ARG for another value. */
+photon_status_t photon_debug_set_multi_query_kernel(int32_t which);
 
 /* photon_paged_decode without a caller-provided workspace.  The pages have no
  * counterpart of this call; it exists for callers that cannot allocate device

@@ -28,6 +28,7 @@ __all__ = [
     "photon_paged_decode_plan", "photon_debug_set_attention_events",
     "photon_paged_decode_noalloc", "photon_paged_decode_step",
     "photon_rope_cos_sin", "photon_paged_decode_step_rope", "photon_paged_multi_query",
+    "photon_paged_multi_query_workspace_size", "photon_debug_set_multi_query_kernel",
     "Scheduler",
     "F32", "F16", "BF16", "STATUS",
 ]
@@ -100,8 +101,12 @@ def _load() -> ctypes.CDLL:
     lib.photon_rope_cos_sin.argtypes = [ctypes.c_double, I32, I32, P, P]
     lib.photon_paged_decode_step_rope.argtypes = [P, P, P, P, P, P, P, P, P, I32,
                                                   ctypes.c_float, P, P, SZ, SP, P]
-    lib.photon_paged_multi_query.argtypes = [P, P, P, P, P, P, I32, I32, ctypes.c_float, P, SP,
-                                             P]
+    lib.photon_paged_multi_query.argtypes = [P, P, P, P, P, P, I32, I32, ctypes.c_float, P, P,
+                                             SZ, SP, P]
+    lib.photon_paged_multi_query_workspace_size.argtypes = [SP, I32, I32]
+    lib.photon_paged_multi_query_workspace_size.restype = SZ
+    lib.photon_debug_set_multi_query_kernel.argtypes = [I32]
+    lib.photon_debug_set_multi_query_kernel.restype = ctypes.c_int
     lib.photon_paged_multi_query.restype = ctypes.c_int
     # host scheduler (include/photon_scheduler.h)
     lib.photon_scheduler_create.argtypes = [P, ctypes.POINTER(P)]
@@ -225,14 +230,28 @@ def photon_paged_decode_step_rope(k_new, v_new, slot_mapping, q, k_cache, v_cach
         _stream(stream)), "photon_paged_decode_step_rope")
 
 
+def photon_paged_multi_query_workspace_size(shape: PagedShape, num_tokens: int,
+                                            max_query_len: int) -> int:
+    return int(_load().photon_paged_multi_query_workspace_size(
+        ctypes.byref(shape), int(num_tokens), int(max_query_len)))
+
+
 def photon_paged_multi_query(q, k_cache, v_cache, block_tables, context_lens, query_start,
                              num_tokens: int, max_query_len: int, scale: float, out,
-                             shape: PagedShape, stream=None) -> None:
+                             workspace, workspace_bytes: int, shape: PagedShape,
+                             stream=None) -> None:
     """Causal attention of the last n_b tokens of each sequence over its cache."""
     _check(_load().photon_paged_multi_query(
         _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), _ptr(context_lens),
         _ptr(query_start), int(num_tokens), int(max_query_len), float(scale), _ptr(out),
-        ctypes.byref(shape), _stream(stream)), "photon_paged_multi_query")
+        _ptr(workspace), int(workspace_bytes), ctypes.byref(shape), _stream(stream)),
+        "photon_paged_multi_query")
+
+
+def photon_debug_set_multi_query_kernel(which: int) -> None:
+    """0 = by the plan, 1 = warp-level mma.sync kernel, 2 = tcgen05 kernel."""
+    _check(_load().photon_debug_set_multi_query_kernel(int(which)),
+           "photon_debug_set_multi_query_kernel")
 
 
 def photon_paged_decode_noalloc(q, k_cache, v_cache, block_tables, context_lens, scale: float,

@@ -116,7 +116,8 @@ __global__ void __launch_bounds__(kMqThreads) paged_multi_query_kernel(const Mul
   const uint32_t sK = sQ + C::kQBytes;
   const uint32_t sV = sK + kMqStages * C::kTileBytes;
 
-  const int b = blockIdx.z, kvh = blockIdx.y, tile = blockIdx.x;
+  const int b = blockIdx.z, kvh = blockIdx.y;
+  const int tile = blockIdx.x / a.pmax, part_idx = blockIdx.x % a.pmax;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = a.Hq / a.Hkv;
   const int q0 = __ldg(a.query_start + b);
@@ -133,7 +134,8 @@ __global__ void __launch_bounds__(kMqThreads) paged_multi_query_kernel(const Mul
     return;
   }
   if (n > a.max_query_len || ctx < n || ctx > a.MBS * kBlockSize) {
-    // inconsistent lengths: flag once, zero the rows this CTA owns
+    // inconsistent lengths: flag once, zero the rows this tile owns
+    if (part_idx != 0) return;
     if (tile == 0 && kvh == 0 && tid == 0)
       raise_error(a.err, n > a.max_query_len ? kErrQuery : kErrContext);
     const int rows = min(kMqRows, max(0, min(n, a.max_query_len) * G - row0));
@@ -149,6 +151,11 @@ __global__ void __launch_bounds__(kMqThreads) paged_multi_query_kernel(const Mul
   const int first_pos = ctx - n;                        // position of query token 0
   const int tok_last = (row0 + rows_here - 1) / G;      // last token of this tile
   const int kend = first_pos + tok_last + 1;            // keys [0, kend) are needed
+  // this CTA's partition of them: [kb, ke), a multiple of 64 keys long
+  const int kb = part_idx * a.part;
+  if (kb >= kend) return;
+  const int ke = min(kb + a.part, kend);
+  const int nparts = (kend + a.part - 1) / a.part;       // partitions of this tile
 
   // ---- query tile into shared memory; rows past the tile are zero
   for (int p = tid; p < kMqRows * C::kChunks; p += kMqThreads) {
@@ -162,11 +169,11 @@ __global__ void __launch_bounds__(kMqThreads) paged_multi_query_kernel(const Mul
   const T* vg = static_cast<const T*>(a.v_cache);
   const int32_t* table = a.block_tables + (size_t)b * a.MBS;
   auto load_stage = [&](int c, int buf) {
-    const int key0 = c * kMqKeys;
+    const int key0 = kb + c * kMqKeys;
     for (int p = tid; p < kMqKeys * C::kChunks; p += kMqThreads) {
       const int r = p / C::kChunks, ch = p % C::kChunks;
       const int j = key0 + r;
-      bool valid = j < kend;
+      bool valid = j < ke;
       size_t off = 0;
       if (valid) {
         const int blk = __ldg(table + j / kBlockSize);
@@ -181,7 +188,7 @@ __global__ void __launch_bounds__(kMqThreads) paged_multi_query_kernel(const Mul
       cp_async16(sV + buf * C::kTileBytes + swz<D>(r, ch), vg + off, valid);
     }
   };
-  const int nchunks = (kend + kMqKeys - 1) / kMqKeys;
+  const int nchunks = (ke - kb + kMqKeys - 1) / kMqKeys;
   load_stage(0, 0);
   cp_async_commit();
 
@@ -212,8 +219,8 @@ __global__ void __launch_bounds__(kMqThreads) paged_multi_query_kernel(const Mul
           ldsm_x4(sQ + swz<D>(warp * 16 + (lane & 15), kk * 2 + (lane >> 4)), qa[kk][0],
                   qa[kk][1], qa[kk][2], qa[kk][3]);
       }
-      const uint32_t kb = sK + (c & 1) * C::kTileBytes;
-      const uint32_t vb = sV + (c & 1) * C::kTileBytes;
+      const uint32_t kbuf = sK + (c & 1) * C::kTileBytes;
+      const uint32_t vbuf = sV + (c & 1) * C::kTileBytes;
       // S = Q K^T for 16 rows x 64 keys
       float s[8][4];
 #pragma unroll
@@ -223,7 +230,7 @@ __global__ void __launch_bounds__(kMqThreads) paged_multi_query_kernel(const Mul
 #pragma unroll
         for (int np = 0; np < 4; ++np) {
           uint32_t b0, b1, b2, b3;
-          ldsm_x4(kb + swz<D>(np * 16 + ((lane >> 4) << 3) + (lane & 7),
+          ldsm_x4(kbuf + swz<D>(np * 16 + ((lane >> 4) << 3) + (lane & 7),
                               kk * 2 + ((lane >> 3) & 1)),
                   b0, b1, b2, b3);
           Mma<T>::run(s[2 * np], qa[kk], b0, b1);
@@ -231,7 +238,9 @@ __global__ void __launch_bounds__(kMqThreads) paged_multi_query_kernel(const Mul
         }
       }
       // scale into the log2 domain; mask keys after each row's position
-      const int key0 = c * kMqKeys;
+      // keys past ke only occur when ke == kend, and those lie past every
+      // row's position: the causal mask covers them
+      const int key0 = kb + c * kMqKeys;
       const bool mask = key0 + kMqKeys - 1 > pos_min;
 #pragma unroll
       for (int i = 0; i < 8; ++i)
@@ -250,13 +259,16 @@ __global__ void __launch_bounds__(kMqThreads) paged_multi_query_kernel(const Mul
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
         const float m_new = fmaxf(m_r[h], mx);
-        const float corr = softmax_exp2(m_r[h] - m_new);
+        // a row with every key so far masked (possible in a later partition)
+        // keeps m = -inf: exponents then use 0, giving weights 0, not NaN
+        const float m_use = m_new == -INFINITY ? 0.f : m_new;
+        const float corr = softmax_exp2(m_r[h] - m_use);
         m_r[h] = m_new;
         float sum = 0.f;
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-          s[i][2 * h] = softmax_exp2(s[i][2 * h] - m_new);
-          s[i][2 * h + 1] = softmax_exp2(s[i][2 * h + 1] - m_new);
+          s[i][2 * h] = softmax_exp2(s[i][2 * h] - m_use);
+          s[i][2 * h + 1] = softmax_exp2(s[i][2 * h + 1] - m_use);
           sum += s[i][2 * h] + s[i][2 * h + 1];
         }
         l_r[h] = l_r[h] * corr + sum;
@@ -277,7 +289,7 @@ __global__ void __launch_bounds__(kMqThreads) paged_multi_query_kernel(const Mul
 #pragma unroll
         for (int dp = 0; dp < D / 16; ++dp) {
           uint32_t b0, b1, b2, b3;
-          ldsm_x4_trans(vb + swz<D>(ks * 16 + (((lane >> 3) & 1) << 3) + (lane & 7),
+          ldsm_x4_trans(vbuf + swz<D>(ks * 16 + (((lane >> 3) & 1) << 3) + (lane & 7),
                                     dp * 2 + (lane >> 4)),
                         b0, b1, b2, b3);
           Mma<T>::run(o[2 * dp], pa, b0, b1);
@@ -288,23 +300,83 @@ __global__ void __launch_bounds__(kMqThreads) paged_multi_query_kernel(const Mul
     __syncthreads();  // this stage's buffer is refilled two iterations on
   }
 
-  // ---- normalise and store the tile's valid rows
+  // ---- one partition: normalise and store the tile's valid rows; several:
+  // leave (m, l, unnormalised o) for the merge kernel
   if (!active) return;
 #pragma unroll
   for (int h = 0; h < 2; ++h) {
     float l = l_r[h];
     l += __shfl_xor_sync(0xffffffffu, l, 1);
     l += __shfl_xor_sync(0xffffffffu, l, 2);
-    const float inv = 1.f / l;
     const int r = warp * 16 + (lane >> 2) + 8 * h;
     if (r >= rows_here) continue;
     const int rr = row0 + r;
+    if (nparts > 1) {
+      const size_t prow = ((size_t)(q0 + rr / G) * a.Hq + kvh * G + rr % G) * a.pmax + part_idx;
+      if ((lane & 3) == 0) {
+        a.ws_m[prow] = m_r[h];
+        a.ws_l[prow] = l;
+      }
+      float* po = a.ws_o + prow * D + 2 * (lane & 3);
+#pragma unroll
+      for (int i = 0; i < D / 8; ++i)
+        *reinterpret_cast<float2*>(po + i * 8) = make_float2(o[i][2 * h], o[i][2 * h + 1]);
+      continue;
+    }
+    const float inv = 1.f / l;
     T* dst = outg + ((size_t)(q0 + rr / G) * a.Hq + kvh * G + rr % G) * D + 2 * (lane & 3);
 #pragma unroll
     for (int i = 0; i < D / 8; ++i)
       *reinterpret_cast<uint32_t*>(dst + i * 8) = Mma<T>::pack(o[i][2 * h] * inv,
                                                                 o[i][2 * h + 1] * inv);
   }
+}
+
+// Combines the partitions of the rows whose tile was split: one warp per
+// (query token, q head) row of sequence blockIdx.y.  Partition p of a row at
+// position pos holds keys [p*part, (p+1)*part) up to pos; the ones past pos
+// were fully masked and are skipped.
+template <typename T, int D>
+__global__ void __launch_bounds__(128) multi_query_merge_kernel(const MultiQueryArgs a) {
+  const int b = blockIdx.y;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int q0 = __ldg(a.query_start + b);
+  const int n = __ldg(a.query_start + b + 1) - q0;
+  const int ctx = __ldg(a.context_lens + b);
+  if (n <= 0 || q0 < 0 || q0 + n > a.num_tokens || n > a.max_query_len || ctx < n ||
+      ctx > a.MBS * kBlockSize)
+    return;  // flagged (and zeroed where possible) by the attention kernel
+  const int row = blockIdx.x * 4 + warp;  // (token i, head h) of this sequence
+  if (row >= n * a.Hq) return;
+  const int i = row / a.Hq, h = row % a.Hq;
+  const int G = a.Hq / a.Hkv;
+  const int r = i * G + h % G;            // row inside its KV head's tiles
+  const int tile = r / kMqRows;
+  const int rows_here = min(kMqRows, n * G - tile * kMqRows);
+  const int tok_last = (tile * kMqRows + rows_here - 1) / G;
+  const int kend = ctx - n + tok_last + 1;
+  if (kend <= a.part) return;             // single partition: written directly
+  const int pos = ctx - n + i;
+  const int np = pos / a.part + 1;        // partitions that hold keys <= pos
+  const size_t base = ((size_t)(q0 + i) * a.Hq + h) * a.pmax;
+  float mx = -INFINITY;
+  for (int p = 0; p < np; ++p) mx = fmaxf(mx, a.ws_m[base + p]);
+  float den = 0.f;
+  constexpr int kPer = D / 32;
+  float acc[kPer];
+#pragma unroll
+  for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
+  for (int p = 0; p < np; ++p) {
+    const float w = softmax_exp2(a.ws_m[base + p] - mx);
+    den += w * a.ws_l[base + p];
+    const float* po = a.ws_o + (base + p) * D + lane * kPer;
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) acc[e] += w * po[e];
+  }
+  const float inv = 1.f / den;
+  T* dst = static_cast<T*>(a.out) + ((size_t)(q0 + i) * a.Hq + h) * D + lane * kPer;
+#pragma unroll
+  for (int e = 0; e < kPer; ++e) dst[e] = Elem<T>::narrow(acc[e] * inv);
 }
 
 template <typename T, int D>
@@ -323,8 +395,12 @@ cudaError_t launch_mq(const MultiQueryArgs& a, cudaStream_t stream) {
   }
   const int G = a.Hq / a.Hkv;
   const int tiles = (a.max_query_len * G + kMqRows - 1) / kMqRows;
-  dim3 grid(tiles, a.Hkv, a.B);
+  dim3 grid(tiles * a.pmax, a.Hkv, a.B);
   kern<<<grid, kMqThreads, C::kSmem, stream>>>(a);
+  e = cudaGetLastError();
+  if (e != cudaSuccess || a.pmax == 1) return e;
+  dim3 mgrid((a.max_query_len * a.Hq + 3) / 4, a.B);
+  multi_query_merge_kernel<T, D><<<mgrid, 128, 0, stream>>>(a);
   return cudaGetLastError();
 }
 
@@ -332,8 +408,9 @@ cudaError_t launch_mq(const MultiQueryArgs& a, cudaStream_t stream) {
 
 cudaError_t launch_multi_query(const MultiQueryArgs& a, cudaStream_t stream) {
   if (!a.q || !a.k_cache || !a.v_cache || !a.block_tables || !a.context_lens || !a.query_start ||
-      !a.out || !a.err)
+      !a.out || !a.err || a.pmax < 1 || a.part < kMqKeys || a.part % kMqKeys != 0)
     return cudaErrorInvalidValue;
+  if (a.pmax > 1 && (!a.ws_m || !a.ws_l || !a.ws_o)) return cudaErrorInvalidValue;
   if (a.dtype == 1) {
     if (a.D == 64) return launch_mq<__half, 64>(a, stream);
     if (a.D == 128) return launch_mq<__half, 128>(a, stream);

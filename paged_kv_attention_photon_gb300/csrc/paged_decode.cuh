@@ -79,14 +79,16 @@ enum : int { kFirst = 1, kLast = 2, kDone = 4 };
 constexpr int kMaxRuns = 10;
 
 // Persistent-kernel geometry: NC consumer warps, 1 producer warp, S ring stages.
-template <typename T, int D, int G, int NC, int S>
+template <typename T, int D, int G, int NC, int S, bool R = false>
 struct PersistCfg {
   using C = DecodeCfg<T, D, G>;
   static constexpr int kThreads = (NC + 1) * 32;
   static constexpr int kBlockElems = kBlockSize * D;
   static constexpr int kBlockBytes = kBlockElems * (int)sizeof(T);
   static constexpr int kQBytes = G * D * (int)sizeof(T);
-  static constexpr int kQStride = (kQBytes + 127) / 128 * 128;
+  // with RoPE the item's (cos, sin) row, D/2 float pairs, follows its q rows
+  static constexpr int kCsBytes = R ? 4 * D : 0;
+  static constexpr int kQStride = (kQBytes + kCsBytes + 127) / 128 * 128;
   static constexpr int kStageBytes = 2 * NC * kBlockBytes;     // K blocks, then V blocks
   static constexpr int kOffFull = 0;
   static constexpr int kOffEmpty = kOffFull + 8 * S;
@@ -188,6 +190,9 @@ __device__ __forceinline__ void attend_block(const T* __restrict__ ks, const T* 
 // by the table's (cos, sin) for (pos, k).  Positions outside the table are
 // flagged and left unrotated.
 //
+// The item's (cos, sin) row for its position sits in shared memory next to
+// its q rows (the producer copies it with them).
+//
 // q rows, in the lane's registers: lane c of a row group holds chunks
 // c, c + 8, ... of each row; a pair's partner sits in the same lane when the
 // chunk distance D/2/kChunk is a multiple of 8, otherwise (16-bit D = 64) in
@@ -204,14 +209,14 @@ __device__ __forceinline__ void rope_q(float (&qf)[G][DecodeCfg<T, D, G>::kEPL],
     if (ctid == 0) raise_error(err, kErrPosition);
     return;
   }
-  const float2* row = cs + (size_t)pos * (D / 2);
+  const float2* row = cs;
   if constexpr (kInLane) {
     // slots of the lower half are the first kEPL/2; each one's partner is
     // kSlotShift further on in the same lane
 #pragma unroll
     for (int s = 0; s < C::kEPL / 2; ++s) {
       const int e = (c + 8 * (s / C::kChunk)) * C::kChunk + s % C::kChunk;
-      const float2 t = __ldg(row + e);
+      const float2 t = row[e];
 #pragma unroll
       for (int g = 0; g < G; ++g) {
         const float x0 = qf[g][s], x1 = qf[g][s + kSlotShift];
@@ -224,7 +229,7 @@ __device__ __forceinline__ void rope_q(float (&qf)[G][DecodeCfg<T, D, G>::kEPL],
 #pragma unroll
     for (int s = 0; s < C::kEPL; ++s) {
       const int e = (c + 8 * (s / C::kChunk)) * C::kChunk + s % C::kChunk;
-      const float2 t = __ldg(row + (lower ? e : e - D / 2));
+      const float2 t = row[lower ? e : e - D / 2];
 #pragma unroll
       for (int g = 0; g < G; ++g) {
         const float x = qf[g][s];
@@ -235,15 +240,24 @@ __device__ __forceinline__ void rope_q(float (&qf)[G][DecodeCfg<T, D, G>::kEPL],
   }
 }
 
+// Pairs k = lane, lane + 32, ... of the item's (cos, sin) row, kept in
+// registers for the new K row (the shared copy is recycled with its stage).
+template <int D>
+struct RopeLaneCs {
+  float2 w[(D / 2 + 31) / 32];
+};
+
 // One row of D elements in shared memory, rotated in place by a warp and
 // rounded back to the storage type.
 template <typename T, int D>
-__device__ __forceinline__ void rope_row(T* row, const float2* __restrict__ cs, int max_pos,
-                                         int pos, int lane) {
+__device__ __forceinline__ void rope_row(T* row, const RopeLaneCs<D>& cs, int max_pos, int pos,
+                                         int lane) {
   if (pos < 0 || pos >= max_pos) return;  // flagged by rope_q of the same item
-  const float2* t = cs + (size_t)pos * (D / 2);
-  for (int k = lane; k < D / 2; k += 32) {
-    const float2 w = __ldg(t + k);
+#pragma unroll
+  for (int i = 0; i < (D / 2 + 31) / 32; ++i) {
+    const int k = lane + 32 * i;
+    if (k >= D / 2) break;
+    const float2 w = cs.w[i];
     const float x0 = Elem<T>::to_f32(row[k]), x1 = Elem<T>::to_f32(row[k + D / 2]);
     row[k] = Elem<T>::narrow(x0 * w.x - x1 * w.y);
     row[k + D / 2] = Elem<T>::narrow(x1 * w.x + x0 * w.y);
@@ -279,7 +293,7 @@ static __device__ unsigned long long g_probe[kProbeCtas][kProbeSlots];
 template <typename T, int D, int G, int NC, int S, bool kRope>
 __global__ void __launch_bounds__((NC + 1) * 32, 1)
     paged_decode_attention_kernel(const DecodeArgs a) {
-  using PC = PersistCfg<T, D, G, NC, S>;
+  using PC = PersistCfg<T, D, G, NC, S, kRope>;
   using C = DecodeCfg<T, D, G>;
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + PC::kOffFull);
@@ -547,7 +561,9 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
           h.new_row = new_lane >= 0 ? new_rows - 1 : -1;
           h.pos = kRope ? it0.ctx - 1 : 0;
           hdr[slot] = h;
-          mbar_arrive_expect_tx(&full[slot], (uint32_t)(bytes + (first ? PC::kQBytes : 0)));
+          const bool cs_copy = kRope && first && h.pos >= 0 && h.pos < a.rope_max_pos;
+          mbar_arrive_expect_tx(&full[slot], (uint32_t)(bytes + (first ? PC::kQBytes : 0) +
+                                                        (cs_copy ? PC::kCsBytes : 0)));
         }
         __syncwarp();
         unsigned char* stage = smem + PC::kOffKV + slot * PC::kStageBytes;
@@ -572,6 +588,14 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
           bulk_copy_g2s(smem + PC::kOffQ + slot * PC::kQStride,
                         qbase + ((size_t)it0.b * a.Hq + (size_t)kvh * G) * D, PC::kQBytes,
                         &full[slot]);
+        if constexpr (kRope) {
+          // the item's (cos, sin) row rides with its q rows
+          const int pos = it0.ctx - 1;
+          if (first && lane == 0 && pos >= 0 && pos < a.rope_max_pos)
+            bulk_copy_g2s(smem + PC::kOffQ + slot * PC::kQStride + PC::kQBytes,
+                          a.rope_cs + (size_t)pos * (D / 2), (uint32_t)PC::kCsBytes,
+                          &full[slot]);
+        }
         if (st == 0) PROBE_SET(1, global_timer_ns());
         if (first && lane == 0) PROBE_SET(8 + 2 * items_done, global_timer_ns());
         ++st;
@@ -619,6 +643,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
   // ================================================================== consumers
   float qf[G][C::kEPL];
   float m[G], l[G], o[G][C::kEPL];
+  RopeLaneCs<D> kcs;  // RoPE only: this lane's (cos, sin) pairs of the current item
   float* const pm_buf = reinterpret_cast<float*>(smem + PC::kOffPm);
   float* const pl_buf = reinterpret_cast<float*>(smem + PC::kOffPl);
   float* const po_buf = reinterpret_cast<float*>(smem + PC::kOffPo);
@@ -663,7 +688,13 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
       }
       if constexpr (kRope) {
         // turn the raw rows first, then scale them like the plain path
-        rope_q<T, D, G>(qf, a.rope_cs, a.rope_max_pos, h.pos, c, a.err, ctid);
+        const float2* cs_row = reinterpret_cast<const float2*>(qs + G * D);
+        rope_q<T, D, G>(qf, cs_row, a.rope_max_pos, h.pos, c, a.err, ctid);
+        if (h.pos >= 0 && h.pos < a.rope_max_pos) {
+#pragma unroll
+          for (int i = 0; i < (D / 2 + 31) / 32; ++i)
+            if (lane + 32 * i < D / 2) kcs.w[i] = cs_row[lane + 32 * i];
+        }
 #pragma unroll
         for (int g = 0; g < G; ++g)
 #pragma unroll
@@ -676,7 +707,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
       if (kRope && warp == h.new_warp) {
         // fused step with RoPE: turn the new K row by its position, in place,
         // before it is attended and stored
-        rope_row<T, D>(const_cast<T*>(stage) + warp * PC::kBlockElems + h.new_row * D, a.rope_cs,
+        rope_row<T, D>(const_cast<T*>(stage) + warp * PC::kBlockElems + h.new_row * D, kcs,
                        a.rope_max_pos, h.pos, lane);
         __syncwarp();
       }
@@ -884,7 +915,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) paged_decode_merge_kernel(co
 // device, after raising its dynamic shared-memory limit).
 template <typename T, int D, int G, int NC, int S, bool kRope>
 int attention_ctas_per_sm() {
-  using PC = PersistCfg<T, D, G, NC, S>;
+  using PC = PersistCfg<T, D, G, NC, S, kRope>;
   constexpr int kMaxDev = 64;
   static int cache[kMaxDev];  // 0 = not yet queried
   int dev = 0;
@@ -936,9 +967,10 @@ cudaError_t launch_decode_impl(const DecodeArgs& a0, cudaStream_t stream) {
   const int grid = per_sm * a.num_sms;
 
   if (a.ev_start) cudaEventRecord(a.ev_start, stream);
+  using PCR = PersistCfg<T, D, G, NC, S, true>;
   cudaError_t err =
       rope ? launch_pdl(paged_decode_attention_kernel<T, D, G, NC, S, true>, dim3(grid),
-                        dim3(PC::kThreads), PC::kSmemBytes, stream, a)
+                        dim3(PCR::kThreads), PCR::kSmemBytes, stream, a)
            : launch_pdl(paged_decode_attention_kernel<T, D, G, NC, S, false>, dim3(grid),
                         dim3(PC::kThreads), PC::kSmemBytes, stream, a);
   if (err != cudaSuccess) return err;

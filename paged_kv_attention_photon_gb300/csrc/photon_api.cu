@@ -23,6 +23,9 @@ constexpr int kMaxDevices = 64;
 std::atomic<uint32_t*> g_err_ptr[kMaxDevices];
 
 std::atomic<cudaEvent_t> g_ev_start{nullptr};
+// photon_paged_multi_query kernel choice: 0 = by the plan, 1 = warp-level
+// mma.sync kernel, 2 = tcgen05 kernel.
+std::atomic<int> g_mq_kernel{0};
 std::atomic<cudaEvent_t> g_ev_stop{nullptr};
 
 constexpr int kMaxPartition = 4096;
@@ -312,7 +315,7 @@ photon_status_t photon_rope_cos_sin(double base, int32_t max_positions, int32_t 
     return PHOTON_ERR_INVALID_ARG;
   if ((long long)max_positions * (head_dim / 2) > (1ll << 31)) return PHOTON_ERR_INVALID_ARG;
   if (!table) return PHOTON_ERR_INVALID_ARG;
-  if (reinterpret_cast<uintptr_t>(table) & 7u) return PHOTON_ERR_MISALIGNED;
+  if (!aligned16(table)) return PHOTON_ERR_MISALIGNED;
   return photon::launch_rope_table(base, max_positions, head_dim, static_cast<float2*>(table),
                                    reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? PHOTON_OK
@@ -330,11 +333,62 @@ photon_status_t photon_paged_decode_step_rope(
   if (!k_new || !v_new || !slot_mapping || !rope_cos_sin || max_positions <= 0)
     return PHOTON_ERR_INVALID_ARG;
   if (!aligned16(k_new) || !aligned16(v_new) || (reinterpret_cast<uintptr_t>(slot_mapping) & 7u) ||
-      (reinterpret_cast<uintptr_t>(rope_cos_sin) & 7u))
+      !aligned16(rope_cos_sin))
     return PHOTON_ERR_MISALIGNED;
   return decode_common(q, k_cache, v_cache, block_tables, context_lens, scale, out, workspace,
                        workspace_bytes, shape, stream, k_new, v_new, slot_mapping, rope_cos_sin,
                        max_positions);
+}
+
+}  // extern "C"
+
+namespace {
+
+// Split-KV plan of photon_paged_multi_query.  Without a split a launch has
+// num_seqs x Hkv x ceil(max_query_len * G / 64) CTAs; when that is below
+// about four waves of the device (2 CTAs per SM on 152 SMs) every tile's keys
+// are cut into partitions (shape->partition_size rounded up to 64 keys, or
+// 512 by default) so that short query batches over long contexts still fill
+// the SMs.  A fixed threshold keeps the plan, and so the workspace size, a
+// function of the arguments alone.
+struct MqPlan {
+  int part, pmax;
+  size_t off_l, off_o, total;
+};
+
+constexpr int kMqTileRows = 64;
+constexpr int kMqSplitBelow = 4 * 2 * 152;
+
+MqPlan mq_plan(const photon_paged_shape_t* s, int32_t num_tokens, int32_t max_query_len) {
+  MqPlan p{};
+  const int64_t G = s->num_q_heads / s->num_kv_heads;
+  const int64_t tiles = ((int64_t)max_query_len * G + kMqTileRows - 1) / kMqTileRows;
+  const int64_t ctas = (int64_t)s->num_seqs * s->num_kv_heads * tiles;
+  const int64_t span = (int64_t)s->max_blocks_per_seq * s->block_size;
+  int part = s->partition_size > 0 ? (s->partition_size + 63) / 64 * 64 : 512;
+  if (s->partition_size == 0 && ctas >= kMqSplitBelow) part = (int)((span + 63) / 64 * 64);
+  if (part < 64) part = 64;
+  p.part = part;
+  p.pmax = (int)((span + part - 1) / part);
+  if (p.pmax < 1) p.pmax = 1;
+  if (p.pmax == 1) return p;
+  const size_t rows = (size_t)num_tokens * s->num_q_heads * p.pmax;
+  p.off_l = round_up(rows * sizeof(float), 256);
+  p.off_o = p.off_l + round_up(rows * sizeof(float), 256);
+  p.total = p.off_o + round_up(rows * (size_t)s->head_dim * sizeof(float), 256);
+  return p;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t photon_paged_multi_query_workspace_size(const photon_paged_shape_t* shape,
+                                               int32_t num_tokens, int32_t max_query_len) {
+  if (check_shape(shape) != PHOTON_OK || shape->dtype == PHOTON_F32 || num_tokens <= 0 ||
+      max_query_len <= 0)
+    return 0;
+  return mq_plan(shape, num_tokens, max_query_len).total;
 }
 
 photon_status_t photon_paged_multi_query(const void* q, const void* k_cache, const void* v_cache,
@@ -342,6 +396,7 @@ photon_status_t photon_paged_multi_query(const void* q, const void* k_cache, con
                                          const int32_t* context_lens,
                                          const int32_t* query_start, int32_t num_tokens,
                                          int32_t max_query_len, float scale, void* out,
+                                         void* workspace, size_t workspace_bytes,
                                          const photon_paged_shape_t* shape,
                                          photon_stream_t stream) {
   photon_status_t st = check_shape(shape);
@@ -357,9 +412,28 @@ photon_status_t photon_paged_multi_query(const void* q, const void* k_cache, con
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(block_tables) ||
       !aligned16(context_lens) || !aligned16(query_start) || !aligned16(out))
     return PHOTON_ERR_MISALIGNED;
+  const MqPlan plan = mq_plan(shape, num_tokens, max_query_len);
+  {
+    const int64_t G = shape->num_q_heads / shape->num_kv_heads;
+    const int64_t tiles = ((int64_t)max_query_len * G + kMqTileRows - 1) / kMqTileRows;
+    if (tiles * plan.pmax > INT_MAX || ((int64_t)max_query_len * shape->num_q_heads + 3) / 4 > INT_MAX)
+      return PHOTON_ERR_UNSUPPORTED;
+  }
+  if (plan.total > 0) {
+    if (!workspace || workspace_bytes < plan.total) return PHOTON_ERR_WORKSPACE;
+    if (!aligned16(workspace)) return PHOTON_ERR_MISALIGNED;
+  }
   uint32_t* err = nullptr;
   if ((st = error_word(&err)) != PHOTON_OK) return st;
   photon::MultiQueryArgs a{};
+  a.part = plan.part;
+  a.pmax = plan.pmax;
+  if (plan.total > 0) {
+    char* ws = static_cast<char*>(workspace);
+    a.ws_m = reinterpret_cast<float*>(ws);
+    a.ws_l = reinterpret_cast<float*>(ws + plan.off_l);
+    a.ws_o = reinterpret_cast<float*>(ws + plan.off_o);
+  }
   a.q = q;
   a.k_cache = k_cache;
   a.v_cache = v_cache;
@@ -378,9 +452,19 @@ photon_status_t photon_paged_multi_query(const void* q, const void* k_cache, con
   a.max_query_len = max_query_len;
   a.num_tokens = num_tokens;
   a.dtype = shape->dtype;
-  return photon::launch_multi_query(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
-             ? PHOTON_OK
-             : PHOTON_ERR_CUDA;
+  // The warp-level kernel (with its key split) runs by default; the tcgen05
+  // kernel is selected through photon_debug_set_multi_query_kernel.
+  const int choice = g_mq_kernel.load(std::memory_order_relaxed);
+  const bool tc = choice == 2;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const cudaError_t e = tc ? photon::launch_multi_query_tc(a, s) : photon::launch_multi_query(a, s);
+  return e == cudaSuccess ? PHOTON_OK : PHOTON_ERR_CUDA;
+}
+
+photon_status_t photon_debug_set_multi_query_kernel(int32_t which) {
+  if (which < 0 || which > 2) return PHOTON_ERR_INVALID_ARG;
+  g_mq_kernel.store(which, std::memory_order_relaxed);
+  return PHOTON_OK;
 }
 
 photon_status_t photon_paged_gather(const void* k_cache, const void* v_cache,

@@ -180,8 +180,18 @@ struct MultiQueryArgs {
   int B, Hq, Hkv, D, NB, MBS, max_query_len;
   int num_tokens;     // rows of q and out
   int dtype;          // 1 = fp16, 2 = bf16
+  // split-KV: each tile's keys are cut into partitions of `part` keys (a
+  // multiple of 64); pmax partitions per row at most.  pmax == 1: no split,
+  // no workspace.  Otherwise partials [num_tokens][Hq][pmax] (m, l) and
+  // [...][D] (o), merged by a second kernel.
+  int part, pmax;
+  float* ws_m;
+  float* ws_l;
+  float* ws_o;
 };
 cudaError_t launch_multi_query(const MultiQueryArgs& a, cudaStream_t stream);
+// The same operation on tcgen05 / TMEM tiles of 128 rows (no key split).
+cudaError_t launch_multi_query_tc(const MultiQueryArgs& a, cudaStream_t stream);
 
 
 // Launch with programmatic stream serialization: the kernel may be scheduled

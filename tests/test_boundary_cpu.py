@@ -121,7 +121,8 @@ def test_rope_entry_points_validation(lib):
     assert f(1e4, 0, 128, FAKE, None) == 1
     assert f(1e4, 16, 127, FAKE, None) == 1              # odd head_dim
     assert f(1e4, 1 << 30, 128, FAKE, None) == 1         # table too large
-    assert f(1e4, 16, 128, FAKE + 4, None) == 3          # float2 alignment
+    assert f(1e4, 16, 128, FAKE + 4, None) == 3          # 16-byte alignment
+    assert f(1e4, 16, 128, FAKE + 8, None) == 3
     g = lib.photon_paged_decode_step_rope
     s = _shape()
     args = lambda **o: [o.get("kn", FAKE), o.get("vn", FAKE), o.get("sm", FAKE), FAKE, FAKE,
@@ -131,6 +132,7 @@ def test_rope_entry_points_validation(lib):
     assert g(*args(mp=0)) == 1
     assert g(*args(kn=None)) == 1
     assert g(*args(cs=FAKE + 4)) == 3
+    assert g(*args(cs=FAKE + 8)) == 3
     assert g(*args(sm=FAKE + 4)) == 3
     assert g(*args(shape=_shape(head_dim=96))) == 2
     assert g(*args(shape=_shape(num_seqs=0), cs=None)) == 0    # empty batch: no-op
@@ -141,6 +143,7 @@ def test_multi_query_validation(lib):
     s = _shape()
     args = lambda **o: [o.get("q", FAKE), FAKE, FAKE, FAKE, FAKE, o.get("qs", FAKE),
                         o.get("T", 64), o.get("maxq", 16), o.get("scale", 0.1), o.get("out", FAKE2),
+                        o.get("ws", FAKE2), o.get("wsb", 1 << 40),
                         ctypes.byref(o.get("shape", s)), None]
     assert f(*args(shape=_shape(dtype=P.F32))) == 2            # tensor-core path: 16-bit only
     assert f(*args(shape=_shape(head_dim=96))) == 2
@@ -154,3 +157,30 @@ def test_multi_query_validation(lib):
     assert f(*args(T=0, q=None, qs=None, out=None)) == 0        # no tokens: no-op
     assert f(*args(maxq=0, q=None)) == 0
     assert f(*args(shape=_shape(num_seqs=0), q=None)) == 0
+    # a small batch over long contexts splits its keys: it needs a workspace
+    long_ctx = _shape(max_blocks_per_seq=512)
+    need = P.photon_paged_multi_query_workspace_size(long_ctx, 64, 16)
+    assert need > 0 and need % 256 == 0
+    assert f(*args(ws=None, shape=long_ctx)) == 4
+    assert f(*args(wsb=need - 1, shape=long_ctx)) == 4
+    assert f(*args(ws=FAKE2 + 8, shape=long_ctx)) == 3
+    assert P.photon_paged_multi_query_workspace_size(_shape(dtype=P.F32), 64, 16) == 0
+    assert P.photon_paged_multi_query_workspace_size(s, 0, 16) == 0
+
+
+def test_multi_query_plan_splits_small_batches_only(lib):
+    s = _shape(num_seqs=64, max_blocks_per_seq=512)
+    # 64 sequences x 8 KV heads x 1 tile (4 tokens x group 2 rows): split
+    assert P.photon_paged_multi_query_workspace_size(s, 256, 4) > 0
+    # 1024 tokens each: 64 x 8 x 32 tiles fill the device without a split
+    assert P.photon_paged_multi_query_workspace_size(s, 64 * 1024, 1024) == 0
+    # a nonzero partition_size forces the split
+    s2 = _shape(num_seqs=64, max_blocks_per_seq=512, partition_size=1024)
+    assert P.photon_paged_multi_query_workspace_size(s2, 64 * 1024, 1024) > 0
+
+
+def test_multi_query_kernel_hook(lib):
+    assert lib.photon_debug_set_multi_query_kernel(3) == 1
+    assert lib.photon_debug_set_multi_query_kernel(-1) == 1
+    for k in (1, 2, 0):
+        assert lib.photon_debug_set_multi_query_kernel(k) == 0

@@ -13,7 +13,10 @@ oracle, through the C ABI.
   ones, 16q/8kv, d = 128) and a speculative-verify batch (64 sequences x 4
   draft tokens on the long-context batch-64 lengths), all rows;
 * one token per sequence agrees with photon_paged_decode;
-* inconsistent lengths are flagged (bits 4 / 32) and zero-filled, not faulted.
+* inconsistent lengths are flagged (bits 4 / 32) and zero-filled, not faulted;
+* every case runs on both kernels -- the warp-level mma.sync one (with and
+  without key splits) and the tcgen05/TMEM one -- chosen through
+  photon_debug_set_multi_query_kernel.
 """
 import os
 
@@ -38,16 +41,30 @@ def _lib():
     assert st == 0
 
 
-def _run(mq: W.MultiQueryWorkload, max_query_len=None, query_start=None):
+@pytest.fixture(params=[1, 2], ids=["mma_sync", "tcgen05"])
+def kernel(request):
+    P.photon_debug_set_multi_query_kernel(request.param)
+    yield request.param
+    P.photon_debug_set_multi_query_kernel(0)
+
+
+def _workspace(shape, num_tokens, max_query_len):
+    n = P.photon_paged_multi_query_workspace_size(shape, num_tokens, max_query_len)
+    # no initialisation is needed: start from NaN bytes
+    return torch.full((max(n, 16),), 0xFF, dtype=torch.uint8, device="cuda"), n
+
+
+def _run(mq: W.MultiQueryWorkload, max_query_len=None, partition=0, context_lens=None):
     p = mq.pool
-    shape = P.PagedShape.make(**p.shape_dict())
+    shape = P.PagedShape.make(partition_size=partition, **p.shape_dict())
+    mql = mq.max_query_len if max_query_len is None else max_query_len
+    ws, nws = _workspace(shape, mq.num_tokens, mql)
     qd = dev(mq.q)
     out = torch.full(qd.shape, -1, dtype=qd.dtype, device="cuda")
-    qs = mq.query_start if query_start is None else query_start
+    ctx = p.context_lens if context_lens is None else context_lens
     P.photon_paged_multi_query(qd, dev(p.k_cache), dev(p.v_cache), dev(p.block_tables),
-                               dev(p.context_lens), dev(qs), mq.num_tokens,
-                               mq.max_query_len if max_query_len is None else max_query_len,
-                               p.scale, out, shape)
+                               dev(ctx), dev(mq.query_start), mq.num_tokens, mql, p.scale, out,
+                               ws, nws, shape)
     torch.cuda.synchronize()
     return out
 
@@ -82,7 +99,7 @@ RAGGED_PREFIX = [0, 1, 15, 16, 100, 0, 511, 1000, 2000]
 @pytest.mark.parametrize("dtype", [W.DTYPE_F16, W.DTYPE_BF16])
 @pytest.mark.parametrize("Hq,Hkv,d", [(4, 4, 128), (16, 8, 128), (32, 8, 64), (16, 2, 64),
                                       (8, 2, 128), (8, 8, 64)])
-def test_ragged_matches_oracle(dtype, Hq, Hkv, d):
+def test_ragged_matches_oracle(dtype, Hq, Hkv, d, kernel):
     mq = W.multi_query(300 + Hq + d + dtype, query_lens=RAGGED_N, prefix_lens=RAGGED_PREFIX,
                        num_q_heads=Hq, num_kv_heads=Hkv, head_dim=d, dtype=dtype)
     out = _run(mq)
@@ -91,7 +108,7 @@ def test_ragged_matches_oracle(dtype, Hq, Hkv, d):
     _check(to_float64(out, dtype), mq, f"mq {Hq}/{Hkv}/{d}")
 
 
-def test_chunked_prefill_batch():
+def test_chunked_prefill_batch(kernel):
     mq = W.multi_query(310, query_lens=[512] * 4, prefix_lens=[0, 512, 2048, 3584],
                        num_q_heads=16, num_kv_heads=8, head_dim=128, dtype=W.DTYPE_F16)
     out = _run(mq)
@@ -100,7 +117,7 @@ def test_chunked_prefill_batch():
     assert_close(to_float64(out, W.DTYPE_F16), _want(mq), W.DTYPE_F16, "chunked prefill")
 
 
-def test_speculative_verify_batch():
+def test_speculative_verify_batch(kernel):
     rng = np.random.Generator(np.random.PCG64(2))
     ctx = W.qwen_context_lens(rng, 64)
     mq = W.multi_query(311, query_lens=[4] * 64, prefix_lens=(ctx - 4).tolist(),
@@ -111,7 +128,7 @@ def test_speculative_verify_batch():
     _check(to_float64(out, W.DTYPE_BF16), mq, "verify")
 
 
-def test_one_token_agrees_with_decode():
+def test_one_token_agrees_with_decode(kernel):
     mq = W.multi_query(312, query_lens=[1] * 9, prefix_lens=[0, 5, 15, 16, 63, 64, 200, 777, 0],
                        num_q_heads=16, num_kv_heads=8, head_dim=128, dtype=W.DTYPE_F16)
     got = to_float64(_run(mq), W.DTYPE_F16)
@@ -128,7 +145,7 @@ def test_one_token_agrees_with_decode():
     assert_close(got, _want(mq), W.DTYPE_F16)
 
 
-def test_inconsistent_lengths_are_flagged_and_zeroed():
+def test_inconsistent_lengths_are_flagged_and_zeroed(kernel):
     mq = W.multi_query(313, query_lens=[3, 40, 5], prefix_lens=[10, 10, 10], num_q_heads=8,
                        num_kv_heads=2, head_dim=64, dtype=W.DTYPE_F16)
     # max_query_len 8 < 40: sequence 1 is flagged (bit 32); its first 8 rows are zeroed
@@ -142,16 +159,51 @@ def test_inconsistent_lengths_are_flagged_and_zeroed():
     assert_close(got[qs[2]:qs[3]], want[qs[2]:qs[3]], W.DTYPE_F16)
     assert (got[qs[1]:qs[1] + 8] == 0).all()
     # a context shorter than the query count: bit 4, rows zeroed
-    p = mq.pool
-    bad_ctx = p.context_lens.copy()
+    bad_ctx = mq.pool.context_lens.copy()
     bad_ctx[0] = 2
-    shape = P.PagedShape.make(**p.shape_dict())
-    out = torch.full(mq.q.shape, -1, dtype=torch.float16, device="cuda")
-    P.photon_paged_multi_query(dev(mq.q), dev(p.k_cache), dev(p.v_cache), dev(p.block_tables),
-                               dev(bad_ctx), dev(qs), mq.num_tokens, mq.max_query_len, p.scale,
-                               out, shape)
+    out = _run(mq, context_lens=bad_ctx)
     st, bits = P.photon_get_last_device_error()
     assert st == 6 and bits == 4, bits
     got = to_float64(out, W.DTYPE_F16)
     assert (got[qs[0]:qs[1]] == 0).all()
     assert_close(got[qs[1]:], want[qs[1]:], W.DTYPE_F16)
+
+
+@pytest.mark.parametrize("partition", [64, 128, 512, 4096])
+def test_split_partitions_match_oracle(partition):
+    """Forced split-KV: every tile's keys in partitions of `partition` keys,
+    merged by the second kernel; rows whose position falls in an early
+    partition and fully masked partitions included."""
+    mq = W.multi_query(320 + partition, query_lens=[1, 4, 70, 3, 130, 9],
+                       prefix_lens=[0, 60, 200, 1500, 700, 4000], num_q_heads=16,
+                       num_kv_heads=4, head_dim=128, dtype=W.DTYPE_F16)
+    out = _run(mq, partition=partition)
+    st, bits = P.photon_get_last_device_error()
+    assert st == 0 and bits == 0, bits
+    assert_close(to_float64(out, W.DTYPE_F16), _want(mq), W.DTYPE_F16, f"part {partition}")
+
+
+
+
+@pytest.mark.parametrize("which", [0, 2], ids=["default", "tcgen05"])
+def test_prefill_without_split_matches(which):
+    """A prefill batch big enough to skip the key split (no workspace), on
+    the default and the tcgen05 kernel: every row of four sequences against
+    the oracle."""
+    P.photon_debug_set_multi_query_kernel(which)
+    mq = W.multi_query(330, query_lens=[1024] * 16, prefix_lens=[0] * 8 + [4096] * 8,
+                       num_q_heads=16, num_kv_heads=8, head_dim=128, dtype=W.DTYPE_F16)
+    p = mq.pool
+    shape = P.PagedShape.make(**p.shape_dict())
+    assert P.photon_paged_multi_query_workspace_size(shape, mq.num_tokens, mq.max_query_len) == 0
+    got = to_float64(_run(mq), W.DTYPE_F16)
+    st, bits = P.photon_get_last_device_error()
+    assert st == 0 and bits == 0, bits
+    qs = mq.query_start
+    for b in [0, 7, 8, 15]:
+        want = oracle.multi_query(mq.q[qs[b]:qs[b + 1]], p.k_cache, p.v_cache,
+                                  p.block_tables[b:b + 1], p.context_lens[b:b + 1],
+                                  np.array([0, qs[b + 1] - qs[b]], np.int32), p.scale,
+                                  dtype=p.dtype, num_threads=THREADS)
+        assert_close(got[qs[b]:qs[b + 1]], want, W.DTYPE_F16, f"prefill seq {b}")
+    P.photon_debug_set_multi_query_kernel(0)
