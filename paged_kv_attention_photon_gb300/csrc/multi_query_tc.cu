@@ -39,7 +39,7 @@ constexpr int kTcRows = 128;    // query rows per CTA = TMEM lanes
 constexpr int kTcThreads = 128;
 constexpr int kTcKeys = 64;     // keys per chunk
 constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kTmemS = 0;     // S: columns [0, 64)
+constexpr uint32_t kTmemS = 0;     // S: two buffers, columns [0, 64) and [64, 128)
 constexpr uint32_t kTmemO = 128;   // O: columns [128, 128 + D)
 constexpr float kRescaleLog2 = 8.f;
 
@@ -141,7 +141,7 @@ template <typename T, int D>
 struct TcCfg {
   static constexpr int kQBytes = kTcRows * D * 2;     // Q tile
   static constexpr int kKBytes = kTcKeys * D * 2;     // one K chunk
-  static constexpr int kVBytes = D * kTcKeys * 2;     // one transposed V chunk
+  static constexpr int kVBytes = kTcKeys * D * 2;     // one V chunk
   static constexpr int kPBytes = kTcRows * kTcKeys * 2;
   static constexpr int kOffQ = 0;
   static constexpr int kOffK = kOffQ + kQBytes;       // [2]
@@ -151,14 +151,28 @@ struct TcCfg {
   // at least ~100 KB so that no more than two CTAs (2 x 256 TMEM columns)
   // share an SM, plus 1 KB to align the base to a swizzle atom
   static constexpr int kSmem = (kUsed > 100 * 1024 ? kUsed : 100 * 1024) + 1024;
-  static constexpr int kVPieces = kTcKeys * D / 8 / kTcThreads;  // 16-byte V pieces per thread
 };
+
+// MN-major (V) operand: the same 128-byte-swizzled rows of 64 elements as the
+// K-major tiles, but the MMA walks N along a row: 64-element blocks of N are
+// 64 keys x 128 B = 8 KB apart (leading byte offset), groups of 8 keys 1 KB
+// apart (stride byte offset).
+__device__ __forceinline__ uint64_t sw128_mn_desc(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr >> 4) & 0x3FFF);
+  d |= (uint64_t)((kTcKeys * 128) >> 4) << 16;
+  d |= (uint64_t)(1024 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kTcThreads) paged_multi_query_tc_kernel(const MultiQueryArgs a) {
   using C = TcCfg<T, D>;
   extern __shared__ unsigned char tc_smem_raw[];
-  __shared__ __align__(8) uint64_t bar;
+  __shared__ __align__(8) uint64_t bar_s[2];   // S(c) completes on bar_s[c & 1]
+  __shared__ __align__(8) uint64_t bar_o;      // each P V product
   __shared__ uint32_t tmem_slot;
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -201,9 +215,11 @@ __global__ void __launch_bounds__(kTcThreads) paged_multi_query_tc_kernel(const 
   const int my_pos = first_pos + (row0 + my_row) / G;
   const int pos_min = first_pos + (row0 + min(warp * 32, rows_here - 1)) / G;
 
-  // ---- barrier, TMEM
+  // ---- barriers, TMEM
   if (tid == 0) {
-    mbar_init(&bar, 1);
+    mbar_init(&bar_s[0], 1);
+    mbar_init(&bar_s[1], 1);
+    mbar_init(&bar_o, 1);
     mbar_init_fence();
   }
   if (warp == 0) {
@@ -214,7 +230,8 @@ __global__ void __launch_bounds__(kTcThreads) paged_multi_query_tc_kernel(const 
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
 
-  // ---- Q tile (rows past the tile zero), chunk 0 of K and V
+  // ---- loads: Q tile (rows past the tile zero); K and V chunks keep their
+  // rows of 16-byte chunks, swizzled (K read K-major, V read MN-major)
   for (int p = tid; p < kTcRows * (D / 8); p += kTcThreads) {
     const int r = p / (D / 8), ch = p % (D / 8);
     const bool valid = r < rows_here;
@@ -225,55 +242,28 @@ __global__ void __launch_bounds__(kTcThreads) paged_multi_query_tc_kernel(const 
   const T* kg = static_cast<const T*>(a.k_cache);
   const T* vg = static_cast<const T*>(a.v_cache);
   const int32_t* table = a.block_tables + (size_t)b * a.MBS;
-  // global element offset of key j's row (KV head kvh), or -1 past kend / bad block
-  auto key_row = [&](int j) -> long long {
-    if (j >= kend) return -1;
-    const int blk = __ldg(table + j / kBlockSize);
-    if (blk < 0 || blk >= a.NB) {
-      raise_error(a.err, kErrBlock);
-      return -1;
-    }
-    return (((long long)blk * a.Hkv + kvh) * kBlockSize + j % kBlockSize) * D;
-  };
-  auto load_k = [&](int c, int buf) {
+  // 64 keys of chunk c (zero past kend or for a bad block) into a tile
+  auto load_chunk = [&](const T* pool, uint32_t dst, int c) {
     for (int p = tid; p < kTcKeys * (D / 8); p += kTcThreads) {
       const int r = p / (D / 8), ch = p % (D / 8);
-      const long long off = key_row(c * kTcKeys + r);
-      cp_async16_zfill(sK + buf * C::kKBytes + sw_chunk<kTcKeys>(r, ch),
-                       off >= 0 ? kg + off + ch * 8 : kg, off >= 0);
-    }
-  };
-  uint4 vpre[C::kVPieces];
-  // piece i of this thread: key = p % 64, 8 dims from 8 * (p / 64), p = tid + 128 i
-  auto fetch_v = [&](int c) {
-#pragma unroll
-    for (int i = 0; i < C::kVPieces; ++i) {
-      const int p = tid + kTcThreads * i;
-      const long long off = key_row(c * kTcKeys + (p % kTcKeys));
-      vpre[i] = off >= 0 ? *reinterpret_cast<const uint4*>(vg + off + (p / kTcKeys) * 8)
-                         : make_uint4(0, 0, 0, 0);
-    }
-  };
-  // transposed store: element (dim d, key k) of the V^T tile (D rows of 64 keys)
-  auto store_v = [&](int buf) {
-    unsigned char* base = smem + C::kOffV + buf * C::kVBytes;
-#pragma unroll
-    for (int i = 0; i < C::kVPieces; ++i) {
-      const int p = tid + kTcThreads * i;
-      const int k = p % kTcKeys, d0 = (p / kTcKeys) * 8;
-      const uint16_t* h = reinterpret_cast<const uint16_t*>(&vpre[i]);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const int d = d0 + e;
-        const uint32_t off = (uint32_t)((d >> 3) * 1024 + (d & 7) * 128 +
-                                        ((((k >> 3) ^ (d & 7))) << 4) + (k & 7) * 2);
-        *reinterpret_cast<uint16_t*>(base + off) = h[e];
+      const int j = c * kTcKeys + r;
+      long long off = -1;
+      if (j < kend) {
+        const int blk = __ldg(table + j / kBlockSize);
+        if (blk >= 0 && blk < a.NB)
+          off = (((long long)blk * a.Hkv + kvh) * kBlockSize + j % kBlockSize) * D + ch * 8;
+        else
+          raise_error(a.err, kErrBlock);
       }
+      cp_async16_zfill(dst + sw_chunk<kTcKeys>(r, ch), off >= 0 ? pool + off : pool, off >= 0);
     }
   };
-  load_k(0, 0);
-  fetch_v(0);
-  store_v(0);
+  auto commit_group = [] { asm volatile("cp.async.commit_group;" ::: "memory"); };
+  load_chunk(kg, sK, 0);
+  load_chunk(vg, sV, 0);
+  commit_group();
+  if (nchunks > 1) load_chunk(kg, sK + C::kKBytes, 1);
+  commit_group();
   cp_async_wait_all();
   fence_async_smem();
   tc_fence_before();
@@ -282,43 +272,37 @@ __global__ void __launch_bounds__(kTcThreads) paged_multi_query_tc_kernel(const 
   const uint32_t tmem = tmem_slot;
   const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
   const uint32_t id_s = f16_idesc<T>(kTcRows, kTcKeys);
-  const uint32_t id_o = f16_idesc<T>(kTcRows, D);
+  const uint32_t id_o = f16_idesc<T>(kTcRows, D) | (1u << 16);   // B (V) MN-major
 
+  auto issue_s = [&](int c) {   // S(c) = Q K(c)^T into S buffer c & 1
+    tc_fence_after();
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const uint32_t koff = (kk & 3) * 32;   // 16 elements inside a 64-element block
+      tc_mma(tmem + kTmemS + (c & 1) * kTcKeys,
+             sw128_desc(sQ + (kk >> 2) * (kTcRows * 128) + koff),
+             sw128_desc(sK + (c & 1) * C::kKBytes + (kk >> 2) * (kTcKeys * 128) + koff), id_s,
+             kk > 0);
+    }
+    tc_commit(&bar_s[c & 1]);
+  };
+  if (tid == 0) issue_s(0);
+
+  // Per chunk c:  wait S(c) | load K(c+2), issue S(c+1) | softmax(c) |
+  // wait PV(c-1), rescale O, load V(c+1) | P(c) to shared | sync | PV(c).
   float m_run = -INFINITY, l_run = 0.f;
   bool ok = true;
-  uint32_t phase = 0;
-  for (int c = 0; c < nchunks && ok; ++c) {
-    const int buf = c & 1;
-    if (tid == 0) {
-      tc_fence_after();
-#pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk) {
-        const uint32_t koff = (kk & 3) * 32;   // 16 elements inside a 64-element block
-        tc_mma(tmem + kTmemS,
-               sw128_desc(sQ + (kk >> 2) * (kTcRows * 128) + koff),
-               sw128_desc(sK + buf * C::kKBytes + (kk >> 2) * (kTcKeys * 128) + koff), id_s,
-               kk > 0);
-      }
-      tc_commit(&bar);
-    }
-    // next chunk's K and V travel while the scores are computed
-    if (c + 1 < nchunks) {
-      load_k(c + 1, buf ^ 1);
-      fetch_v(c + 1);
-    }
-    // every thread waits; the verdict is made uniform so that the warp-wide
-    // TMEM loads below run in all lanes or in none
-    ok = __syncthreads_and(mbar_wait_bounded(&bar, phase) ? 1 : 0) != 0;
-    phase ^= 1u;
-    if (!ok) {
-      if (tid == 0) raise_error(a.err, kErrTimeout);
-      break;
-    }
+  for (int c = 0; c < nchunks; ++c) {
+    ok = __syncthreads_and(mbar_wait_bounded(&bar_s[c & 1], (c >> 1) & 1) ? 1 : 0) != 0;
+    if (!ok) break;
     tc_fence_after();
-    // ---- softmax of this thread's row over the chunk's 64 keys
+    if (c + 2 < nchunks) load_chunk(kg, sK + (c & 1) * C::kKBytes, c + 2);
+    commit_group();
+    if (c + 1 < nchunks && tid == 0) issue_s(c + 1);
+
     float s[kTcKeys];
-    tmem_ld32(tmem + lane_base + kTmemS, s);
-    tmem_ld32(tmem + lane_base + kTmemS + 32, s + 32);
+    tmem_ld32(tmem + lane_base + kTmemS + (c & 1) * kTcKeys, s);
+    tmem_ld32(tmem + lane_base + kTmemS + (c & 1) * kTcKeys + 32, s + 32);
     const int key0 = c * kTcKeys;
     float mx = -INFINITY;
 #pragma unroll
@@ -330,21 +314,28 @@ __global__ void __launch_bounds__(kTcThreads) paged_multi_query_tc_kernel(const 
     }
     // the maximum moves only when a score passes it by more than 2^8; then
     // what is accumulated so far is rescaled (TMEM loads and stores are
-    // warp-wide: a warp rescales if any of its rows must, others by 1)
+    // warp-wide: a warp rescales if any of its rows must, the others by 1)
     const bool moved = mx > m_run + kRescaleLog2;
     const float corr = moved ? softmax_exp2(m_run - mx) : 1.f;   // 0 on the first chunk
     l_run *= corr;
     if (moved) m_run = mx;
-    if (c > 0 && __any_sync(0xffffffffu, moved)) {
+    if (c > 0) {
+      ok = __syncthreads_and(mbar_wait_bounded(&bar_o, (c - 1) & 1) ? 1 : 0) != 0;
+      if (!ok) break;
+      tc_fence_after();
+      if (__any_sync(0xffffffffu, moved)) {
 #pragma unroll 1
-      for (int col = 0; col < D; col += 32) {
-        float o[32];
-        tmem_ld32(tmem + lane_base + kTmemO + col, o);
+        for (int col = 0; col < D; col += 32) {
+          float o[32];
+          tmem_ld32(tmem + lane_base + kTmemO + col, o);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) o[i] *= corr;
-        tmem_st32(tmem + lane_base + kTmemO + col, o);
+          for (int i = 0; i < 32; ++i) o[i] *= corr;
+          tmem_st32(tmem + lane_base + kTmemO + col, o);
+        }
       }
     }
+    if (c + 1 < nchunks) load_chunk(vg, sV + ((c + 1) & 1) * C::kVBytes, c + 1);
+    commit_group();
     float sum = 0.f;
     unsigned char* prow = smem + C::kOffP;
 #pragma unroll
@@ -363,13 +354,12 @@ __global__ void __launch_bounds__(kTcThreads) paged_multi_query_tc_kernel(const 
           w[e] = *reinterpret_cast<uint32_t*>(&h);
         }
       }
-      *reinterpret_cast<uint4*>(prow + sw_chunk<kTcRows>(tid, ch)) = make_uint4(w[0], w[1], w[2], w[3]);
+      *reinterpret_cast<uint4*>(prow + sw_chunk<kTcRows>(tid, ch)) =
+          make_uint4(w[0], w[1], w[2], w[3]);
     }
     l_run += sum;
-    if (c + 1 < nchunks) {
-      store_v(buf ^ 1);
-      cp_async_wait_all();
-    }
+    // everything but V(c+1) has landed: K(c+2) for the next S, V(c) for this PV
+    asm volatile("cp.async.wait_group 1;" ::: "memory");
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
@@ -377,16 +367,15 @@ __global__ void __launch_bounds__(kTcThreads) paged_multi_query_tc_kernel(const 
       tc_fence_after();
 #pragma unroll
       for (int kk = 0; kk < kTcKeys / 16; ++kk)
-        tc_mma(tmem + kTmemO, sw128_desc(sP + kk * 32), sw128_desc(sV + buf * C::kVBytes + kk * 32),
-               id_o, (c > 0 || kk > 0) ? 1u : 0u);
+        tc_mma(tmem + kTmemO, sw128_desc(sP + kk * 32),
+               sw128_mn_desc(sV + (c & 1) * C::kVBytes + kk * 2048), id_o,
+               (c > 0 || kk > 0) ? 1u : 0u);
+      tc_commit(&bar_o);
     }
   }
-  // ---- wait for the last products, then O / l
-  if (ok) {
-    if (tid == 0) tc_commit(&bar);
-    ok = __syncthreads_and(mbar_wait_bounded(&bar, phase) ? 1 : 0) != 0;
-    if (!ok && tid == 0) raise_error(a.err, kErrTimeout);
-  }
+  // ---- the last product, then O / l
+  if (ok) ok = __syncthreads_and(mbar_wait_bounded(&bar_o, (nchunks - 1) & 1) ? 1 : 0) != 0;
+  if (!ok && tid == 0) raise_error(a.err, kErrTimeout);
   tc_fence_after();
   if (ok) {
     const bool store = tid < rows_here;
@@ -415,8 +404,13 @@ __global__ void __launch_bounds__(kTcThreads) paged_multi_query_tc_kernel(const 
         *reinterpret_cast<uint4*>(dst + col + ch * 8) = make_uint4(w[0], w[1], w[2], w[3]);
       }
     }
+  } else {
+    // a timed-out tile leaves its rows unwritten (the error word says so);
+    // let any product still in flight land before TMEM is released
+    if (tid == 0) raise_error(a.err, kErrTimeout);
+    mbar_wait_bounded(&bar_o, (nchunks - 1) & 1);
   }
-  // (a timed-out tile leaves its rows unwritten; the error word says so)
+  asm volatile("cp.async.wait_all;" ::: "memory");
   tc_fence_before();
   __syncthreads();
   if (warp == 0)
