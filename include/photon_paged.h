@@ -238,9 +238,11 @@ size_t photon_paged_multi_query_workspace_size(const photon_paged_shape_t* shape
                                                int32_t num_tokens, int32_t max_query_len);
 
 /* Test and tuning hook: which kernel photon_paged_multi_query runs.
- * 0 (default) and 1 = the warp-level mma.sync kernel with the key split of
- * the plan; 2 = the tcgen05/TMEM kernel (128-row tiles, no key split,
- * workspace unused).  Results
+ * 0 (default) = chosen by the plan: the tcgen05/TMEM kernel (256-row
+ * tiles, no key split) when the query tiles fill the device without a split,
+ * the warp-level mma.sync kernel with its key split otherwise; 1 = always the
+ * warp-level kernel (with the plan's split); 2 = always the tcgen05 kernel
+ * (no split, workspace unused).  Results
  * agree within the documented tolerance, not bit for bit.  Process-wide;
  * PHOTON_ERR_INVALID_ARG for another value. */
 photon_status_t photon_debug_set_multi_query_kernel(int32_t which);

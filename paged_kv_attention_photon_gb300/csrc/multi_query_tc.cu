@@ -28,6 +28,8 @@
 // next 64-element block of R x 128 bytes.  K rows arrive with cp.async; V is
 // needed transposed (d rows, key columns), so each thread loads 16-byte V
 // pieces into registers one chunk ahead and scatters them as 2-byte stores.
+#include <cuda.h>
+
 #include <type_traits>
 
 #include "photon_common.cuh"
@@ -83,22 +85,32 @@ __device__ __forceinline__ void tc_fence_after() {
 __device__ __forceinline__ void fence_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
-// 32 consecutive fp32 columns of this thread's TMEM lane.
+// 32 consecutive fp32 columns of this thread's TMEM lane.  The wait sits in
+// the same asm statement as the load, so no use of the registers can be
+// scheduled before the data has arrived.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
   uint32_t r[32];
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
-      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-        "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]),
-        "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
-        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]),
-        "=r"(r[31])
-      : "r"(taddr));
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+// 64 consecutive columns: two loads in flight, one wait.
+__device__ __forceinline__ void tmem_ld64(uint32_t taddr, float* v) {
+  uint32_t r[64];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%64];\n"
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%65];\n"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]), "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]), "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]), "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]), "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+      : "r"(taddr), "r"(taddr + 32)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
 }
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
   asm volatile(
@@ -137,20 +149,25 @@ __device__ __forceinline__ uint32_t sw_chunk(int r, int c) {
                     (((c & 7) ^ (r & 7)) << 4));
 }
 
+// Shared-memory plan of the warp-specialised kernel: two Q tiles of 128 rows,
+// a ring of kStages K/V chunks (filled by the tensor memory accelerator), one
+// P buffer per Q tile.
 template <typename T, int D>
 struct TcCfg {
-  static constexpr int kQBytes = kTcRows * D * 2;     // Q tile
+  static constexpr int kTiles = 2;
+  static constexpr int kStages = 4;
+  static constexpr int kQBytes = kTcRows * D * 2;     // one Q tile
   static constexpr int kKBytes = kTcKeys * D * 2;     // one K chunk
   static constexpr int kVBytes = kTcKeys * D * 2;     // one V chunk
   static constexpr int kPBytes = kTcRows * kTcKeys * 2;
-  static constexpr int kOffQ = 0;
-  static constexpr int kOffK = kOffQ + kQBytes;       // [2]
-  static constexpr int kOffV = kOffK + 2 * kKBytes;   // [2]
-  static constexpr int kOffP = kOffV + 2 * kVBytes;
-  static constexpr int kUsed = kOffP + kPBytes;
-  // at least ~100 KB so that no more than two CTAs (2 x 256 TMEM columns)
-  // share an SM, plus 1 KB to align the base to a swizzle atom
-  static constexpr int kSmem = (kUsed > 100 * 1024 ? kUsed : 100 * 1024) + 1024;
+  static constexpr int kOffQ = 0;                               // [kTiles]
+  static constexpr int kOffK = kOffQ + kTiles * kQBytes;        // [kStages]
+  static constexpr int kOffV = kOffK + kStages * kKBytes;       // [kStages]
+  static constexpr int kOffP = kOffV + kStages * kVBytes;       // [kTiles]
+  static constexpr int kUsed = kOffP + kTiles * kPBytes;
+  static constexpr int kSmem = kUsed + 1024;   // + alignment of the base to a swizzle atom
+  // softmax warps, then the copy warp and the MMA warp
+  static constexpr int kThreads = kTiles * kTcThreads + 64;
 };
 
 // MN-major (V) operand: the same 128-byte-swizzled rows of 64 elements as the
@@ -167,13 +184,47 @@ __device__ __forceinline__ uint64_t sw128_mn_desc(uint32_t saddr) {
   return d;
 }
 
+// 2-D tiled bulk tensor copy (box: 16 rows x 64 elements, 128-byte swizzle)
+// into this CTA's shared memory, completing on `bar`.
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+      "%3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_cnt(uint64_t* bar) { mbar_arrive(bar); }
+
+// Warp roles: a CTA owns 256 query rows of one (sequence, KV head) as two
+// tiles of 128.  Warps 0-3 own tile 0 and warps 4-7 tile 1 (thread r of a
+// tile: TMEM lane r of that tile's columns): softmax, O rescale, epilogue.
+// Warp 8 copies: its lane 0 issues the bulk tensor copies of each chunk as
+// soon as the ring stage is free.  Warp 9 computes: its lanes zero the V rows
+// that lie past the last key, its lane 0 issues every MMA.  Both tiles use
+// every K/V chunk, so each chunk is fetched once for 256 rows.  TMEM: tile t
+// owns columns [256 t, 256 t + 256): two S buffers of 64, then O.
+// Barriers (each completes once per use; a use's parity is its index & 1):
+//   kv_full[s]     K and V of a chunk landed in stage s (copy transaction bytes)
+//   kv_free[s]     the P V products reading stage s finished (MMA commit)
+//   s_full[t][b]   S of a chunk is in tile t's TMEM buffer b (MMA commit)
+//   s_free[t][b]   tile t's 4 softmax warps have read that buffer (4 arrivals)
+//   p_full[t]      tile t's P of a chunk is in its shared buffer (128 arrivals)
+//   p_done[t]      the P V product reading that buffer finished (MMA commit)
 template <typename T, int D>
-__global__ void __launch_bounds__(kTcThreads) paged_multi_query_tc_kernel(const MultiQueryArgs a) {
+__global__ void __launch_bounds__(TcCfg<T, D>::kThreads)
+    paged_multi_query_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
+                                const __grid_constant__ CUtensorMap tm_v, const MultiQueryArgs a) {
   using C = TcCfg<T, D>;
+  constexpr int S = C::kStages;
+  constexpr int NT = C::kTiles;
+  constexpr int kSuper = NT * kTcRows;
   extern __shared__ unsigned char tc_smem_raw[];
-  __shared__ __align__(8) uint64_t bar_s[2];   // S(c) completes on bar_s[c & 1]
-  __shared__ __align__(8) uint64_t bar_o;      // each P V product
+  __shared__ __align__(8) uint64_t kv_full[S], kv_free[S], s_full[NT][2], s_free[NT][2],
+      p_full[NT], p_done[NT];
   __shared__ uint32_t tmem_slot;
+  __shared__ int tail_rows[S];   // per stage: first V row to zero (64 = none)
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_addr(smem);
@@ -181,12 +232,12 @@ __global__ void __launch_bounds__(kTcThreads) paged_multi_query_tc_kernel(const 
                  sP = sbase + C::kOffP;
 
   const int b = blockIdx.z, kvh = blockIdx.y, tile = blockIdx.x;
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = a.Hq / a.Hkv;
   const int q0 = __ldg(a.query_start + b);
   const int n = __ldg(a.query_start + b + 1) - q0;
   const int ctx = __ldg(a.context_lens + b);
-  const int row0 = tile * kTcRows;
+  const int row0 = tile * kSuper;
   const T* qg = static_cast<const T*>(a.q);
   T* outg = static_cast<T*>(a.out);
 
@@ -198,225 +249,337 @@ __global__ void __launch_bounds__(kTcThreads) paged_multi_query_tc_kernel(const 
   if (n > a.max_query_len || ctx < n || ctx > a.MBS * kBlockSize) {
     if (tile == 0 && kvh == 0 && tid == 0)
       raise_error(a.err, n > a.max_query_len ? kErrQuery : kErrContext);
-    const int rows = min(kTcRows, max(0, min(n, a.max_query_len) * G - row0));
-    for (int p = tid; p < rows * (D / 8); p += kTcThreads) {
+    const int rows = min(kSuper, max(0, min(n, a.max_query_len) * G - row0));
+    for (int p = tid; p < rows * (D / 8); p += C::kThreads) {
       const int r = row0 + p / (D / 8), ch = p % (D / 8);
       T* dst = outg + ((size_t)(q0 + r / G) * a.Hq + kvh * G + r % G) * D + ch * 8;
       *reinterpret_cast<uint4*>(dst) = make_uint4(0, 0, 0, 0);
     }
     return;
   }
-  const int rows_here = min(kTcRows, n * G - row0);
+  const int rows_here = min(kSuper, n * G - row0);   // rows of the CTA, tile 0 first
   if (rows_here <= 0) return;
+  const int ntiles = (rows_here + kTcRows - 1) / kTcRows;   // tiles with rows: 1 or 2
   const int first_pos = ctx - n;
   const int kend = first_pos + (row0 + rows_here - 1) / G + 1;   // keys [0, kend)
   const int nchunks = (kend + kTcKeys - 1) / kTcKeys;
-  const int my_row = min(tid, rows_here - 1);
-  const int my_pos = first_pos + (row0 + my_row) / G;
-  const int pos_min = first_pos + (row0 + min(warp * 32, rows_here - 1)) / G;
 
-  // ---- barriers, TMEM
+  // ---- setup: barriers, TMEM, the Q tiles (rows past the CTA's rows zero)
   if (tid == 0) {
-    mbar_init(&bar_s[0], 1);
-    mbar_init(&bar_s[1], 1);
-    mbar_init(&bar_o, 1);
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&kv_full[i], 1);
+      mbar_init(&kv_free[i], 1);
+    }
+    for (int t = 0; t < NT; ++t) {
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(&s_full[t][i], 1);
+        mbar_init(&s_free[t][i], 4);
+      }
+      mbar_init(&p_full[t], kTcThreads);
+      mbar_init(&p_done[t], 1);
+    }
     mbar_init_fence();
   }
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      smem_addr(&tmem_slot)),
-                 "r"(kTmemCols)
+                 "r"(NT * kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-
-  // ---- loads: Q tile (rows past the tile zero); K and V chunks keep their
-  // rows of 16-byte chunks, swizzled (K read K-major, V read MN-major)
-  for (int p = tid; p < kTcRows * (D / 8); p += kTcThreads) {
+  for (int p = tid; p < kSuper * (D / 8); p += C::kThreads) {
     const int r = p / (D / 8), ch = p % (D / 8);
     const bool valid = r < rows_here;
     const int rr = row0 + r;
     const T* src = valid ? qg + ((size_t)(q0 + rr / G) * a.Hq + kvh * G + rr % G) * D + ch * 8 : qg;
-    cp_async16_zfill(sQ + sw_chunk<kTcRows>(r, ch), src, valid);
+    cp_async16_zfill(sQ + (r / kTcRows) * C::kQBytes + sw_chunk<kTcRows>(r % kTcRows, ch), src,
+                     valid);
   }
-  const T* kg = static_cast<const T*>(a.k_cache);
-  const T* vg = static_cast<const T*>(a.v_cache);
-  const int32_t* table = a.block_tables + (size_t)b * a.MBS;
-  // 64 keys of chunk c (zero past kend or for a bad block) into a tile
-  auto load_chunk = [&](const T* pool, uint32_t dst, int c) {
-    for (int p = tid; p < kTcKeys * (D / 8); p += kTcThreads) {
-      const int r = p / (D / 8), ch = p % (D / 8);
-      const int j = c * kTcKeys + r;
-      long long off = -1;
-      if (j < kend) {
-        const int blk = __ldg(table + j / kBlockSize);
-        if (blk >= 0 && blk < a.NB)
-          off = (((long long)blk * a.Hkv + kvh) * kBlockSize + j % kBlockSize) * D + ch * 8;
-        else
-          raise_error(a.err, kErrBlock);
-      }
-      cp_async16_zfill(dst + sw_chunk<kTcKeys>(r, ch), off >= 0 ? pool + off : pool, off >= 0);
-    }
-  };
-  auto commit_group = [] { asm volatile("cp.async.commit_group;" ::: "memory"); };
-  load_chunk(kg, sK, 0);
-  load_chunk(vg, sV, 0);
-  commit_group();
-  if (nchunks > 1) load_chunk(kg, sK + C::kKBytes, 1);
-  commit_group();
   cp_async_wait_all();
   fence_async_smem();
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
-  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-  const uint32_t id_s = f16_idesc<T>(kTcRows, kTcKeys);
-  const uint32_t id_o = f16_idesc<T>(kTcRows, D) | (1u << 16);   // B (V) MN-major
-
-  auto issue_s = [&](int c) {   // S(c) = Q K(c)^T into S buffer c & 1
-    tc_fence_after();
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-      const uint32_t koff = (kk & 3) * 32;   // 16 elements inside a 64-element block
-      tc_mma(tmem + kTmemS + (c & 1) * kTcKeys,
-             sw128_desc(sQ + (kk >> 2) * (kTcRows * 128) + koff),
-             sw128_desc(sK + (c & 1) * C::kKBytes + (kk >> 2) * (kTcKeys * 128) + koff), id_s,
-             kk > 0);
-    }
-    tc_commit(&bar_s[c & 1]);
-  };
-  if (tid == 0) issue_s(0);
-
-  // Per chunk c:  wait S(c) | load K(c+2), issue S(c+1) | softmax(c) |
-  // wait PV(c-1), rescale O, load V(c+1) | P(c) to shared | sync | PV(c).
-  float m_run = -INFINITY, l_run = 0.f;
   bool ok = true;
-  for (int c = 0; c < nchunks; ++c) {
-    ok = __syncthreads_and(mbar_wait_bounded(&bar_s[c & 1], (c >> 1) & 1) ? 1 : 0) != 0;
-    if (!ok) break;
-    tc_fence_after();
-    if (c + 2 < nchunks) load_chunk(kg, sK + (c & 1) * C::kKBytes, c + 2);
-    commit_group();
-    if (c + 1 < nchunks && tid == 0) issue_s(c + 1);
 
-    float s[kTcKeys];
-    tmem_ld32(tmem + lane_base + kTmemS + (c & 1) * kTcKeys, s);
-    tmem_ld32(tmem + lane_base + kTmemS + (c & 1) * kTcKeys + 32, s + 32);
-    const int key0 = c * kTcKeys;
-    float mx = -INFINITY;
+  auto lane0_ok = [&](bool v) { return __shfl_sync(0xffffffffu, v ? 1 : 0, 0) != 0; };
+  if (warp == NT * 4) {
+    // ================================================================ copies
+    const int32_t* table = a.block_tables + (size_t)b * a.MBS;
+    for (int c = 0; c < nchunks && ok; ++c) {
+      const int st = c % S;
+      if (c >= S) {   // the stage's previous chunk, c - S, has been consumed
+        ok = lane0_ok(mbar_wait_bounded(&kv_free[st], ((c / S) - 1) & 1));
+        if (!ok) break;
+      }
+      if (lane != 0) continue;
+      uint32_t bytes = 0;
+      int tail = kTcKeys;
+      int phys[4];
 #pragma unroll
-    for (int j = 0; j < kTcKeys; ++j) {
-      float v = s[j] * a.qscale;
-      if (key0 + kTcKeys - 1 > pos_min && key0 + j > my_pos) v = -INFINITY;
-      s[j] = v;
-      mx = fmaxf(mx, v);
+      for (int i = 0; i < 4; ++i) {
+        const int kb = c * 4 + i;   // 16-key block of the sequence
+        phys[i] = -1;
+        if (kb * kBlockSize < kend) {
+          const int p = __ldg(table + kb);
+          if (p >= 0 && p < a.NB) {
+            phys[i] = p;
+            bytes += 2u * kBlockSize * D * 2u;
+          } else {
+            raise_error(a.err, kErrBlock);
+          }
+        }
+        // rows to zero: past kend, or a whole skipped block
+        const int valid_rows = phys[i] < 0 ? 0 : min(kBlockSize, kend - kb * kBlockSize);
+        if (valid_rows < kBlockSize && tail == kTcKeys) tail = i * kBlockSize + valid_rows;
+      }
+      tail_rows[st] = tail;   // published by the barrier's arrive below
+      mbar_arrive_expect_tx(&kv_full[st], bytes);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        if (phys[i] < 0) continue;
+        const int y = (phys[i] * a.Hkv + kvh) * kBlockSize;
+#pragma unroll
+        for (int h = 0; h < D / 64; ++h) {
+          tma_load_2d(sK + st * C::kKBytes + h * (kTcKeys * 128) + i * 2048, &tm_k, h * 64, y,
+                      &kv_full[st]);
+          tma_load_2d(sV + st * C::kVBytes + h * (kTcKeys * 128) + i * 2048, &tm_v, h * 64, y,
+                      &kv_full[st]);
+        }
+      }
     }
-    // the maximum moves only when a score passes it by more than 2^8; then
-    // what is accumulated so far is rescaled (TMEM loads and stores are
-    // warp-wide: a warp rescales if any of its rows must, the others by 1)
-    const bool moved = mx > m_run + kRescaleLog2;
-    const float corr = moved ? softmax_exp2(m_run - mx) : 1.f;   // 0 on the first chunk
-    l_run *= corr;
-    if (moved) m_run = mx;
-    if (c > 0) {
-      ok = __syncthreads_and(mbar_wait_bounded(&bar_o, (c - 1) & 1) ? 1 : 0) != 0;
-      if (!ok) break;
+    if (!ok && lane == 0) raise_error(a.err, kErrTimeout);
+  } else if (warp == NT * 4 + 1) {
+    // ================================================================ MMAs
+    const uint32_t id_s = f16_idesc<T>(kTcRows, kTcKeys);
+    const uint32_t id_o = f16_idesc<T>(kTcRows, D) | (1u << 16);   // B (V) MN-major
+    for (int c = 0; c <= nchunks && ok; ++c) {
+      if (c < nchunks) {
+        const int st = c % S;
+        ok = lane0_ok(mbar_wait_bounded(&kv_full[st], (c / S) & 1));
+        if (!ok) break;
+        // zero the V rows past the last key (a partial or missing block):
+        // they are multiplied by zero weights, and 0 x NaN would not vanish
+        const int tail = tail_rows[st];
+        if (tail < kTcKeys) {
+          unsigned char* vt = smem + C::kOffV + st * C::kVBytes;
+          for (int p = lane; p < (kTcKeys - tail) * (D / 8); p += 32) {
+            const int r = tail + p / (D / 8), ch = p % (D / 8);
+            *reinterpret_cast<uint4*>(vt + sw_chunk<kTcKeys>(r, ch)) = make_uint4(0, 0, 0, 0);
+          }
+          fence_async_smem();
+        }
+        __syncwarp();
+        for (int t = 0; t < ntiles && ok; ++t) {
+          if (c >= 2) {
+            ok = lane0_ok(mbar_wait_bounded(&s_free[t][c & 1], ((c - 2) >> 1) & 1));
+            if (!ok) break;
+          }
+          if (lane == 0) {
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t koff = (kk & 3) * 32;
+              tc_mma(tmem + t * kTmemCols + kTmemS + (c & 1) * kTcKeys,
+                     sw128_desc(sQ + t * C::kQBytes + (kk >> 2) * (kTcRows * 128) + koff),
+                     sw128_desc(sK + st * C::kKBytes + (kk >> 2) * (kTcKeys * 128) + koff), id_s,
+                     kk > 0);
+            }
+            tc_commit(&s_full[t][c & 1]);
+          }
+        }
+        if (!ok) break;
+      }
+      if (c >= 1) {
+        // P V of the previous chunk, tile by tile, once its weights are written
+        const int pc = c - 1, pst = pc % S;
+        for (int t = 0; t < ntiles && ok; ++t) {
+          ok = lane0_ok(mbar_wait_bounded(&p_full[t], pc & 1));
+          if (!ok) break;
+          if (lane == 0) {
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < kTcKeys / 16; ++kk)
+              tc_mma(tmem + t * kTmemCols + kTmemO, sw128_desc(sP + t * C::kPBytes + kk * 32),
+                     sw128_mn_desc(sV + pst * C::kVBytes + kk * 2048), id_o,
+                     (pc > 0 || kk > 0) ? 1u : 0u);
+            tc_commit(&p_done[t]);
+          }
+        }
+        if (!ok) break;
+        if (lane == 0) tc_commit(&kv_free[pst]);
+      }
+    }
+    if (!ok && lane == 0) raise_error(a.err, kErrTimeout);
+  } else {
+    // ================================================================ softmax rows
+    const int t = warp >> 2;                    // tile of this warp
+    const int trow = (warp & 3) * 32 + lane;    // row inside the tile = TMEM lane
+    const int crow = t * kTcRows + trow;        // row inside the CTA
+    const bool tile_used = t < ntiles;
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t tbase = tmem + t * kTmemCols;
+    const int my_row = min(crow, rows_here - 1);
+    const int my_pos = first_pos + (row0 + my_row) / G;
+    const int pos_min = first_pos + (row0 + min(t * kTcRows + (warp & 3) * 32, rows_here - 1)) / G;
+    float m_run = -INFINITY, l_run = 0.f;
+    const float qscale = a.qscale;
+    const float qmul = qscale > 0.f ? qscale : 1.f;   // multiplier left for the exponent
+    for (int c = 0; c < nchunks && tile_used; ++c) {
+      ok = mbar_wait_bounded(&s_full[t][c & 1], (c >> 1) & 1);
+      if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       tc_fence_after();
-      if (__any_sync(0xffffffffu, moved)) {
+      float s[kTcKeys];
+      tmem_ld64(tbase + lane_base + kTmemS + (c & 1) * kTcKeys, s);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cnt(&s_free[t][c & 1]);
+      const int key0 = c * kTcKeys;
+      // mask (only the chunks that reach past a row's position), then the row
+      // maximum as a tree of 8 independent chains.  With a positive scale the
+      // maximum is taken on the raw scores and the scale is folded into the
+      // exponent's fused multiply-add below; otherwise the scores are scaled
+      // first and the multiplier becomes 1.
+      if (key0 + kTcKeys - 1 > pos_min) {
+#pragma unroll
+        for (int j = 0; j < kTcKeys; ++j)
+          if (key0 + j > my_pos) s[j] = -INFINITY;
+      }
+      if (!(qscale > 0.f)) {
+#pragma unroll
+        for (int j = 0; j < kTcKeys; ++j) s[j] *= qscale;
+      }
+      float m8[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) m8[k] = s[k];
+#pragma unroll
+      for (int j = 8; j < kTcKeys; ++j) m8[j & 7] = fmaxf(m8[j & 7], s[j]);
+      const float mx = qmul * fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
+                                    fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
+      // the maximum moves only when a score passes it by more than 2^8; then
+      // what is accumulated so far is rescaled (warp-wide TMEM access: a warp
+      // rescales if any of its rows must, the others by 1)
+      const bool moved = mx > m_run + kRescaleLog2;
+      const float corr = moved ? softmax_exp2(m_run - mx) : 1.f;   // 0 on the first chunk
+      l_run *= corr;
+      if (moved) m_run = mx;
+      // the product of chunk c - 1 reads this tile's P buffer and updates O:
+      // it must be done before O is rescaled or P overwritten
+      if (c > 0) {
+        ok = mbar_wait_bounded(&p_done[t], (c - 1) & 1);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        tc_fence_after();
+      }
+      if (c > 0 && __any_sync(0xffffffffu, moved)) {
 #pragma unroll 1
         for (int col = 0; col < D; col += 32) {
           float o[32];
-          tmem_ld32(tmem + lane_base + kTmemO + col, o);
+          tmem_ld32(tbase + lane_base + kTmemO + col, o);
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] *= corr;
-          tmem_st32(tmem + lane_base + kTmemO + col, o);
+          tmem_st32(tbase + lane_base + kTmemO + col, o);
         }
+        tc_fence_before();
       }
-    }
-    if (c + 1 < nchunks) load_chunk(vg, sV + ((c + 1) & 1) * C::kVBytes, c + 1);
-    commit_group();
-    float sum = 0.f;
-    unsigned char* prow = smem + C::kOffP;
+      float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+      unsigned char* prow = smem + C::kOffP + t * C::kPBytes;
 #pragma unroll
-    for (int ch = 0; ch < kTcKeys / 8; ++ch) {
-      uint32_t w[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float p0 = softmax_exp2(s[ch * 8 + 2 * e] - m_run);
-        const float p1 = softmax_exp2(s[ch * 8 + 2 * e + 1] - m_run);
-        sum += p0 + p1;
-        if constexpr (std::is_same<T, __nv_bfloat16>::value) {
-          __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
-          w[e] = *reinterpret_cast<uint32_t*>(&h);
-        } else {
-          __half2 h = __floats2half2_rn(p0, p1);
-          w[e] = *reinterpret_cast<uint32_t*>(&h);
-        }
-      }
-      *reinterpret_cast<uint4*>(prow + sw_chunk<kTcRows>(tid, ch)) =
-          make_uint4(w[0], w[1], w[2], w[3]);
-    }
-    l_run += sum;
-    // everything but V(c+1) has landed: K(c+2) for the next S, V(c) for this PV
-    asm volatile("cp.async.wait_group 1;" ::: "memory");
-    fence_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    if (tid == 0) {
-      tc_fence_after();
-#pragma unroll
-      for (int kk = 0; kk < kTcKeys / 16; ++kk)
-        tc_mma(tmem + kTmemO, sw128_desc(sP + kk * 32),
-               sw128_mn_desc(sV + (c & 1) * C::kVBytes + kk * 2048), id_o,
-               (c > 0 || kk > 0) ? 1u : 0u);
-      tc_commit(&bar_o);
-    }
-  }
-  // ---- the last product, then O / l
-  if (ok) ok = __syncthreads_and(mbar_wait_bounded(&bar_o, (nchunks - 1) & 1) ? 1 : 0) != 0;
-  if (!ok && tid == 0) raise_error(a.err, kErrTimeout);
-  tc_fence_after();
-  if (ok) {
-    const bool store = tid < rows_here;
-    const int rr = row0 + my_row;
-    T* dst = outg + ((size_t)(q0 + rr / G) * a.Hq + kvh * G + rr % G) * D;
-    const float inv = 1.f / l_run;
-#pragma unroll 1
-    for (int col = 0; col < D; col += 32) {
-      float o[32];
-      tmem_ld32(tmem + lane_base + kTmemO + col, o);   // warp-wide: every lane
-      if (!store) continue;
-#pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
+      for (int ch = 0; ch < kTcKeys / 8; ++ch) {
         uint32_t w[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const float x0 = o[ch * 8 + 2 * e] * inv, x1 = o[ch * 8 + 2 * e + 1] * inv;
+          const float p0 = softmax_exp2(fmaf(s[ch * 8 + 2 * e], qmul, -m_run));
+          const float p1 = softmax_exp2(fmaf(s[ch * 8 + 2 * e + 1], qmul, -m_run));
+          sum4[e] += p0 + p1;
           if constexpr (std::is_same<T, __nv_bfloat16>::value) {
-            __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+            __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
             w[e] = *reinterpret_cast<uint32_t*>(&h);
           } else {
-            __half2 h = __floats2half2_rn(x0, x1);
+            __half2 h = __floats2half2_rn(p0, p1);
             w[e] = *reinterpret_cast<uint32_t*>(&h);
           }
         }
-        *reinterpret_cast<uint4*>(dst + col + ch * 8) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(prow + sw_chunk<kTcRows>(trow, ch)) =
+            make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      l_run += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
+      fence_async_smem();
+      mbar_arrive_cnt(&p_full[t]);
+    }
+    // ---- the last product, then O / l
+    if (tile_used) {
+      if (ok) {
+        ok = mbar_wait_bounded(&p_done[t], (nchunks - 1) & 1);
+        ok = __all_sync(0xffffffffu, ok);
+      }
+      if (!ok) {
+        if (lane == 0) raise_error(a.err, kErrTimeout);
+      } else {
+        tc_fence_after();
+        const bool store = crow < rows_here;
+        const int rr = row0 + my_row;
+        T* dst = outg + ((size_t)(q0 + rr / G) * a.Hq + kvh * G + rr % G) * D;
+        const float inv = 1.f / l_run;
+#pragma unroll 1
+        for (int col = 0; col < D; col += 32) {
+          float o[32];
+          tmem_ld32(tbase + lane_base + kTmemO + col, o);   // warp-wide: every lane
+          if (!store) continue;
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float x0 = o[ch * 8 + 2 * e] * inv, x1 = o[ch * 8 + 2 * e + 1] * inv;
+              if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+                __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+                w[e] = *reinterpret_cast<uint32_t*>(&h);
+              } else {
+                __half2 h = __floats2half2_rn(x0, x1);
+                w[e] = *reinterpret_cast<uint32_t*>(&h);
+              }
+            }
+            *reinterpret_cast<uint4*>(dst + col + ch * 8) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        }
       }
     }
-  } else {
-    // a timed-out tile leaves its rows unwritten (the error word says so);
-    // let any product still in flight land before TMEM is released
-    if (tid == 0) raise_error(a.err, kErrTimeout);
-    mbar_wait_bounded(&bar_o, (nchunks - 1) & 1);
   }
-  asm volatile("cp.async.wait_all;" ::: "memory");
   tc_fence_before();
   __syncthreads();
   if (warp == 0)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
-                 "r"(kTmemCols)
+                 "r"(NT * kTmemCols)
                  : "memory");
+}
+
+// Tensor map over a K or V pool seen as rows of head_dim elements:
+// (num_blocks x Hkv x 16) rows, box 16 rows x 64 elements, 128-byte swizzle.
+cudaError_t make_pool_map(CUtensorMap* map, const void* pool, int dtype, int NB, int Hkv, int D) {
+  using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+  static EncodeFn encode = nullptr;
+  if (!encode) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                     cudaEnableDefault, &q);
+    if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
+    encode = reinterpret_cast<EncodeFn>(fn);
+  }
+  const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)NB * Hkv * kBlockSize};
+  const cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+  const cuuint32_t box[2] = {64, (cuuint32_t)kBlockSize};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = encode(
+      map, dtype == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+      const_cast<void*>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 template <typename T, int D>
@@ -433,9 +596,13 @@ cudaError_t launch_tc(const MultiQueryArgs& a, cudaStream_t stream) {
     if (e != cudaSuccess) return e;
     configured[dev] = true;
   }
+  CUtensorMap tk, tv;
+  if ((e = make_pool_map(&tk, a.k_cache, a.dtype, a.NB, a.Hkv, a.D)) != cudaSuccess) return e;
+  if ((e = make_pool_map(&tv, a.v_cache, a.dtype, a.NB, a.Hkv, a.D)) != cudaSuccess) return e;
   const int G = a.Hq / a.Hkv;
-  const int tiles = (a.max_query_len * G + kTcRows - 1) / kTcRows;
-  kern<<<dim3(tiles, a.Hkv, a.B), kTcThreads, C::kSmem, stream>>>(a);
+  const int rows = C::kTiles * kTcRows;
+  const int tiles = (a.max_query_len * G + rows - 1) / rows;
+  kern<<<dim3(tiles, a.Hkv, a.B), C::kThreads, C::kSmem, stream>>>(tk, tv, a);
   return cudaGetLastError();
 }
 

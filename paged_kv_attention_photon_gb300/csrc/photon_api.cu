@@ -452,10 +452,11 @@ photon_status_t photon_paged_multi_query(const void* q, const void* k_cache, con
   a.max_query_len = max_query_len;
   a.num_tokens = num_tokens;
   a.dtype = shape->dtype;
-  // The warp-level kernel (with its key split) runs by default; the tcgen05
-  // kernel is selected through photon_debug_set_multi_query_kernel.
+  // Query batches that fill the device without a key split (chunked prefill)
+  // run on the tcgen05 kernel; split batches (a few tokens per sequence) on
+  // the warp-level kernel and its merge.
   const int choice = g_mq_kernel.load(std::memory_order_relaxed);
-  const bool tc = choice == 2;
+  const bool tc = choice == 2 || (choice == 0 && plan.pmax == 1);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const cudaError_t e = tc ? photon::launch_multi_query_tc(a, s) : photon::launch_multi_query(a, s);
   return e == cudaSuccess ? PHOTON_OK : PHOTON_ERR_CUDA;
