@@ -190,6 +190,32 @@ def multi_query_side(P, torch, stream, flush_l2, K, hbm_peak):
     return res
 
 
+def scheduler_side(P, steps: int = 200):
+    """Host cost of one continuous-batching step of the C++ scheduler (plan +
+    commit, through the ctypes binding) with 256 running requests in the
+    batch-256 serving mix, after a warm-up that fills the batch."""
+    mbs = 1024
+    sched = P.Scheduler(num_blocks=40000, block_size=16, max_blocks_per_seq=mbs, max_seqs=256,
+                        max_step_tokens=8192)
+    trace = W.request_trace(5, 2000, max_prompt=8192, max_new=2048, pool_tokens=40000 * 16,
+                            arrivals_per_step=64.0)
+    for _, rid, prompt, new in trace:
+        sched.add_request(rid, prompt, new)
+    for _ in range(100):              # fill the batch, get past the prompts
+        sched.schedule()
+        sched.update()
+    t0 = time.perf_counter()
+    rows = 0
+    for _ in range(steps):
+        r = sched.schedule()
+        rows += r["num_rows"]
+        sched.update()
+    dt = (time.perf_counter() - t0) / steps
+    sched.close()
+    return {"us_per_step": round(dt * 1e6, 1), "rows_per_step": round(rows / steps, 1),
+            "note": "schedule + update through the Python binding, host CPU"}
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -564,6 +590,7 @@ def run_ours(args):
     mq_side = None
     if not args.no_mq:
         mq_side = multi_query_side(P, torch, stream, flush_l2, K, peak)
+    host_sched = scheduler_side(P) if rank == 0 and not args.no_mq else None
     achieved = decode_bytes / (attn_mean_ms / 1e3) / 1e9
     roofline = {"bound": "hbm",
                 "kernel": "paged_decode_attention_kernel + paged_decode_merge_kernel",
@@ -599,6 +626,7 @@ def run_ours(args):
             "e2e": e2e,
             "rope_step": rope,
             "multi_query": mq_side,
+            "host_scheduler": host_sched,
             "gpu_launches": K * plan["kernels_per_call"],
             "clocks": clocks,
             "wall_ms_per_step_incl_flush": round(1e3 * t_wall / K, 4),

@@ -247,6 +247,14 @@ size_t photon_paged_multi_query_workspace_size(const photon_paged_shape_t* shape
  * PHOTON_ERR_INVALID_ARG for another value. */
 photon_status_t photon_debug_set_multi_query_kernel(int32_t which);
 
+/* Failure-detection self-test: launches one thread that waits on a barrier
+ * phase nothing completes, bounded by limit_ns (1 .. 10^9 ns), exactly as
+ * every wait inside this library's kernels is bounded.  The bound runs out,
+ * the kernel sets device error bit 8 and returns: no fault, no hang, the
+ * context stays usable.  Read the bit with photon_get_last_device_error.
+ * PHOTON_ERR_INVALID_ARG for a limit outside the range. */
+photon_status_t photon_debug_wait_probe(uint64_t limit_ns, photon_stream_t stream);
+
 /* photon_paged_decode without a caller-provided workspace.  The pages have no
  * counterpart of this call; it exists for callers that cannot allocate device
  * memory for the decode: an engine that reserved nearly all of HBM for its KV

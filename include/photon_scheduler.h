@@ -113,8 +113,11 @@ photon_status_t photon_scheduler_add_request(photon_scheduler_t* sched, int64_t 
  *   context_lens  int32 [max_seqs]                 cached tokens of row r after
  *                                                  this step's writes (counts
  *                                                  its new tokens)
- *   block_tables  int32 [max_seqs][max_blocks_per_seq]  row r's blocks, -1 past
- *                                                  ceil(context_lens[r] / block_size)
+ *   block_tables  int32 [max_seqs][max_blocks_per_seq]  row r's blocks: the
+ *                                                  first ceil(context_lens[r] /
+ *                                                  block_size) entries are written,
+ *                                                  the rest of the row is left as it
+ *                                                  was (no kernel reads past them)
  *   slot_mapping  int64 [max_step_tokens]          slot of each new token, rows
  *                                                  in order, positions ascending
  * Only the first num_rows rows / num_tokens slots are written.  A row with

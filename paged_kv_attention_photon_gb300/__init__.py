@@ -29,7 +29,7 @@ __all__ = [
     "photon_paged_decode_noalloc", "photon_paged_decode_step",
     "photon_rope_cos_sin", "photon_paged_decode_step_rope", "photon_paged_multi_query",
     "photon_paged_multi_query_workspace_size", "photon_debug_set_multi_query_kernel",
-    "Scheduler",
+    "photon_debug_wait_probe", "Scheduler",
     "F32", "F16", "BF16", "STATUS",
 ]
 
@@ -105,6 +105,8 @@ def _load() -> ctypes.CDLL:
                                              SZ, SP, P]
     lib.photon_paged_multi_query_workspace_size.argtypes = [SP, I32, I32]
     lib.photon_paged_multi_query_workspace_size.restype = SZ
+    lib.photon_debug_wait_probe.argtypes = [ctypes.c_uint64, P]
+    lib.photon_debug_wait_probe.restype = ctypes.c_int
     lib.photon_debug_set_multi_query_kernel.argtypes = [I32]
     lib.photon_debug_set_multi_query_kernel.restype = ctypes.c_int
     lib.photon_paged_multi_query.restype = ctypes.c_int
@@ -246,6 +248,12 @@ def photon_paged_multi_query(q, k_cache, v_cache, block_tables, context_lens, qu
         _ptr(query_start), int(num_tokens), int(max_query_len), float(scale), _ptr(out),
         _ptr(workspace), int(workspace_bytes), ctypes.byref(shape), _stream(stream)),
         "photon_paged_multi_query")
+
+
+def photon_debug_wait_probe(limit_ns: int, stream=None) -> None:
+    """Runs the bounded-wait self-test kernel (sets device error bit 8)."""
+    _check(_load().photon_debug_wait_probe(int(limit_ns), _stream(stream)),
+           "photon_debug_wait_probe")
 
 
 def photon_debug_set_multi_query_kernel(which: int) -> None:

@@ -14,6 +14,11 @@
 #include "../../include/photon_paged.h"
 #include "photon_common.cuh"
 
+namespace photon {
+// selftest.cu
+cudaError_t launch_wait_probe(unsigned long long limit_ns, uint32_t* err, cudaStream_t stream);
+}  // namespace photon
+
 namespace {
 
 // Sticky device error word, one per device that loads the library.
@@ -511,6 +516,17 @@ photon_status_t photon_get_last_device_error(photon_stream_t stream, uint32_t* b
     return PHOTON_ERR_CUDA;
   if (bits) *bits = word;
   return word ? PHOTON_ERR_DEVICE_BOUNDS : PHOTON_OK;
+}
+
+photon_status_t photon_debug_wait_probe(uint64_t limit_ns, photon_stream_t stream) {
+  if (limit_ns == 0 || limit_ns > 1000000000ull) return PHOTON_ERR_INVALID_ARG;
+  uint32_t* err = nullptr;
+  photon_status_t st = error_word(&err);
+  if (st != PHOTON_OK) return st;
+  return photon::launch_wait_probe(limit_ns, err, reinterpret_cast<cudaStream_t>(stream)) ==
+                 cudaSuccess
+             ? PHOTON_OK
+             : PHOTON_ERR_CUDA;
 }
 
 photon_status_t photon_debug_set_attention_events(void* start_event, void* stop_event) {

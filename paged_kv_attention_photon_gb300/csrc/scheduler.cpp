@@ -206,10 +206,9 @@ photon_status_t photon_scheduler_schedule(photon_scheduler_t* s, int64_t* reques
     if (query_lens) query_lens[i] = n;
     if (context_lens) context_lens[i] = ctx;
     if (block_tables) {
+      // only the blocks the row holds: entries past them are never read
       int32_t* row = block_tables + i * (size_t)mbs;
-      const int32_t nb = (int32_t)r->blocks.size();
-      std::memcpy(row, r->blocks.data(), sizeof(int32_t) * (size_t)nb);
-      std::fill(row + nb, row + mbs, -1);
+      std::memcpy(row, r->blocks.data(), sizeof(int32_t) * r->blocks.size());
     }
     if (slot_mapping) {
       for (int32_t p = r->computed; p < ctx; ++p)

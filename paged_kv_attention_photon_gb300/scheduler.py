@@ -34,8 +34,11 @@ def _p(a: np.ndarray) -> int:
 
 
 class Scheduler:
-    """One photon_scheduler_t.  schedule() returns a dict of numpy arrays
-    (copies of the first num_rows rows / num_tokens slots) plus the counts."""
+    """One photon_scheduler_t.  schedule() returns a dict of numpy views of the
+    first num_rows rows / num_tokens slots of this object's output buffers
+    (valid until the next schedule(); copy them to keep them) plus the counts.
+    Block-table rows hold the row's blocks first; entries past them are
+    stale (no kernel reads them)."""
 
     def __init__(self, *, num_blocks: int, block_size: int, max_blocks_per_seq: int,
                  max_seqs: int, max_step_tokens: int):
@@ -52,7 +55,7 @@ class Scheduler:
         self._ids = np.zeros(max_seqs, np.int64)
         self._qlen = np.zeros(max_seqs, np.int32)
         self._ctx = np.zeros(max_seqs, np.int32)
-        self._tables = np.zeros((max_seqs, max_blocks_per_seq), np.int32)
+        self._tables = np.full((max_seqs, max_blocks_per_seq), -1, np.int32)
         self._slots = np.zeros(max_step_tokens, np.int64)
         self._fin = np.zeros(max_seqs, np.int64)
 
@@ -83,9 +86,9 @@ class Scheduler:
             self._h, _p(self._ids), _p(self._qlen), _p(self._ctx), _p(self._tables),
             _p(self._slots), ctypes.byref(res)), "photon_scheduler_schedule")
         n, t = res.num_rows, res.num_tokens
-        return {"request_ids": self._ids[:n].copy(), "query_lens": self._qlen[:n].copy(),
-                "context_lens": self._ctx[:n].copy(), "block_tables": self._tables[:n].copy(),
-                "slot_mapping": self._slots[:t].copy(), "num_rows": n, "num_tokens": t,
+        return {"request_ids": self._ids[:n], "query_lens": self._qlen[:n],
+                "context_lens": self._ctx[:n], "block_tables": self._tables[:n],
+                "slot_mapping": self._slots[:t], "num_rows": n, "num_tokens": t,
                 "num_decode": res.num_decode, "num_admitted": res.num_admitted,
                 "num_preempted": res.num_preempted, "free_blocks": res.free_blocks}
 
