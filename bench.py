@@ -520,38 +520,87 @@ def run_ours(args):
         pg, ms, attn_mean_ms, step_bytes, wl.num_seqs, wl.tokens_attended())
     value = tot_bytes / (ms_max / 1e3) / 1e9
 
-    # ---- end to end through the public API, host buffers, copies inside the timing
+    # ---- end to end through the public API, host buffers, copies inside the timing.
+    # Every step copies its inputs (q, new K/V rows, slots, block tables,
+    # context lengths: one packed pinned buffer) host -> device and its output
+    # device -> host.  Pipelined as a serving loop would run it: two device
+    # input/output sets, the copies on their own streams, so step i+1's input
+    # copy and step i-1's output copy overlap step i's kernels.  The step's
+    # working set (478 MB) exceeds L2, so no flush is needed inside this loop.
     e2e = None
     if not args.no_e2e:
-        h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        h_out = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
         h2d = int(packed_host.numel())
-        d2h = h_out.numel() * h_out.element_size()
+        d2h = h_out[0].numel() * h_out[0].element_size()
+        pdev = [packed_dev, torch.empty_like(packed_dev)]
+        pviews = [views]
+        v2 = []
+        for a_, off in zip(host_arrays, offsets):
+            t_ = torch.from_numpy(a_)
+            v2.append(pdev[1][off:off + a_.nbytes].view(t_.dtype).view(t_.shape))
+        pviews.append(v2)
+        outs = [out, torch.empty_like(out)]
+        s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+        ev = lambda: torch.cuda.Event(enable_timing=False)
+
+        def run_pipelined(nsteps):
+            in_ready = [ev(), ev()]
+            done = [None, None]
+            out_done = [None, None]
+            t_start = torch.cuda.Event(enable_timing=True)
+            t_end = torch.cuda.Event(enable_timing=True)
+            t_start.record(s_in)
+            for i in range(nsteps):
+                j = i & 1
+                if done[j] is not None:
+                    s_in.wait_event(done[j])        # step i-2 has finished reading set j
+                with torch.cuda.stream(s_in):
+                    pdev[j].copy_(packed_host, non_blocking=True)
+                in_ready[j].record(s_in)
+                stream.wait_event(in_ready[j])
+                if out_done[j] is not None:
+                    stream.wait_event(out_done[j])  # step i-2's output has left set j
+                qj, knj, vnj, smj, btj, clj = pviews[j]
+                P.photon_paged_decode_step(knj, vnj, smj, qj, kc, vc, btj, clj, wl.scale,
+                                           outs[j], ws, ws_bytes, shape, stream)
+                done[j] = ev()
+                done[j].record(stream)
+                s_out.wait_event(done[j])
+                with torch.cuda.stream(s_out):
+                    h_out[j].copy_(outs[j], non_blocking=True)
+                out_done[j] = ev()
+                out_done[j].record(s_out)
+            s_in.wait_stream(s_out)
+            t_end.record(s_in)
+            torch.cuda.synchronize()
+            return t_start.elapsed_time(t_end)
+
+        run_pipelined(max(3, args.warmup))
+        e2e_ms = run_pipelined(K) / K
+        # the same steps one at a time (copy in, step, copy out, no overlap)
         ee = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
               for _ in range(K)]
-
-        def e2e_step(i):
+        for i in range(K):
             ee[i][0].record(stream)
             packed_dev.copy_(packed_host, non_blocking=True)
             step()
-            h_out.copy_(out, non_blocking=True)
+            h_out[0].copy_(out, non_blocking=True)
             ee[i][1].record(stream)
-
-        for i in range(min(3, K)):
-            flush_l2()
-            e2e_step(i)
         torch.cuda.synchronize()
-        for i in range(K):
-            flush_l2()
-            e2e_step(i)
-        torch.cuda.synchronize()
-        e2e_ms = sum(a.elapsed_time(b) for a, b in ee) / K
+        serial_ms = sum(a.elapsed_time(b) for a, b in ee) / K
         if pg:
-            t = torch.tensor([e2e_ms], dtype=torch.float64)
+            t = torch.tensor([e2e_ms, serial_ms], dtype=torch.float64)
             pg.all_reduce(t, op=pg.ReduceOp.MAX)
-            e2e_ms = float(t[0])
+            e2e_ms, serial_ms = float(t[0]), float(t[1])
         e2e = {"value": round(tot_bytes / (e2e_ms / 1e3) / 1e9, 2), "unit": "GB/s",
                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(h2d),
-               "d2h_bytes_per_step": int(d2h)}
+               "d2h_bytes_per_step": int(d2h),
+               "pipelining": "input copy of step i+1 and output copy of step i-1 overlap step i",
+               "serial_ms_per_step": round(serial_ms, 4),
+               "serial_value": round(tot_bytes / (serial_ms / 1e3) / 1e9, 2)}
+        st, bits = P.photon_get_last_device_error(stream)
+        if st != 0:
+            raise RuntimeError(f"device error word {bits} during the end-to-end steps")
 
     # ---- side measurement: the same step with the rotary embedding fused in
     rope = None
