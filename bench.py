@@ -64,6 +64,8 @@ def parse():
                     help="skip the side measurement of the step with RoPE fused in")
     ap.add_argument("--no-mq", action="store_true",
                     help="skip the side measurements of multi-query attention")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the side measurements of the other decode configurations")
     ap.add_argument("--json-out", default="")
     return ap.parse_args()
 
@@ -187,6 +189,62 @@ def multi_query_side(P, torch, stream, flush_l2, K, hbm_peak):
                                         "kv_GBps": round(mq.kv_bytes() / (ms_tc / 1e3) / 1e9,
                                                          1)}}
         del q, kc, vc, bt, cl, qs, out, ws
+    return res
+
+
+def configs_side(P, torch, stream, flush_l2, K, peak):
+    """The other decode configurations (Llama-3.2-1B-shaped batch 16, the
+    batch sweep 4/8/16/32, the batch-256 serving mix): fused step per call,
+    L2 flushed before each; for the mix also the cache write and the decode
+    timed as separate calls."""
+    def dev(a):
+        a = np.ascontiguousarray(a)
+        return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).cuda()
+
+    def timed(fn):
+        for _ in range(3):
+            flush_l2()
+            fn()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(K)]
+        for i in range(K):
+            flush_l2()
+            ev[i][0].record(stream)
+            fn()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in ev) / K
+
+    res = {}
+    for name in ("llama_b16", "sweep_b4", "sweep_b8", "sweep_b16", "sweep_b32", "mix_b256"):
+        wl = W.NAMED[name]()
+        shape = P.PagedShape.make(**wl.shape_dict())
+        q, kc, vc = dev(wl.q), dev(wl.k_cache), dev(wl.v_cache)
+        bt, cl = dev(wl.block_tables), dev(wl.context_lens)
+        kn, vn, sm = dev(wl.k_new), dev(wl.v_new), dev(wl.slot_mapping)
+        out = torch.empty_like(q)
+        nws = P.photon_paged_decode_workspace_size(shape)
+        ws = torch.empty(max(nws, 16), dtype=torch.uint8, device="cuda")
+        T = wl.slot_mapping.shape[0]
+        ms = timed(lambda: P.photon_paged_decode_step(kn, vn, sm, q, kc, vc, bt, cl, wl.scale,
+                                                      out, ws, nws, shape, stream))
+        nbytes = wl.decode_bytes() + wl.cache_write_bytes()
+        gbs = nbytes / (ms / 1e3) / 1e9
+        r = {"ms_per_step": round(ms, 5), "GBps": round(gbs, 1),
+             "hbm_fraction": round(gbs / peak, 4),
+             "tokens_attended_per_s": round(wl.tokens_attended() / (ms / 1e3), 1),
+             "decode_tokens_per_s_per_layer": round(wl.num_seqs / (ms / 1e3), 1),
+             "algorithmic_bytes": int(nbytes)}
+        if name == "mix_b256":
+            ms_w = timed(lambda: P.photon_cache_write(kn, vn, sm, T, kc, vc, shape, stream))
+            ms_d = timed(lambda: P.photon_paged_decode(q, kc, vc, bt, cl, wl.scale, out, ws, nws,
+                                                       shape, stream))
+            r["separate_calls_ms"] = {"cache_write": round(ms_w, 5), "decode": round(ms_d, 5)}
+        st, bits = P.photon_get_last_device_error(stream)
+        if st != 0:
+            raise RuntimeError(f"device error word {bits} in config {name}")
+        res[name] = r
+        del q, kc, vc, bt, cl, kn, vn, sm, out, ws
     return res
 
 
@@ -640,6 +698,9 @@ def run_ours(args):
     if not args.no_mq:
         mq_side = multi_query_side(P, torch, stream, flush_l2, K, peak)
     host_sched = scheduler_side(P) if rank == 0 and not args.no_mq else None
+    other_configs = None
+    if not args.no_configs:
+        other_configs = configs_side(P, torch, stream, flush_l2, K, peak)
     achieved = decode_bytes / (attn_mean_ms / 1e3) / 1e9
     roofline = {"bound": "hbm",
                 "kernel": "paged_decode_attention_kernel + paged_decode_merge_kernel",
@@ -676,6 +737,7 @@ def run_ours(args):
             "rope_step": rope,
             "multi_query": mq_side,
             "host_scheduler": host_sched,
+            "other_configs": other_configs,
             "gpu_launches": K * plan["kernels_per_call"],
             "clocks": clocks,
             "wall_ms_per_step_incl_flush": round(1e3 * t_wall / K, 4),

@@ -554,6 +554,8 @@ __global__ void __launch_bounds__(TcCfg<T, D>::kThreads)
                  : "memory");
 }
 
+}  // namespace
+
 // Tensor map over a K or V pool seen as rows of head_dim elements:
 // (num_blocks x Hkv x 16) rows, box 16 rows x 64 elements, 128-byte swizzle.
 cudaError_t make_pool_map(CUtensorMap* map, const void* pool, int dtype, int NB, int Hkv, int D) {
@@ -581,6 +583,8 @@ cudaError_t make_pool_map(CUtensorMap* map, const void* pool, int dtype, int NB,
       CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
+
+namespace {
 
 template <typename T, int D>
 cudaError_t launch_tc(const MultiQueryArgs& a, cudaStream_t stream) {

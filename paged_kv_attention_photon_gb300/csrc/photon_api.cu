@@ -72,6 +72,16 @@ int partition_of(const photon_paged_shape_t* s) {
   if (s->partition_size) return s->partition_size;
   const int per_token = 2 * s->head_dim * (int)elem_bytes(s->dtype);  // K + V bytes
   int part = kItemBytes / per_token / s->block_size * s->block_size;
+  // A small batch has too few such items to keep the grid busy, and one
+  // item's latency then sets the call's time: shrink the partition so that
+  // even the largest contexts the shape allows give about two items per
+  // resident CTA (2 per SM on 152 SMs), down to 64 tokens.
+  constexpr int64_t kTargetItems = 2 * 2 * 152;
+  const int64_t span_tokens = (int64_t)s->num_seqs * s->max_blocks_per_seq * s->block_size *
+                              s->num_kv_heads;
+  int64_t fit = span_tokens / kTargetItems / s->block_size * s->block_size;
+  if (fit < 64) fit = 64;
+  if (fit < part) part = (int)fit;
   if (part < s->block_size) part = s->block_size;
   if (part > kMaxPartition) part = kMaxPartition;
   return part;
