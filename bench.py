@@ -64,6 +64,9 @@ def parse():
                     help="skip the side measurement of the step with RoPE fused in")
     ap.add_argument("--no-mq", action="store_true",
                     help="skip the side measurements of multi-query attention")
+    ap.add_argument("--mq-case", default="", choices=["", "verify_b64x4", "prefill_b16x1024"],
+                    help="profiling aid: run only this multi-query case (default kernel "
+                         "choice, --steps calls) and print its timing")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the side measurements of the other decode configurations")
     ap.add_argument("--json-out", default="")
@@ -118,7 +121,8 @@ def measured_bf16_tflops():
     return FALLBACK_BF16_TFLOPS, "fallback"
 
 
-def multi_query_side(P, torch, stream, flush_l2, K, hbm_peak):
+def multi_query_side(P, torch, stream, flush_l2, K, hbm_peak, only: str = "",
+                     with_tc: bool = True):
     """Speculative-verify and chunked-prefill timings of photon_paged_multi_query."""
     rng = np.random.Generator(np.random.PCG64(2))
     ctx = W.qwen_context_lens(rng, 64)
@@ -139,6 +143,8 @@ def multi_query_side(P, torch, stream, flush_l2, K, hbm_peak):
         return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).cuda()
 
     for name, (mq, bound) in cases.items():
+        if only and name != only:
+            continue
         p = mq.pool
         shape = P.PagedShape.make(**p.shape_dict())
         q, kc, vc = dev(mq.q), dev(p.k_cache), dev(p.v_cache)
@@ -171,7 +177,7 @@ def multi_query_side(P, torch, stream, flush_l2, K, hbm_peak):
             return sum(a.elapsed_time(b) for a, b in ev) / K
 
         ms = timed(0)
-        ms_tc = timed(2)
+        ms_tc = timed(2) if with_tc else ms
         gbs = mq.kv_bytes() / (ms / 1e3) / 1e9
         tfs = mq.flops() / (ms / 1e3) / 1e12
         achieved, peak, unit = (gbs, hbm_peak, "GB/s") if bound == "hbm" else \
@@ -755,10 +761,30 @@ def run_ours(args):
     return 0
 
 
+def run_mq_case(args):
+    """Only one multi-query case (profiling aid)."""
+    import torch
+    import paged_kv_attention_photon_gb300 as P
+    torch.cuda.set_device(0)
+    P.build()
+    flush_w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+
+    def flush_l2():
+        flush_w.zero_()
+
+    peak, _ = measured_peaks()
+    res = multi_query_side(P, torch, torch.cuda.current_stream(), flush_l2, args.steps,
+                           peak or FALLBACK_HBM_GBS, only=args.mq_case, with_tc=False)
+    print(json.dumps(res), flush=True)
+    return 0
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
+    if args.mq_case:
+        return run_mq_case(args)
     return run_ours(args)
 
 

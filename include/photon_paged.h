@@ -228,7 +228,7 @@ photon_status_t photon_paged_multi_query(const void* q, const void* k_cache, con
 /* Bytes of device workspace photon_paged_multi_query needs (0: none).  When
  * the query tiles alone (num_seqs x num_kv_heads x ceil(max_query_len * G /
  * 64)) give fewer than 1216 CTAs, each tile's keys are split into partitions
- * of shape->partition_size keys rounded up to a multiple of 64 (512 when 0)
+ * of shape->partition_size keys rounded up to a multiple of 64 (1024 when 0)
  * that run in parallel and are merged by their log-sum-exp weights; a nonzero
  * partition_size forces the split.  The workspace then holds the partials
  * (m, l, o) of num_tokens x num_q_heads rows x ceil(max_blocks_per_seq *

@@ -118,8 +118,10 @@ struct MqCfg {
   static constexpr int kQBytes = kMqRows * kRowBytes;
   static constexpr int kKVBytes = kMqKeys * kRowBytes;     // one K or V chunk
   static constexpr int kOffQ = 0;
-  // the Q tile's space also holds the key-split combine: 64 rows x 64 fp32
-  static constexpr int kQSpace = kQBytes > 64 * 64 * 4 ? kQBytes : 64 * 64 * 4;
+  // the Q tile's space also holds the key-split combine: 64 rows of 64 fp32,
+  // padded to 72 so that neighbouring rows fall in other banks
+  static constexpr int kCombStride = 72;
+  static constexpr int kQSpace = kQBytes > 64 * kCombStride * 4 ? kQBytes : 64 * kCombStride * 4;
   static constexpr int kOffK = kQSpace;                    // [kStages]
   static constexpr int kOffV = kOffK + kStages * kKVBytes; // [kStages]
   static constexpr int kUsed = kOffV + kStages * kKVBytes;
@@ -559,10 +561,12 @@ __global__ void __launch_bounds__(MqCfg<T, D>::kThreads, 2)
           comb_l[ks * nrows + r] = l_r[h];
         }
       }
-      float* co = reinterpret_cast<float*>(smem + C::kOffQ);   // [KS][nrows][64]
+      constexpr int CS = C::kCombStride;
+      float* co = reinterpret_cast<float*>(smem + C::kOffQ);   // [KS][nrows][CS]
       const int tpr = kMqThreads / nrows;                      // threads per row: 8 or 4
       const int cols = 64 / tpr;
-      const int r = tid / tpr, cb = (tid % tpr) * cols;
+      // thread: row tid / tpr, columns k, k + tpr, k + 2 tpr, ... (k = tid % tpr)
+      const int r = tid / tpr, k0 = tid % tpr;
       for (int half = 0; half < D / 64; ++half) {
         mma_warps_sync();   // (the Q tile is no longer read; the previous half is done)
         if (active) {
@@ -571,7 +575,7 @@ __global__ void __launch_bounds__(MqCfg<T, D>::kThreads, 2)
             const int rr = rbase + (lane >> 2) + 8 * h;
 #pragma unroll
             for (int i = 0; i < 8; ++i)
-              *reinterpret_cast<float2*>(co + (ks * nrows + rr) * 64 + i * 8 + 2 * (lane & 3)) =
+              *reinterpret_cast<float2*>(co + (ks * nrows + rr) * CS + i * 8 + 2 * (lane & 3)) =
                   make_float2(o[half * 8 + i][2 * h], o[half * 8 + i][2 * h + 1]);
           }
         }
@@ -593,22 +597,21 @@ __global__ void __launch_bounds__(MqCfg<T, D>::kThreads, 2)
               a.ws_m[prow] = M;
               a.ws_l[prow] = L;
             }
-            float* po = a.ws_o + prow * D + half * 64 + cb;
+            float* po = a.ws_o + prow * D + half * 64;
             for (int e = 0; e < cols; ++e) {
+              const int col = k0 + e * tpr;
               float acc = 0.f;
-              for (int w = 0; w < KS; ++w) acc += wgt[w] * co[(w * nrows + r) * 64 + cb + e];
-              po[e] = acc;
+              for (int w = 0; w < KS; ++w) acc += wgt[w] * co[(w * nrows + r) * CS + col];
+              po[col] = acc;
             }
           } else {
             const float inv = 1.f / L;
-            T* dst = outg + orow * D + half * 64 + cb;
-            for (int e = 0; e < cols; e += 2) {
-              float acc0 = 0.f, acc1 = 0.f;
-              for (int w = 0; w < KS; ++w) {
-                acc0 += wgt[w] * co[(w * nrows + r) * 64 + cb + e];
-                acc1 += wgt[w] * co[(w * nrows + r) * 64 + cb + e + 1];
-              }
-              *reinterpret_cast<uint32_t*>(dst + e) = Mma<T>::pack(acc0 * inv, acc1 * inv);
+            T* dst = outg + orow * D + half * 64;
+            for (int e = 0; e < cols; ++e) {
+              const int col = k0 + e * tpr;
+              float acc = 0.f;
+              for (int w = 0; w < KS; ++w) acc += wgt[w] * co[(w * nrows + r) * CS + col];
+              dst[col] = Elem<T>::narrow(acc * inv);
             }
           }
         }

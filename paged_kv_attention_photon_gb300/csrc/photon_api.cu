@@ -363,7 +363,8 @@ namespace {
 // num_seqs x Hkv x ceil(max_query_len * G / 64) CTAs; when that is below
 // about four waves of the device (2 CTAs per SM on 152 SMs) every tile's keys
 // are cut into partitions (shape->partition_size rounded up to 64 keys, or
-// 512 by default) so that short query batches over long contexts still fill
+// 1024 by default, the best of 256..4096 measured on 64 x 4 draft tokens over
+// long contexts) so that short query batches over long contexts still fill
 // the SMs.  A fixed threshold keeps the plan, and so the workspace size, a
 // function of the arguments alone.
 struct MqPlan {
@@ -380,7 +381,7 @@ MqPlan mq_plan(const photon_paged_shape_t* s, int32_t num_tokens, int32_t max_qu
   const int64_t tiles = ((int64_t)max_query_len * G + kMqTileRows - 1) / kMqTileRows;
   const int64_t ctas = (int64_t)s->num_seqs * s->num_kv_heads * tiles;
   const int64_t span = (int64_t)s->max_blocks_per_seq * s->block_size;
-  int part = s->partition_size > 0 ? (s->partition_size + 63) / 64 * 64 : 512;
+  int part = s->partition_size > 0 ? (s->partition_size + 63) / 64 * 64 : 1024;
   if (s->partition_size == 0 && ctas >= kMqSplitBelow) part = (int)((span + 63) / 64 * 64);
   if (part < 64) part = 64;
   p.part = part;
