@@ -829,6 +829,23 @@ constexpr int kMergeRows = 32;
 template <typename T, int D>
 __global__ void __launch_bounds__(kMergeWarps * 32) paged_decode_merge_kernel(const DecodeArgs a) {
   constexpr int EPL = D / 32;
+  // This kernel runs only after the attention kernel has passed its own wait
+  // for the kernel before it, so the context lengths (which the attention
+  // kernel does not write) can be read before waiting for the attention grid:
+  // one round trip off the merge's critical path.  Rows of empty or rejected
+  // contexts are not touched by the attention kernel either.
+  const int item = blockIdx.x * kMergeWarps + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  const int b = item < a.B * a.Hq ? item / a.Hq : 0;
+  const int ctx = item < a.B * a.Hq ? __ldg(a.context_lens + b) : 0;
+  T* out = static_cast<T*>(a.out) + (size_t)item * D + lane * EPL;
+  const bool zero_row = item < a.B * a.Hq && (ctx <= 0 || ctx > a.MBS * kBlockSize);
+  if (zero_row) {
+    // empty or rejected context: a zero row
+    if (ctx != 0 && lane == 0 && item % a.Hq == 0) raise_error(a.err, kErrContext);
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) out[e] = Elem<T>::narrow(0.f);
+  }
   pdl_wait_primary();
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     // The attention grid is done handing out items: leave the queue clean for
@@ -836,19 +853,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) paged_decode_merge_kernel(co
     a.ws_ctrl[1] = 0ull;
     a.ws_ctrl[0] = kQueueReady;
   }
-  const int item = blockIdx.x * kMergeWarps + (threadIdx.x >> 5);
-  if (item >= a.B * a.Hq) return;
-  const int lane = threadIdx.x & 31;
-  const int b = item / a.Hq;
-  const int ctx = __ldg(a.context_lens + b);
-  T* out = static_cast<T*>(a.out) + (size_t)item * D + lane * EPL;
-  if (ctx <= 0 || ctx > a.MBS * kBlockSize) {
-    // empty or rejected context: a zero row
-    if (ctx != 0 && lane == 0 && item % a.Hq == 0) raise_error(a.err, kErrContext);
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) out[e] = Elem<T>::narrow(0.f);
-    return;
-  }
+  if (item >= a.B * a.Hq || zero_row) return;
   const int nparts = (ctx + a.part - 1) / a.part;
   if (nparts < 2) return;                             // the attention kernel wrote out
   const size_t row0 = (size_t)item * a.pmax;          // item = b * Hq + h
