@@ -12,8 +12,9 @@ preempted requests are handed out again while still holding their old rows,
 so a read past a context length would show.  At the end the device pool
 equals the host mirror byte for byte.
 
-(The prompt chunks' own attention is multi-query work that these kernels do
-not do; only their K/V rows are written here.)
+The second test runs each whole step -- prompt chunks and decode rows alike --
+as one cache write of every new row and one multi-query causal attention call
+over all scheduled rows, each step against the oracle's multi-query.
 """
 import numpy as np
 import pytest
@@ -127,4 +128,80 @@ def test_scheduler_drives_decode_steps(seed, num_blocks, max_seqs, budget, n_req
     assert kc.cpu().numpy().tobytes() == host_k.tobytes()
     assert vc.cpu().numpy().tobytes() == host_v.tobytes()
     if num_blocks < 1000:
+        assert preempted > 0
+
+
+@pytest.mark.parametrize("seed,num_blocks,max_seqs,budget,n_req", [
+    (7, 600, 16, 256, 24),      # roomy: prompts chunked across steps
+    (8, 60, 8, 128, 16),        # tight: preemption and recompute
+])
+def test_scheduler_drives_multi_query_steps(seed, num_blocks, max_seqs, budget, n_req):
+    """A whole serving step in one attention call: every scheduled row (prompt
+    chunks and decode rows alike) writes its new K/V rows with one
+    photon_cache_write and attends causally with one photon_paged_multi_query
+    (query_start = the rows' cumulative query lengths); each step's output
+    against the oracle's multi-query on the host mirror of the pool."""
+    max_prompt, max_new = 200, 24
+    mbs = (max_prompt + max_new + BS - 1) // BS
+    trace = W.request_trace(seed, n_req, max_prompt=max_prompt, max_new=max_new,
+                            pool_tokens=num_blocks * BS, arrivals_per_step=2.0)
+    rows = {rid: W.request_rows(seed, rid, prompt + new, HKV, D, DT)
+            for _, rid, prompt, new in trace}
+    sched = P.Scheduler(num_blocks=num_blocks, block_size=BS, max_blocks_per_seq=mbs,
+                        max_seqs=max_seqs, max_step_tokens=budget)
+    host_k = np.full((num_blocks, HKV, BS, D), np.nan, np.float16)
+    host_v = np.full((num_blocks, HKV, BS, D), np.nan, np.float16)
+    kc, vc = dev(host_k), dev(host_v)
+    nxt, steps, rows_done, preempted = 0, 0, 0, 0
+    while steps < 2000:
+        while nxt < len(trace) and trace[nxt][0] <= steps:
+            _, rid, prompt, new = trace[nxt]
+            sched.add_request(rid, prompt, new)
+            nxt += 1
+        st = sched.schedule()
+        preempted += st["num_preempted"]
+        B, T = st["num_rows"], st["num_tokens"]
+        if B:
+            q_lens = st["query_lens"].astype(np.int32)
+            ctx = st["context_lens"].astype(np.int32)
+            tabs = np.ascontiguousarray(st["block_tables"]).astype(np.int32)
+            slots = st["slot_mapping"].astype(np.int64).copy()
+            ids = st["request_ids"].copy()
+            kk, vv, qq = [], [], []
+            for r in range(B):
+                k_all, v_all = rows[int(ids[r])]
+                c, n = int(ctx[r]), int(q_lens[r])
+                kk.append(k_all[c - n:c])
+                vv.append(v_all[c - n:c])
+                qq.extend(W.request_queries(seed, int(ids[r]), pos, HQ, D, DT)
+                          for pos in range(c - n, c))
+            kk, vv, q = np.concatenate(kk), np.concatenate(vv), np.stack(qq)
+            qs = np.zeros(B + 1, np.int32)
+            qs[1:] = np.cumsum(q_lens)
+            shape = P.PagedShape.make(num_seqs=B, num_q_heads=HQ, num_kv_heads=HKV, head_dim=D,
+                                      num_blocks=num_blocks, max_blocks_per_seq=mbs, dtype=DT)
+            P.photon_cache_write(dev(kk), dev(vv), dev(slots), T, kc, vc, shape)
+            oracle.cache_write(kk, vv, slots, host_k, host_v, block_size=BS, dtype=DT)
+            maxq = int(q_lens.max())
+            nws = P.photon_paged_multi_query_workspace_size(shape, T, maxq)
+            ws = torch.empty(max(nws, 16), dtype=torch.uint8, device="cuda")
+            out = torch.empty((T, HQ, D), dtype=torch.float16, device="cuda")
+            P.photon_paged_multi_query(dev(q), kc, vc, dev(tabs), dev(ctx), dev(qs), T, maxq,
+                                       0.125, out, ws, nws, shape)
+            want = oracle.multi_query(q, host_k, host_v, tabs, ctx, qs, 0.125, dtype=DT,
+                                      num_threads=8)
+            torch.cuda.synchronize()
+            s_, bits = P.photon_get_last_device_error()
+            assert s_ == 0 and bits == 0, (steps, bits)
+            assert_close(to_float64(out, DT), want, DT, f"step {steps}")
+            rows_done += B
+        sched.update()
+        steps += 1
+        s = sched.stats()
+        if nxt == len(trace) and s["running"] == 0 and s["waiting"] == 0:
+            break
+    torch.cuda.synchronize()
+    assert sched.stats()["finished"] == n_req and rows_done > 0
+    assert kc.cpu().numpy().tobytes() == host_k.tobytes()
+    if num_blocks < 100:
         assert preempted > 0
