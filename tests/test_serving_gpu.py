@@ -131,17 +131,17 @@ def test_scheduler_drives_decode_steps(seed, num_blocks, max_seqs, budget, n_req
         assert preempted > 0
 
 
-@pytest.mark.parametrize("seed,num_blocks,max_seqs,budget,n_req", [
-    (7, 600, 16, 256, 24),      # roomy: prompts chunked across steps
-    (8, 60, 8, 128, 16),        # tight: preemption and recompute
+@pytest.mark.parametrize("seed,num_blocks,max_seqs,budget,n_req,max_new", [
+    (7, 600, 16, 256, 24, 24),  # roomy: prompts chunked across steps
+    (8, 32, 8, 128, 16, 48),    # tight: growing decodes force preemption and recompute
 ])
-def test_scheduler_drives_multi_query_steps(seed, num_blocks, max_seqs, budget, n_req):
+def test_scheduler_drives_multi_query_steps(seed, num_blocks, max_seqs, budget, n_req, max_new):
     """A whole serving step in one attention call: every scheduled row (prompt
     chunks and decode rows alike) writes its new K/V rows with one
     photon_cache_write and attends causally with one photon_paged_multi_query
     (query_start = the rows' cumulative query lengths); each step's output
     against the oracle's multi-query on the host mirror of the pool."""
-    max_prompt, max_new = 200, 24
+    max_prompt = 200
     mbs = (max_prompt + max_new + BS - 1) // BS
     trace = W.request_trace(seed, n_req, max_prompt=max_prompt, max_new=max_new,
                             pool_tokens=num_blocks * BS, arrivals_per_step=2.0)
