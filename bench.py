@@ -69,6 +69,8 @@ def parse():
                          "choice, --steps calls) and print its timing")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the side measurements of the other decode configurations")
+    ap.add_argument("--decode-consumer", type=int, default=0, choices=[0, 1, 2],
+                    help="decode attention consumer: 0 by group size, 1 CUDA cores, 2 tensor cores")
     ap.add_argument("--json-out", default="")
     return ap.parse_args()
 
@@ -198,7 +200,16 @@ def multi_query_side(P, torch, stream, flush_l2, K, hbm_peak, only: str = "",
     return res
 
 
-def configs_side(P, torch, stream, flush_l2, K, peak):
+def consumer_name(choice: int, wl: W.Workload) -> str:
+    """Which decode consumer a workload runs under a selector value (the
+    library's rule: tensor cores for 16-bit storage with 2+ q heads per KV
+    head by default)."""
+    g = wl.num_q_heads // wl.num_kv_heads
+    tc = wl.dtype != W.DTYPE_F32 and (choice == 2 or (choice == 0 and g >= 2))
+    return "tensor cores (mma.sync)" if tc else "CUDA cores"
+
+
+def configs_side(P, torch, stream, flush_l2, K, peak, choice=0):
     """The other decode configurations (Llama-3.2-1B-shaped batch 16, the
     batch sweep 4/8/16/32, the batch-256 serving mix): fused step per call,
     L2 flushed before each; for the mix also the cache write and the decode
@@ -232,15 +243,24 @@ def configs_side(P, torch, stream, flush_l2, K, peak):
         nws = P.photon_paged_decode_workspace_size(shape)
         ws = torch.empty(max(nws, 16), dtype=torch.uint8, device="cuda")
         T = wl.slot_mapping.shape[0]
-        ms = timed(lambda: P.photon_paged_decode_step(kn, vn, sm, q, kc, vc, bt, cl, wl.scale,
-                                                      out, ws, nws, shape, stream))
+        def fused():
+            P.photon_paged_decode_step(kn, vn, sm, q, kc, vc, bt, cl, wl.scale, out, ws, nws,
+                                       shape, stream)
+        ms = timed(fused)
+        # the same step on each consumer, for comparison
+        per_consumer = {}
+        for which, key in ((1, "cuda_cores"), (2, "tensor_cores")):
+            P.photon_debug_set_decode_consumer(which)
+            per_consumer[key] = round(timed(fused), 5)
+        P.photon_debug_set_decode_consumer(choice)
         nbytes = wl.decode_bytes() + wl.cache_write_bytes()
         gbs = nbytes / (ms / 1e3) / 1e9
         r = {"ms_per_step": round(ms, 5), "GBps": round(gbs, 1),
              "hbm_fraction": round(gbs / peak, 4),
              "tokens_attended_per_s": round(wl.tokens_attended() / (ms / 1e3), 1),
              "decode_tokens_per_s_per_layer": round(wl.num_seqs / (ms / 1e3), 1),
-             "algorithmic_bytes": int(nbytes)}
+             "algorithmic_bytes": int(nbytes), "consumer": consumer_name(choice, wl),
+             "ms_per_consumer": per_consumer}
         if name == "mix_b256":
             ms_w = timed(lambda: P.photon_cache_write(kn, vn, sm, T, kc, vc, shape, stream))
             ms_d = timed(lambda: P.photon_paged_decode(q, kc, vc, bt, cl, wl.scale, out, ws, nws,
@@ -475,6 +495,7 @@ def run_ours(args):
         pg = dist
     torch.cuda.set_device(local)
     P.build()
+    P.photon_debug_set_decode_consumer(args.decode_consumer)
 
     wl = make_workload(args.workload, rank)
     shape = P.PagedShape.make(partition_size=args.partition, **wl.shape_dict())
@@ -706,7 +727,7 @@ def run_ours(args):
     host_sched = scheduler_side(P) if rank == 0 and not args.no_mq else None
     other_configs = None
     if not args.no_configs:
-        other_configs = configs_side(P, torch, stream, flush_l2, K, peak)
+        other_configs = configs_side(P, torch, stream, flush_l2, K, peak, args.decode_consumer)
     achieved = decode_bytes / (attn_mean_ms / 1e3) / 1e9
     roofline = {"bound": "hbm",
                 "kernel": "paged_decode_attention_kernel + paged_decode_merge_kernel",
@@ -732,6 +753,7 @@ def run_ours(args):
                        "head_dim": wl.head_dim, "block_size": wl.block_size,
                        "num_blocks": wl.num_blocks, "tokens_attended": wl.tokens_attended(),
                        "partition_size": plan["partition_size"],
+                       "decode_consumer": consumer_name(args.decode_consumer, wl),
                        "l2": "flushed before every step (512 MB write + 256 MB read of another buffer), outside the timed events; step working set 478 MB > L2",
                        "parallelism": f"dp{world} (independent batches per GPU)"},
             "hbm_fraction": round(value / peak, 4),

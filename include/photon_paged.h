@@ -237,6 +237,16 @@ photon_status_t photon_paged_multi_query(const void* q, const void* k_cache, con
 size_t photon_paged_multi_query_workspace_size(const photon_paged_shape_t* shape,
                                                int32_t num_tokens, int32_t max_query_len);
 
+/* Test and tuning hook: which consumer the decode attention kernel runs
+ * (photon_paged_decode, _step, _noalloc; the RoPE step always takes the
+ * CUDA-core one).  0 (default) = by the group size: the tensor-core consumer
+ * (mma.sync over tensor-map copies of the blocks) for fp16/bf16 storage and
+ * 2 or more query heads per KV head, the CUDA-core consumer otherwise; 1 =
+ * always the CUDA-core consumer; 2 = the tensor-core one wherever the storage
+ * type is fp16 or bf16.  Results agree within the documented tolerance, not
+ * bit for bit.  Process-wide; PHOTON_ERR_INVALID_ARG for another value. */
+photon_status_t photon_debug_set_decode_consumer(int32_t which);
+
 /* Test and tuning hook: which kernel photon_paged_multi_query runs.
  * 0 (default) = chosen by the plan: the tcgen05/TMEM kernel (256-row
  * tiles, no key split) when the query tiles fill the device without a split,

@@ -29,6 +29,7 @@ __all__ = [
     "photon_paged_decode_noalloc", "photon_paged_decode_step",
     "photon_rope_cos_sin", "photon_paged_decode_step_rope", "photon_paged_multi_query",
     "photon_paged_multi_query_workspace_size", "photon_debug_set_multi_query_kernel",
+    "photon_debug_set_decode_consumer",
     "photon_debug_wait_probe", "Scheduler",
     "F32", "F16", "BF16", "STATUS",
 ]
@@ -109,6 +110,8 @@ def _load() -> ctypes.CDLL:
     lib.photon_debug_wait_probe.restype = ctypes.c_int
     lib.photon_debug_set_multi_query_kernel.argtypes = [I32]
     lib.photon_debug_set_multi_query_kernel.restype = ctypes.c_int
+    lib.photon_debug_set_decode_consumer.argtypes = [I32]
+    lib.photon_debug_set_decode_consumer.restype = ctypes.c_int
     lib.photon_paged_multi_query.restype = ctypes.c_int
     # host scheduler (include/photon_scheduler.h)
     lib.photon_scheduler_create.argtypes = [P, ctypes.POINTER(P)]
@@ -260,6 +263,13 @@ def photon_debug_set_multi_query_kernel(which: int) -> None:
     """0 = by the plan, 1 = warp-level mma.sync kernel, 2 = tcgen05 kernel."""
     _check(_load().photon_debug_set_multi_query_kernel(int(which)),
            "photon_debug_set_multi_query_kernel")
+
+
+def photon_debug_set_decode_consumer(which: int) -> None:
+    """Decode attention consumer: 0 = by group size, 1 = CUDA cores, 2 = tensor
+    cores (fp16/bf16 storage)."""
+    _check(_load().photon_debug_set_decode_consumer(int(which)),
+           "photon_debug_set_decode_consumer")
 
 
 def photon_paged_decode_noalloc(q, k_cache, v_cache, block_tables, context_lens, scale: float,

@@ -184,17 +184,6 @@ __device__ __forceinline__ uint64_t sw128_mn_desc(uint32_t saddr) {
   return d;
 }
 
-// 2-D tiled bulk tensor copy (box: 16 rows x 64 elements, 128-byte swizzle)
-// into this CTA's shared memory, completing on `bar`.
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
-                                            uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
-      "%3}], [%4];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
-      : "memory");
-}
-
 __device__ __forceinline__ void mbar_arrive_cnt(uint64_t* bar) { mbar_arrive(bar); }
 
 // Warp roles: a CTA owns 256 query rows of one (sequence, KV head) as two
@@ -342,9 +331,9 @@ __global__ void __launch_bounds__(TcCfg<T, D>::kThreads)
         const int y = (phys[i] * a.Hkv + kvh) * kBlockSize;
 #pragma unroll
         for (int h = 0; h < D / 64; ++h) {
-          tma_load_2d(sK + st * C::kKBytes + h * (kTcKeys * 128) + i * 2048, &tm_k, h * 64, y,
+          tma_load_box(sK + st * C::kKBytes + h * (kTcKeys * 128) + i * 2048, &tm_k, h * 64, y,
                       &kv_full[st]);
-          tma_load_2d(sV + st * C::kVBytes + h * (kTcKeys * 128) + i * 2048, &tm_v, h * 64, y,
+          tma_load_box(sV + st * C::kVBytes + h * (kTcKeys * 128) + i * 2048, &tm_v, h * 64, y,
                       &kv_full[st]);
         }
       }
@@ -556,8 +545,6 @@ __global__ void __launch_bounds__(TcCfg<T, D>::kThreads)
 
 }  // namespace
 
-// Tensor map over a K or V pool seen as rows of head_dim elements:
-// (num_blocks x Hkv x 16) rows, box 16 rows x 64 elements, 128-byte swizzle.
 cudaError_t make_pool_map(CUtensorMap* map, const void* pool, int dtype, int NB, int Hkv, int D) {
   using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
                                 const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,

@@ -43,6 +43,9 @@
 
 #include <float.h>
 #include <math.h>
+#include <string.h>
+
+#include <type_traits>
 
 #include "photon_common.cuh"
 
@@ -79,7 +82,11 @@ enum : int { kFirst = 1, kLast = 2, kDone = 4 };
 constexpr int kMaxRuns = 10;
 
 // Persistent-kernel geometry: NC consumer warps, 1 producer warp, S ring stages.
-template <typename T, int D, int G, int NC, int S, bool R = false>
+// M: the tensor-core consumer, whose blocks arrive as swizzled tensor-map
+// copies: every block starts on a 1024-byte swizzle atom (the dynamic
+// shared-memory base is aligned up at run time, hence kAlignPad), and the
+// fused step's new K/V row lands in a side slot of its stage.
+template <typename T, int D, int G, int NC, int S, bool R = false, bool M = false>
 struct PersistCfg {
   using C = DecodeCfg<T, D, G>;
   static constexpr int kThreads = (NC + 1) * 32;
@@ -97,12 +104,19 @@ struct PersistCfg {
   static constexpr int kOffRuns = kOffAbort + 4;                        // int[kMaxRuns + 1]
   static constexpr int kOffHdr = (kOffRuns + 4 * (kMaxRuns + 1) + 15) / 16 * 16;
   static constexpr int kOffQ = (kOffHdr + (int)sizeof(StageHdr) * S + 127) / 128 * 128;
-  static constexpr int kOffKV = kOffQ + kQStride * S;
+  static constexpr int kKVAlign = M ? 1024 : 128;
+  static constexpr int kOffKV = (kOffQ + kQStride * S + kKVAlign - 1) / kKVAlign * kKVAlign;
+  // M only: the new token's K row then V row, per stage
+  static constexpr int kSideBytes = M ? 2 * D * (int)sizeof(T) : 0;
+  static constexpr int kOffSide = kOffKV + kStageBytes * S;
   // Per-warp partial state at an item's end, double-buffered by item parity.
-  static constexpr int kOffPm = kOffKV + kStageBytes * S;       // float[2][NC][G]
+  static constexpr int kOffPm = kOffSide + kSideBytes * S;      // float[2][NC][G]
   static constexpr int kOffPl = kOffPm + 4 * 2 * NC * G;        // float[2][NC][G]
   static constexpr int kOffPo = (kOffPl + 4 * 2 * NC * G + 15) / 16 * 16;   // float[2][NC][G][D]
-  static constexpr int kSmemBytes = kOffPo + 4 * 2 * NC * G * D;
+  static constexpr int kAlignPad = M ? 1024 : 0;
+  static constexpr int kSmemBytes = kOffPo + 4 * 2 * NC * G * D + kAlignPad;
+  static_assert(!M || (kBlockBytes % 1024 == 0 && sizeof(T) == 2), "swizzled blocks");
+  static_assert(!(M && R), "the tensor-core consumer has no RoPE form");
 };
 
 // ------------------------------------------------------------------ consumer math
@@ -181,6 +195,98 @@ __device__ __forceinline__ void attend_block(const T* __restrict__ ks, const T* 
       l[g] += pw;
 #pragma unroll
       for (int e = 0; e < C::kEPL; ++e) o[g][e] = fmaf(pw, vf[e], o[g][e]);
+    }
+  }
+}
+
+// ------------------------------------------------------------------ tensor-core consumer math
+// Byte offset of 16-byte chunk `chunk` (0 .. D/8 - 1) of row `row` of a block
+// as the tensor-map copies lay it out: D/64 column halves of 16 rows x 128 B,
+// the 128-byte swizzle inside each 8-row atom.
+__device__ __forceinline__ uint32_t blk_chunk(int row, int chunk) {
+  return (uint32_t)((chunk >> 3) * 2048 + row * 128 + (((chunk & 7) ^ (row & 7)) << 4));
+}
+
+// One 16-token block for one warp on mma.sync m16n8k16 (fp32 accumulate).
+// The G query rows of the KV head's group are the n = 8 columns (slots >= G
+// hold zero rows), so the block's keys and the head dimension are the m side:
+//   S^T (16 keys x 8)  = K (16 x D) * Q^T (D x 8),       D/16 products;
+//   O^T (D x 8)       += V^T (D x 16 keys) * P^T (16 x 8), D/16 products per
+//                        half of P (below).
+// Lane l holds query slots 2(l%4) and 2(l%4)+1: their scores for keys l/4 and
+// l/4 + 8, their running max m and a partial sum l over the keys this lane
+// sees, and their O^T accumulators for dims 16i + l/4 and 16i + l/4 + 8.
+// P^T, the B operand of the second product, is the score fragment packed and
+// transposed 8x8 at a time (movmatrix).  P is split into a rounded part and
+// its rounding residual, two products, so the weights enter the sum with
+// about 2^-17 relative error instead of one storage-type rounding; the sums l
+// take the fp32 weights.  Scores are the fp32 products times qscale.
+// Rows >= n_valid: their scores are set to -inf and their V rows must be
+// zero (0 * NaN would otherwise reach the accumulators).
+template <typename T, int D>
+__device__ __forceinline__ void attend_block_mma(uint32_t kblk, uint32_t vblk, int n_valid,
+                                                 float qscale, const uint32_t (&bq)[D / 16][2],
+                                                 float (&m)[2], float (&l)[2],
+                                                 float (&o)[D / 16][4], int lane) {
+  const int r = lane >> 2;
+  float s[4] = {0.f, 0.f, 0.f, 0.f};
+  {
+    // ldmatrix row addresses: matrices (keys 0-7 | 8-15) x (dims lo | hi of the k-step)
+    const int krow = (lane & 7) + ((lane >> 3) & 1) * 8;
+    const int khi = lane >> 4;
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      uint32_t a[4];
+      ldsm_x4(kblk + blk_chunk(krow, 2 * kk + khi), a[0], a[1], a[2], a[3]);
+      Mma<T>::run(s, a, bq[kk][0], bq[kk][1]);
+    }
+  }
+  const bool v0 = r < n_valid, v1 = r + 8 < n_valid;
+  const float x0 = v0 ? s[0] * qscale : -INFINITY;   // key r,     slot 2t
+  const float x1 = v0 ? s[1] * qscale : -INFINITY;   // key r,     slot 2t + 1
+  const float x2 = v1 ? s[2] * qscale : -INFINITY;   // key r + 8, slot 2t
+  const float x3 = v1 ? s[3] * qscale : -INFINITY;   // key r + 8, slot 2t + 1
+  float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+#pragma unroll
+  for (int off = 4; off < 32; off <<= 1) {
+    mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+  }
+  // key 0 is always valid, so the block maxima are finite
+  const float n0 = fmaxf(m[0], mx0), n1 = fmaxf(m[1], mx1);
+  if (__any_sync(0xffffffffu, n0 > m[0] || n1 > m[1])) {
+    const float c0 = softmax_exp2(m[0] - n0), c1 = softmax_exp2(m[1] - n1);
+    l[0] *= c0;
+    l[1] *= c1;
+#pragma unroll
+    for (int i = 0; i < D / 16; ++i) {
+      o[i][0] *= c0;
+      o[i][1] *= c1;
+      o[i][2] *= c0;
+      o[i][3] *= c1;
+    }
+    m[0] = n0;
+    m[1] = n1;
+  }
+  const float p0 = softmax_exp2(x0 - m[0]), p1 = softmax_exp2(x1 - m[1]);
+  const float p2 = softmax_exp2(x2 - m[0]), p3 = softmax_exp2(x3 - m[1]);
+  l[0] += p0 + p2;
+  l[1] += p1 + p3;
+  const uint32_t h01 = Mma<T>::pack(p0, p1), h23 = Mma<T>::pack(p2, p3);
+  const float2 r01 = Mma<T>::unpack(h01), r23 = Mma<T>::unpack(h23);
+  const uint32_t b0 = movmatrix_trans(h01), b1 = movmatrix_trans(h23);
+  const uint32_t e0 = movmatrix_trans(Mma<T>::pack(p0 - r01.x, p1 - r01.y));
+  const uint32_t e1 = movmatrix_trans(Mma<T>::pack(p2 - r23.x, p3 - r23.y));
+  {
+    // ldmatrix.trans row addresses: matrices (keys 0-7 | 8-15) x (dims lo | hi of the tile)
+    const int vrow = (lane & 7) + (lane >> 4) * 8;
+    const int vhi = (lane >> 3) & 1;
+#pragma unroll
+    for (int i = 0; i < D / 16; ++i) {
+      uint32_t a[4];
+      ldsm_x4_trans(vblk + blk_chunk(vrow, 2 * i + vhi), a[0], a[1], a[2], a[3]);
+      Mma<T>::run(o[i], a, b0, b1);
+      Mma<T>::run(o[i], a, e0, e1);
     }
   }
 }
@@ -290,12 +396,20 @@ static __device__ unsigned long long g_probe[kProbeCtas][kProbeSlots];
 // kRope: the fused step with the rotary embedding (q rows and the new K row
 // turn by the token's position); a separate instantiation, so the plain path
 // carries none of it.
-template <typename T, int D, int G, int NC, int S, bool kRope>
+// kMma: the tensor-core consumer (attend_block_mma); its K/V blocks arrive as
+// tensor-map copies (tmk, tmv: the pools as rows of D elements, boxes of 16
+// rows x 64 elements, 128-byte swizzle).  The other instantiations take the
+// maps but never read them.
+template <typename T, int D, int G, int NC, int S, bool kRope, bool kMma>
 __global__ void __launch_bounds__((NC + 1) * 32, 1)
-    paged_decode_attention_kernel(const DecodeArgs a) {
-  using PC = PersistCfg<T, D, G, NC, S, kRope>;
+    paged_decode_attention_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
+                                  const __grid_constant__ CUtensorMap tmv) {
+  using PC = PersistCfg<T, D, G, NC, S, kRope, kMma>;
   using C = DecodeCfg<T, D, G>;
-  extern __shared__ __align__(128) unsigned char smem[];
+  extern __shared__ __align__(128) unsigned char smem_raw[];
+  // swizzled tensor copies want their 1024-byte atoms aligned in the shared window
+  unsigned char* const smem =
+      kMma ? smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u) : smem_raw;
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + PC::kOffFull);
   uint64_t* empty = reinterpret_cast<uint64_t*>(smem + PC::kOffEmpty);
   uint64_t* sync = reinterpret_cast<uint64_t*>(smem + PC::kOffSync);
@@ -542,7 +656,9 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
         const int new_lane = new_mask ? __ffs(new_mask) - 1 : -1;
         const int new_phys = __shfl_sync(0xffffffffu, phys, new_lane >= 0 ? new_lane : 0);
         const int new_rows = __shfl_sync(0xffffffffu, rows, new_lane >= 0 ? new_lane : 0);
-        int bytes = valid ? 2 * rows * D * (int)sizeof(T) : 0;
+        // tensor-map copies move whole 16-row boxes; the new row rides beside them
+        int bytes = valid ? 2 * (kMma ? kBlockSize : rows) * D * (int)sizeof(T) : 0;
+        if (kMma && new_here) bytes += 2 * D * (int)sizeof(T);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
         const bool first = k0 == 0;
@@ -567,7 +683,23 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
         }
         __syncwarp();
         unsigned char* stage = smem + PC::kOffKV + slot * PC::kStageBytes;
-        if (valid) {
+        if (kMma && valid) {
+          const int y = (phys * a.Hkv + kvh) * kBlockSize;
+          const uint32_t kd = smem_addr(stage + lane * PC::kBlockBytes);
+          const uint32_t vd = smem_addr(stage + (NC + lane) * PC::kBlockBytes);
+#pragma unroll
+          for (int hx = 0; hx < D / 64; ++hx) {
+            tma_load_box(kd + hx * 2048, &tmk, hx * 64, y, &full[slot]);
+            tma_load_box(vd + hx * 2048, &tmv, hx * 64, y, &full[slot]);
+          }
+          if (new_here) {
+            const size_t nsrc = ((size_t)it0.b * a.Hkv + kvh) * D;
+            const uint32_t rb = (uint32_t)(D * (int)sizeof(T));
+            unsigned char* side = smem + PC::kOffSide + slot * PC::kSideBytes;
+            bulk_copy_g2s(side, static_cast<const T*>(a.k_new) + nsrc, rb, &full[slot]);
+            bulk_copy_g2s(side + rb, static_cast<const T*>(a.v_new) + nsrc, rb, &full[slot]);
+          }
+        } else if (valid) {
           const size_t src = (size_t)phys * a.Hkv * PC::kBlockElems + head_off;
           const int cache_rows = new_here ? rows - 1 : rows;
           const uint32_t nbytes = (uint32_t)(cache_rows * D * (int)sizeof(T));
@@ -643,6 +775,10 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
   // ================================================================== consumers
   float qf[G][C::kEPL];
   float m[G], l[G], o[G][C::kEPL];
+  // tensor-core consumer: Q^T operand fragments, (m, l) of slots 2(l%4) and
+  // 2(l%4)+1, O^T accumulators
+  uint32_t tq[kMma ? D / 16 : 1][2];
+  float tm[2], tl[2], to[kMma ? D / 16 : 1][4];
   RopeLaneCs<D> kcs;  // RoPE only: this lane's (cos, sin) pairs of the current item
   float* const pm_buf = reinterpret_cast<float*>(smem + PC::kOffPm);
   float* const pl_buf = reinterpret_cast<float*>(smem + PC::kOffPl);
@@ -668,7 +804,19 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
       if (ctid == 0) PROBE_SET(4, global_timer_ns());
       return;
     }
-    if (h.flags & kFirst) {
+    if (kMma && (h.flags & kFirst)) {
+      const uint32_t* q32 = reinterpret_cast<const uint32_t*>(smem + PC::kOffQ + slot * PC::kQStride);
+      const int slot_g = lane >> 2, t2 = 2 * (lane & 3);
+#pragma unroll
+      for (int kk = 0; kk < (kMma ? D / 16 : 1); ++kk) {
+        tq[kk][0] = slot_g < G ? q32[(slot_g * D + 16 * kk + t2) / 2] : 0u;
+        tq[kk][1] = slot_g < G ? q32[(slot_g * D + 16 * kk + t2 + 8) / 2] : 0u;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) to[kk][j] = 0.f;
+      }
+      tm[0] = tm[1] = -INFINITY;
+      tl[0] = tl[1] = 0.f;
+    } else if (h.flags & kFirst) {
       const T* qs = reinterpret_cast<const T*>(smem + PC::kOffQ + slot * PC::kQStride);
 #pragma unroll
       for (int g = 0; g < G; ++g) {
@@ -701,7 +849,43 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
           for (int e = 0; e < C::kEPL; ++e) qf[g][e] *= a.qscale;
       }
     }
-    if (warp < h.nblk && ((h.flags >> (8 + warp)) & 1)) {
+    if (kMma && warp < h.nblk && ((h.flags >> (8 + warp)) & 1)) {
+      unsigned char* const kb = smem + PC::kOffKV + slot * PC::kStageBytes + warp * PC::kBlockBytes;
+      unsigned char* const vb = kb + NC * PC::kBlockBytes;
+      const int n_valid = min(kBlockSize, h.tok_end - (h.blk0 + warp) * kBlockSize);
+      constexpr int kRowChunks = D * (int)sizeof(T) / 16;
+      bool wrote = false;
+      if (warp == h.new_warp) {
+        // fused step: the new token's rows came beside the stage; put them in
+        // row new_row of the blocks (the box brought that slot's stale row)
+        // and store them to their cache slot
+        const unsigned char* side = smem + PC::kOffSide + slot * PC::kSideBytes;
+        const size_t dst = (((size_t)h.new_phys * a.Hkv + h.kvh) * kBlockSize + h.new_row) * D;
+        for (int i = lane; i < 2 * kRowChunks; i += 32) {
+          const bool is_v = i >= kRowChunks;
+          const int ch = is_v ? i - kRowChunks : i;
+          const uint4 val = *reinterpret_cast<const uint4*>(side + i * 16);
+          *reinterpret_cast<uint4*>((is_v ? vb : kb) + blk_chunk(h.new_row, ch)) = val;
+          T* cache = static_cast<T*>(is_v ? a.v_cache_w : a.k_cache_w);
+          *reinterpret_cast<uint4*>(cache + dst + ch * (16 / (int)sizeof(T))) = val;
+        }
+        wrote = true;
+      }
+      if (n_valid < kBlockSize) {
+        // rows past the context carry whatever the pool holds: zero their V
+        for (int i = lane; i < (kBlockSize - n_valid) * kRowChunks; i += 32)
+          *reinterpret_cast<uint4*>(vb + blk_chunk(n_valid + i / kRowChunks, i % kRowChunks)) =
+              make_uint4(0u, 0u, 0u, 0u);
+        wrote = true;
+      }
+      if (wrote) {
+        fence_proxy_async_smem();  // the stage is refilled by tensor copies later
+        __syncwarp();
+      }
+      if constexpr (kMma)
+        attend_block_mma<T, D>(smem_addr(kb), smem_addr(vb), n_valid, a.qscale, tq, tm, tl, to,
+                               lane);
+    } else if (warp < h.nblk && ((h.flags >> (8 + warp)) & 1)) {
       const T* stage = reinterpret_cast<const T*>(smem + PC::kOffKV + slot * PC::kStageBytes);
       const int n_valid = min(kBlockSize, h.tok_end - (h.blk0 + warp) * kBlockSize);
       if (kRope && warp == h.new_warp) {
@@ -709,6 +893,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
         // before it is attended and stored
         rope_row<T, D>(const_cast<T*>(stage) + warp * PC::kBlockElems + h.new_row * D, kcs,
                        a.rope_max_pos, h.pos, lane);
+        fence_proxy_async_smem();  // the stage is refilled by bulk copies later
         __syncwarp();
       }
       attend_block<T, D, G>(stage + warp * PC::kBlockElems, stage + (NC + warp) * PC::kBlockElems,
@@ -742,8 +927,32 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
     float* const pl = pl_buf + parity * NC * G;
     float* const po = po_buf + parity * NC * G * D;
     parity ^= 1;
+    if constexpr (kMma) {
+      // lane partial sums over the 8 key rows; slots >= G are padding
 #pragma unroll
-    for (int g = 0; g < G; ++g) {
+      for (int off = 4; off < 32; off <<= 1) {
+        tl[0] += __shfl_xor_sync(0xffffffffu, tl[0], off);
+        tl[1] += __shfl_xor_sync(0xffffffffu, tl[1], off);
+      }
+      const int r = lane >> 2;
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int g = 2 * (lane & 3) + j;
+        if (g < G) {
+#pragma unroll
+          for (int i = 0; i < (kMma ? D / 16 : 1); ++i) {
+            po[(warp * G + g) * D + 16 * i + r] = to[i][j];
+            po[(warp * G + g) * D + 16 * i + r + 8] = to[i][2 + j];
+          }
+          if (r == 0) {
+            pm[warp * G + g] = tm[j];
+            pl[warp * G + g] = tl[j];
+          }
+        }
+      }
+    }
+#pragma unroll
+    for (int g = 0; g < (kMma ? 0 : G); ++g) {
       l[g] += __shfl_xor_sync(0xffffffffu, l[g], 8);
       l[g] += __shfl_xor_sync(0xffffffffu, l[g], 16);
 #pragma unroll
@@ -752,7 +961,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
         o[g][e] += __shfl_xor_sync(0xffffffffu, o[g][e], 16);
       }
     }
-    if (tg == 0) {
+    if (!kMma && tg == 0) {
 #pragma unroll
       for (int g = 0; g < G; ++g) {
 #pragma unroll
@@ -918,15 +1127,15 @@ __global__ void __launch_bounds__(kMergeWarps * 32) paged_decode_merge_kernel(co
 
 // Resident CTAs per SM of an attention-kernel instantiation (queried once per
 // device, after raising its dynamic shared-memory limit).
-template <typename T, int D, int G, int NC, int S, bool kRope>
+template <typename T, int D, int G, int NC, int S, bool kRope, bool kMma>
 int attention_ctas_per_sm() {
-  using PC = PersistCfg<T, D, G, NC, S, kRope>;
+  using PC = PersistCfg<T, D, G, NC, S, kRope, kMma>;
   constexpr int kMaxDev = 64;
   static int cache[kMaxDev];  // 0 = not yet queried
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
   if (cache[dev] > 0) return cache[dev];
-  auto kern = paged_decode_attention_kernel<T, D, G, NC, S, kRope>;
+  auto kern = paged_decode_attention_kernel<T, D, G, NC, S, kRope, kMma>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PC::kSmemBytes) !=
       cudaSuccess)
     return 0;
@@ -955,29 +1164,64 @@ constexpr int stages_for(int nc) {
              : (kRingBytes / (2 * nc * kBlockSize * D * (int)sizeof(T)));
 }
 
+// Which consumer a (D, G) instantiation runs by default: the tensor-core one
+// for 16-bit storage and groups of PHOTON_MMA_MIN_G or more query heads per KV
+// head.  The CUDA-core consumer spends about 33 instructions per K/V element
+// pair and query head (widening, G dot products with shuffle reductions, G
+// weighted sums); at G = 4, d = 64 that outruns the issue rate (ncu: issue
+// slots 57% busy, DRAM 47%), and at G = 2, d = 128 it still costs about 7% of
+// the step against the tensor-core consumer.
+#ifndef PHOTON_MMA_MIN_G
+#define PHOTON_MMA_MIN_G 2
+#endif
+
+template <typename T, int D, int G, int NC, int S, bool kRope, bool kMma>
+cudaError_t launch_attention(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
+                             cudaStream_t stream) {
+  using PC = PersistCfg<T, D, G, NC, S, kRope, kMma>;
+  const int per_sm = attention_ctas_per_sm<T, D, G, NC, S, kRope, kMma>();
+  if (per_sm <= 0) return cudaErrorInvalidConfiguration;
+  return launch_pdl(paged_decode_attention_kernel<T, D, G, NC, S, kRope, kMma>,
+                    dim3(per_sm * a.num_sms), dim3(PC::kThreads), PC::kSmemBytes, stream, a, tk,
+                    tv);
+}
+
 template <typename T, int D, int G>
 cudaError_t launch_decode_impl(const DecodeArgs& a0, cudaStream_t stream) {
   constexpr int NC = PHOTON_CONSUMER_WARPS;
   constexpr int S = stages_for<T, D>(NC);
-  using PC = PersistCfg<T, D, G, NC, S>;
   DecodeArgs a = a0;
   // Every buffer the kernels touch must have been carved out by the caller.
   if (!a.q || !a.k_cache || !a.v_cache || !a.block_tables || !a.context_lens || !a.out ||
       !a.ws_m || !a.ws_l || !a.ws_o || !a.ws_ctrl || !a.err)
     return cudaErrorInvalidValue;
   const bool rope = a.rope_cs != nullptr;
-  const int per_sm = rope ? attention_ctas_per_sm<T, D, G, NC, S, true>()
-                          : attention_ctas_per_sm<T, D, G, NC, S, false>();
-  if (per_sm <= 0) return cudaErrorInvalidConfiguration;
-  const int grid = per_sm * a.num_sms;
+  CUtensorMap tk, tv;
+  memset(&tk, 0, sizeof(tk));
+  memset(&tv, 0, sizeof(tv));
+  bool mma = false;
+  if constexpr (sizeof(T) == 2) {
+    const int choice = g_decode_consumer.load(std::memory_order_relaxed);  // 0: by group size, 1: CUDA cores, 2: tensor cores
+    mma = !rope && (choice == 2 || (choice == 0 && G >= PHOTON_MMA_MIN_G)) &&
+          (int64_t)a.NB * a.Hkv * kBlockSize <= INT32_MAX;
+    const int dt = std::is_same<T, __half>::value ? 1 : 2;
+    if (mma && (make_pool_map(&tk, a.k_cache, dt, a.NB, a.Hkv, D) != cudaSuccess ||
+                make_pool_map(&tv, a.v_cache, dt, a.NB, a.Hkv, D) != cudaSuccess))
+      return cudaErrorInvalidValue;
+  }
 
   if (a.ev_start) cudaEventRecord(a.ev_start, stream);
-  using PCR = PersistCfg<T, D, G, NC, S, true>;
-  cudaError_t err =
-      rope ? launch_pdl(paged_decode_attention_kernel<T, D, G, NC, S, true>, dim3(grid),
-                        dim3(PCR::kThreads), PCR::kSmemBytes, stream, a)
-           : launch_pdl(paged_decode_attention_kernel<T, D, G, NC, S, false>, dim3(grid),
-                        dim3(PC::kThreads), PC::kSmemBytes, stream, a);
+  cudaError_t err;
+  if (rope) {
+    err = launch_attention<T, D, G, NC, S, true, false>(a, tk, tv, stream);
+  } else if (mma) {
+    if constexpr (sizeof(T) == 2)
+      err = launch_attention<T, D, G, NC, S, false, true>(a, tk, tv, stream);
+    else
+      err = cudaErrorInvalidValue;
+  } else {
+    err = launch_attention<T, D, G, NC, S, false, false>(a, tk, tv, stream);
+  }
   if (err != cudaSuccess) return err;
   const int items = a.B * a.Hq;
   err = launch_pdl(paged_decode_merge_kernel<T, D>, dim3((items + kMergeWarps - 1) / kMergeWarps),

@@ -17,6 +17,7 @@
 namespace photon {
 // selftest.cu
 cudaError_t launch_wait_probe(unsigned long long limit_ns, uint32_t* err, cudaStream_t stream);
+std::atomic<int> g_decode_consumer{0};
 }  // namespace photon
 
 namespace {
@@ -476,6 +477,12 @@ photon_status_t photon_paged_multi_query(const void* q, const void* k_cache, con
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const cudaError_t e = tc ? photon::launch_multi_query_tc(a, s) : photon::launch_multi_query(a, s);
   return e == cudaSuccess ? PHOTON_OK : PHOTON_ERR_CUDA;
+}
+
+photon_status_t photon_debug_set_decode_consumer(int32_t which) {
+  if (which < 0 || which > 2) return PHOTON_ERR_INVALID_ARG;
+  photon::g_decode_consumer.store(which, std::memory_order_relaxed);
+  return PHOTON_OK;
 }
 
 photon_status_t photon_debug_set_multi_query_kernel(int32_t which) {

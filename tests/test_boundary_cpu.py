@@ -186,6 +186,13 @@ def test_multi_query_kernel_hook(lib):
         assert lib.photon_debug_set_multi_query_kernel(k) == 0
 
 
+def test_decode_consumer_hook(lib):
+    assert lib.photon_debug_set_decode_consumer(3) == 1
+    assert lib.photon_debug_set_decode_consumer(-1) == 1
+    for k in (1, 2, 0):
+        assert lib.photon_debug_set_decode_consumer(k) == 0
+
+
 def test_wait_probe_argument_check(lib):
     assert lib.photon_debug_wait_probe(0, None) == 1
     assert lib.photon_debug_wait_probe(2_000_000_000, None) == 1

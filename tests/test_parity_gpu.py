@@ -8,6 +8,10 @@ the same seeded host bytes.
   partition size, unreferenced NaN-filled blocks, device-side index errors;
 * the full-size long-context batch-64 and batch-256 step workloads in the
   launch configuration the benchmark times.
+
+The decode tests run under both attention consumers (photon_debug_set_decode_
+consumer): the CUDA-core one and the tensor-core one (fp16/bf16 storage; fp32
+cases take the CUDA-core path either way).
 """
 import os
 
@@ -30,6 +34,23 @@ def _lib():
     torch.cuda.init()
     st, _ = P.photon_get_last_device_error()
     assert st == 0
+
+
+@pytest.fixture(params=[1, 2], ids=["cuda_cores", "tensor_cores"])
+def consumer(request):
+    P.photon_debug_set_decode_consumer(request.param)
+    yield request.param
+    P.photon_debug_set_decode_consumer(0)
+
+
+_ORACLE_CACHE = {}
+
+
+def _oracle_step_cached(key: str, wl: W.Workload):
+    """_oracle_step of a named workload, computed once per test session."""
+    if key not in _ORACLE_CACHE:
+        _ORACLE_CACHE[key] = _oracle_step(wl)
+    return _ORACLE_CACHE[key]
 
 
 def _oracle_step(wl: W.Workload, write: bool = True):
@@ -135,10 +156,10 @@ CASES = {
 
 
 @pytest.mark.parametrize("name", sorted(CASES))
-def test_step_matches_oracle(name):
+def test_step_matches_oracle(name, consumer):
     """cache write + decode in one stream, against the oracle's step."""
     wl = CASES[name]()
-    kc, vc, want = _oracle_step(wl)
+    kc, vc, want = _oracle_step_cached(name, wl)
     d = DeviceWorkload(wl)
     d.cache_write()
     d.decode()
@@ -149,12 +170,12 @@ def test_step_matches_oracle(name):
 
 
 @pytest.mark.parametrize("name", sorted(CASES) + ["qwen_b64", "mix_b256"])
-def test_fused_step_matches_oracle_and_separate_calls(name):
+def test_fused_step_matches_oracle_and_separate_calls(name, consumer):
     """photon_paged_decode_step == cache write then decode: output against the
     oracle, the written rows bit for bit, and bit-identical to the two
     separate calls."""
     wl = {"qwen_b64": W.qwen_b64, "mix_b256": W.mix_b256}.get(name, CASES.get(name))()
-    kc, vc, want = _oracle_step(wl)
+    kc, vc, want = _oracle_step_cached(name, wl)
     fused = DeviceWorkload(wl)
     fused.step()
     sep = DeviceWorkload(wl)
@@ -176,7 +197,7 @@ def test_fused_step_matches_oracle_and_separate_calls(name):
         assert host(fused.v_cache, vc).tobytes() == vc.tobytes()
 
 
-def test_fused_step_flags_a_slot_that_disagrees_with_the_table():
+def test_fused_step_flags_a_slot_that_disagrees_with_the_table(consumer):
     wl = W.random_small(56, batch=4, num_q_heads=8, num_kv_heads=2, head_dim=64, max_ctx=70,
                         dtype=W.DTYPE_F16, context_lens=[20, 33, 64, 70], extra_blocks=4)
     slots = wl.slot_mapping.copy()
@@ -198,7 +219,7 @@ def test_fused_step_flags_a_slot_that_disagrees_with_the_table():
 
 
 @pytest.mark.parametrize("part", [16, 32, 48, 128, 512, 4096])
-def test_partition_size_invariance(part):
+def test_partition_size_invariance(part, consumer):
     wl = W.random_small(51, batch=6, num_q_heads=16, num_kv_heads=8, head_dim=128,
                         max_ctx=1500, dtype=W.DTYPE_F16,
                         context_lens=[1, 16, 100, 777, 1024, 1500])
@@ -211,7 +232,7 @@ def test_partition_size_invariance(part):
 
 
 @pytest.mark.parametrize("dtype", [W.DTYPE_F16, W.DTYPE_BF16, W.DTYPE_F32])
-def test_one_token_context_is_v_exactly(dtype):
+def test_one_token_context_is_v_exactly(dtype, consumer):
     wl = W.random_small(52, batch=4, num_q_heads=8, num_kv_heads=2, head_dim=64, max_ctx=1,
                         dtype=dtype, context_lens=[1, 1, 1, 1])
     d = DeviceWorkload(wl)
@@ -223,7 +244,7 @@ def test_one_token_context_is_v_exactly(dtype):
             assert got[b, h].tobytes() == wl.v_cache[blk, h // 4, 0].tobytes()
 
 
-def test_zero_context_rows_are_zero_and_repeat_is_stable():
+def test_zero_context_rows_are_zero_and_repeat_is_stable(consumer):
     wl = W.random_small(53, batch=5, num_q_heads=4, num_kv_heads=1, head_dim=64, max_ctx=300,
                         dtype=W.DTYPE_F16, context_lens=[0, 300, 0, 17, 0])
     _, _, want = _oracle_step(wl, write=False)
@@ -239,7 +260,7 @@ def test_zero_context_rows_are_zero_and_repeat_is_stable():
 
 
 @pytest.mark.parametrize("maker", [W.qwen_b64, W.mix_b256])
-def test_fresh_and_reused_workspace_agree_bitwise(maker):
+def test_fresh_and_reused_workspace_agree_bitwise(maker, consumer):
     """A fresh workspace hands items out in a fixed order, a reused one through
     the work queue; every item is computed the same way, so the outputs must be
     identical bit for bit, call after call."""
@@ -256,7 +277,7 @@ def test_fresh_and_reused_workspace_agree_bitwise(maker):
     _no_device_error()
 
 
-def test_uniform_scores_give_mean_of_v():
+def test_uniform_scores_give_mean_of_v(consumer):
     wl = W.random_small(54, batch=3, num_q_heads=8, num_kv_heads=2, head_dim=128, max_ctx=700,
                         dtype=W.DTYPE_F16, context_lens=[5, 333, 700])
     d = DeviceWorkload(wl)
@@ -269,7 +290,7 @@ def test_uniform_scores_give_mean_of_v():
             assert np.abs(got[b, h] - mean).max() <= 2e-3
 
 
-def test_bad_block_and_context_are_flagged_not_faulted():
+def test_bad_block_and_context_are_flagged_not_faulted(consumer):
     wl = W.random_small(55, batch=4, num_q_heads=4, num_kv_heads=2, head_dim=64, max_ctx=90,
                         dtype=W.DTYPE_F16, context_lens=[40, 90, 33, 50])
     _, _, want = _oracle_step(wl, write=False)
@@ -290,7 +311,7 @@ def test_bad_block_and_context_are_flagged_not_faulted():
     _no_device_error()
 
 
-def test_nonzero_stream_and_unreferenced_blocks_untouched():
+def test_nonzero_stream_and_unreferenced_blocks_untouched(consumer):
     wl = W.llama_b16()
     d = DeviceWorkload(wl)
     s = torch.cuda.Stream()
@@ -304,12 +325,12 @@ def test_nonzero_stream_and_unreferenced_blocks_untouched():
 
 
 # ------------------------------------------------------------------ full-size workloads
-def test_qwen_b64_full_size_step():
+def test_qwen_b64_full_size_step(consumer):
     """Batch 64, 16q/8kv, d=128, contexts log-uniform 128..8192, 40 000-block
     pool: the benchmark's workload and launch configuration, every output row
     against the oracle."""
     wl = W.qwen_b64()
-    kc, vc, want = _oracle_step(wl)
+    kc, vc, want = _oracle_step_cached("qwen_b64", wl)
     d = DeviceWorkload(wl)
     d.cache_write()
     d.decode()
@@ -324,11 +345,11 @@ def test_qwen_b64_full_size_step():
     assert got_k.cpu().numpy().tobytes() == kc[blk, :, off].tobytes()
 
 
-def test_mix_b256_full_size_step():
+def test_mix_b256_full_size_step(consumer):
     """Batch 256 continuous-batching step: 256 rows into free-list slots, then
     decode, one stream; all rows against the oracle."""
     wl = W.mix_b256()
-    _, _, want = _oracle_step(wl)
+    _, _, want = _oracle_step_cached("mix_b256", wl)
     d = DeviceWorkload(wl)
     d.cache_write()
     d.decode()
