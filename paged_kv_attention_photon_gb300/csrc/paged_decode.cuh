@@ -109,12 +109,14 @@ struct PersistCfg {
   // M only: the new token's K row then V row, per stage
   static constexpr int kSideBytes = M ? 2 * D * (int)sizeof(T) : 0;
   static constexpr int kOffSide = kOffKV + kStageBytes * S;
-  // Per-warp partial state at an item's end, double-buffered by item parity.
+  // Per-warp (m, l) at an item's end, double-buffered by item parity.  The
+  // warps' o rows (G x D fp32 each) go to their own K block areas of the
+  // item's last stage, which is released only after the combine.
   static constexpr int kOffPm = kOffSide + kSideBytes * S;      // float[2][NC][G]
   static constexpr int kOffPl = kOffPm + 4 * 2 * NC * G;        // float[2][NC][G]
-  static constexpr int kOffPo = (kOffPl + 4 * 2 * NC * G + 15) / 16 * 16;   // float[2][NC][G][D]
   static constexpr int kAlignPad = M ? 1024 : 0;
-  static constexpr int kSmemBytes = kOffPo + 4 * 2 * NC * G * D + kAlignPad;
+  static constexpr int kSmemBytes = kOffPl + 4 * 2 * NC * G + kAlignPad;
+  static_assert(G * D * 4 <= kBlockBytes, "a warp's o rows must fit its K block area");
   static_assert(!M || (kBlockBytes % 1024 == 0 && sizeof(T) == 2), "swizzled blocks");
   static_assert(!(M && R), "the tensor-core consumer has no RoPE form");
 };
@@ -782,7 +784,6 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
   RopeLaneCs<D> kcs;  // RoPE only: this lane's (cos, sin) pairs of the current item
   float* const pm_buf = reinterpret_cast<float*>(smem + PC::kOffPm);
   float* const pl_buf = reinterpret_cast<float*>(smem + PC::kOffPl);
-  float* const po_buf = reinterpret_cast<float*>(smem + PC::kOffPo);
   int parity = 0;  // which partial buffer this item's end uses
   const int c = lane & 7, tg = lane >> 3;
   const int ctid = threadIdx.x;  // 0 .. NC*32-1
@@ -915,17 +916,24 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
       }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[slot]);
     ++st;
-    if (!(h.flags & kLast)) continue;
+    if (!(h.flags & kLast)) {
+      if (lane == 0) mbar_arrive(&empty[slot]);
+      continue;
+    }
 
-    // ---- end of the item: combine the warps' (m, l, o).  The buffers
-    // alternate between items, so one barrier per item suffices: a warp can
-    // only come back to this buffer after every warp has passed the next
-    // item's barrier, i.e. finished reading it here.
+    // ---- end of the item: combine the warps' (m, l, o).  (m, l) alternate
+    // between two buffers by item, so one barrier per item suffices: a warp
+    // can only come back to a buffer after every warp has passed the next
+    // item's barrier, i.e. finished reading it here.  Warp w's o rows sit in
+    // its K block area of this (last) stage, [G][D] fp32, and the stage is
+    // released once the combine has read them.
     float* const pm = pm_buf + parity * NC * G;
     float* const pl = pl_buf + parity * NC * G;
-    float* const po = po_buf + parity * NC * G * D;
+    unsigned char* const last_stage = smem + PC::kOffKV + slot * PC::kStageBytes;
+    auto po_of = [&](int w) -> float* {
+      return reinterpret_cast<float*>(last_stage + w * PC::kBlockBytes);
+    };
     parity ^= 1;
     if constexpr (kMma) {
       // lane partial sums over the 8 key rows; slots >= G are padding
@@ -941,8 +949,8 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
         if (g < G) {
 #pragma unroll
           for (int i = 0; i < (kMma ? D / 16 : 1); ++i) {
-            po[(warp * G + g) * D + 16 * i + r] = to[i][j];
-            po[(warp * G + g) * D + 16 * i + r + 8] = to[i][2 + j];
+            po_of(warp)[g * D + 16 * i + r] = to[i][j];
+            po_of(warp)[g * D + 16 * i + r + 8] = to[i][2 + j];
           }
           if (r == 0) {
             pm[warp * G + g] = tm[j];
@@ -968,13 +976,14 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
         for (int i = 0; i < C::kPPL; ++i)
 #pragma unroll
           for (int e = 0; e < C::kChunk; ++e)
-            po[(warp * G + g) * D + (c + 8 * i) * C::kChunk + e] = o[g][i * C::kChunk + e];
+            po_of(warp)[g * D + (c + 8 * i) * C::kChunk + e] = o[g][i * C::kChunk + e];
         if (c == 0) {
           pm[warp * G + g] = m[g];
           pl[warp * G + g] = l[g];
         }
       }
     }
+    fence_proxy_async_smem();  // o rows written into a stage that copies refill later
     if (!consumer_sync(sync, sync_phase, lane)) {
       fail();
       return;
@@ -992,7 +1001,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
         if (lw > 0.f) {
           const float wt = exp2f(pm[w * G + g] - M);
           L = fmaf(wt, lw, L);
-          O = fmaf(wt, po[(w * G + g) * D + e], O);
+          O = fmaf(wt, po_of(w)[g * D + e], O);
         }
       }
       const int hq = h.kvh * G + g;
@@ -1008,6 +1017,8 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
         }
       }
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[slot]);  // the item's last stage, now read
 #ifdef PHOTON_PROBE
     if (ctid == 0) PROBE_SET(9 + 2 * items_seen, global_timer_ns());
     ++items_seen;
