@@ -30,6 +30,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -325,11 +326,20 @@ ATTENTION_SOURCES = ("photon_common.cuh", "paged_decode.cuh", "paged_decode_f16.
                      "paged_decode_bf16.cu", "paged_decode_f32.cu")
 
 
+def _code_only(text: str) -> str:
+    """A source file without its comments and blank lines: edits to comments
+    leave the hash (and the recorded counters) valid."""
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    lines = (re.sub(r"//.*$", "", ln).rstrip() for ln in text.splitlines())
+    return "\n".join(ln for ln in lines if ln.strip())
+
+
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_kv_attention_photon_gb300", "csrc")
     for f in ATTENTION_SOURCES:
-        h.update(open(os.path.join(csrc, f), "rb").read())
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

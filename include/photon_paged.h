@@ -238,8 +238,7 @@ size_t photon_paged_multi_query_workspace_size(const photon_paged_shape_t* shape
                                                int32_t num_tokens, int32_t max_query_len);
 
 /* Test and tuning hook: which consumer the decode attention kernel runs
- * (photon_paged_decode, _step, _noalloc; the RoPE step always takes the
- * CUDA-core one).  0 (default) = by the group size: the tensor-core consumer
+ * (photon_paged_decode, _step, _step_rope, _noalloc).  0 (default) = by the group size: the tensor-core consumer
  * (mma.sync over tensor-map copies of the blocks) for fp16/bf16 storage and
  * 2 or more query heads per KV head, the CUDA-core consumer otherwise; 1 =
  * always the CUDA-core consumer; 2 = the tensor-core one wherever the storage

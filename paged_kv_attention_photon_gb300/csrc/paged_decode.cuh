@@ -28,17 +28,25 @@
 //      under a full HBM stream those fences and the serialised merges cost far
 //      more than this short kernel.)
 //
-// Consumer arithmetic.  Each consumer warp takes one 16-token block of a stage.
-// Eight lanes cover one token row with 16-byte shared-memory loads (a quarter
-// warp reads 128 contiguous bytes: no bank conflicts), four rows per load step,
-// four steps per block.  A lane keeps its slice of the G query rows of the KV
-// head's group (GQA) in registers, pre-multiplied by scale*log2(e), so every
-// loaded K/V element serves all G heads and exp is one exp2f.  Scores are
-// summed over the eight lanes of a row with three xor-shuffles.  The softmax is
-// the online form: per block the warp takes the block maximum, rescales its
-// running (l, o) by 2^(m_old - m_new) and accumulates 2^(s - m_new) and
-// 2^(s - m_new) * V.  At the end of an item the warps' states are combined
-// through shared memory by the same log-sum-exp rule.
+// Consumer arithmetic.  Each consumer warp takes one 16-token block of a
+// stage, in one of two forms (photon_debug_set_decode_consumer):
+//  * tensor cores (the default for fp16/bf16 storage and G >= 2 query heads
+//    per KV head): the producer brings the blocks as tensor-map copies with
+//    the 128-byte swizzle, and the warp computes S^T = K Q^T (16 keys x the G
+//    heads, padded to 8) and O^T += V^T P^T with mma.sync m16n8k16 from
+//    conflict-free ldmatrix reads; P is fed as its storage-type rounding plus
+//    the residual, so the weights keep ~2^-17 relative precision;
+//  * CUDA cores (fp32 storage, G = 1): eight lanes cover one token row with
+//    16-byte shared-memory loads (a quarter warp reads 128 contiguous bytes:
+//    no bank conflicts), four rows per load step, four steps per block.  A
+//    lane keeps its slice of the G query rows in registers, pre-multiplied by
+//    scale*log2(e), so every loaded K/V element serves all G heads; scores are
+//    summed over the eight lanes of a row with three xor-shuffles.
+// Either way the softmax is the online form in the log2 domain: per block the
+// warp takes the block maximum, rescales its running (l, o) by
+// 2^(m_old - m_new) and accumulates 2^(s - m_new) and 2^(s - m_new) * V.  At
+// the end of an item the warps' states are combined through shared memory by
+// the same log-sum-exp rule.
 #pragma once
 
 #include <float.h>
@@ -118,7 +126,6 @@ struct PersistCfg {
   static constexpr int kSmemBytes = kOffPl + 4 * 2 * NC * G + kAlignPad;
   static_assert(G * D * 4 <= kBlockBytes, "a warp's o rows must fit its K block area");
   static_assert(!M || (kBlockBytes % 1024 == 0 && sizeof(T) == 2), "swizzled blocks");
-  static_assert(!(M && R), "the tensor-core consumer has no RoPE form");
 };
 
 // ------------------------------------------------------------------ consumer math
@@ -223,11 +230,14 @@ __device__ __forceinline__ uint32_t blk_chunk(int row, int chunk) {
 // its rounding residual, two products, so the weights enter the sum with
 // about 2^-17 relative error instead of one storage-type rounding; the sums l
 // take the fp32 weights.  Scores are the fp32 products times qscale.
+// kQLo: q is an fp32 value (rotated by RoPE) given as bq + bql, its rounding
+// to the storage type and the residual, so S^T takes two products per step.
 // Rows >= n_valid: their scores are set to -inf and their V rows must be
 // zero (0 * NaN would otherwise reach the accumulators).
-template <typename T, int D>
+template <typename T, int D, bool kQLo>
 __device__ __forceinline__ void attend_block_mma(uint32_t kblk, uint32_t vblk, int n_valid,
                                                  float qscale, const uint32_t (&bq)[D / 16][2],
+                                                 const uint32_t (&bql)[D / 16][2],
                                                  float (&m)[2], float (&l)[2],
                                                  float (&o)[D / 16][4], int lane) {
   const int r = lane >> 2;
@@ -241,6 +251,7 @@ __device__ __forceinline__ void attend_block_mma(uint32_t kblk, uint32_t vblk, i
       uint32_t a[4];
       ldsm_x4(kblk + blk_chunk(krow, 2 * kk + khi), a[0], a[1], a[2], a[3]);
       Mma<T>::run(s, a, bq[kk][0], bq[kk][1]);
+      if constexpr (kQLo) Mma<T>::run(s, a, bql[kk][0], bql[kk][1]);
     }
   }
   const bool v0 = r < n_valid, v1 = r + 8 < n_valid;
@@ -780,6 +791,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
   // tensor-core consumer: Q^T operand fragments, (m, l) of slots 2(l%4) and
   // 2(l%4)+1, O^T accumulators
   uint32_t tq[kMma ? D / 16 : 1][2];
+  uint32_t tql[kMma && kRope ? D / 16 : 1][2];  // RoPE: residual of the rotated q rows
   float tm[2], tl[2], to[kMma ? D / 16 : 1][4];
   RopeLaneCs<D> kcs;  // RoPE only: this lane's (cos, sin) pairs of the current item
   float* const pm_buf = reinterpret_cast<float*>(smem + PC::kOffPm);
@@ -806,15 +818,58 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
       return;
     }
     if (kMma && (h.flags & kFirst)) {
-      const uint32_t* q32 = reinterpret_cast<const uint32_t*>(smem + PC::kOffQ + slot * PC::kQStride);
+      const unsigned char* qarea = smem + PC::kOffQ + slot * PC::kQStride;
+      const uint32_t* q32 = reinterpret_cast<const uint32_t*>(qarea);
       const int slot_g = lane >> 2, t2 = 2 * (lane & 3);
+      if constexpr (kRope && kMma) {
+        // q rows turned by the token's position in fp32, then split into
+        // their storage-type rounding and its residual
+        const float2* cs_row = reinterpret_cast<const float2*>(qarea + PC::kQBytes);
+        const bool in_table = h.pos >= 0 && h.pos < a.rope_max_pos;
+        if (!in_table && ctid == 0) raise_error(a.err, kErrPosition);
+        const T* qrow = reinterpret_cast<const T*>(qarea) + (slot_g < G ? slot_g : 0) * D;
+        auto turned = [&](int e) -> float {
+          const float x = Elem<T>::to_f32(qrow[e]);
+          if (!in_table) return x;
+          constexpr int kHalf = D / 2;
+          const float2 w = cs_row[e < kHalf ? e : e - kHalf];
+          const float partner = Elem<T>::to_f32(qrow[e < kHalf ? e + kHalf : e - kHalf]);
+          return e < kHalf ? x * w.x - partner * w.y : x * w.x + partner * w.y;
+        };
+        auto split = [&](int e, uint32_t& hi, uint32_t& lo) {
+          const float x0 = turned(e), x1 = turned(e + 1);
+          hi = Mma<T>::pack(x0, x1);
+          const float2 r = Mma<T>::unpack(hi);
+          lo = Mma<T>::pack(x0 - r.x, x1 - r.y);
+        };
 #pragma unroll
-      for (int kk = 0; kk < (kMma ? D / 16 : 1); ++kk) {
-        tq[kk][0] = slot_g < G ? q32[(slot_g * D + 16 * kk + t2) / 2] : 0u;
-        tq[kk][1] = slot_g < G ? q32[(slot_g * D + 16 * kk + t2 + 8) / 2] : 0u;
+        for (int kk = 0; kk < (kMma ? D / 16 : 1); ++kk) {
+          uint32_t h0 = 0u, l0 = 0u, h1 = 0u, l1 = 0u;
+          if (slot_g < G) {
+            split(16 * kk + t2, h0, l0);
+            split(16 * kk + t2 + 8, h1, l1);
+          }
+          tq[kk][0] = h0;
+          tq[kk][1] = h1;
+          tql[kk][0] = l0;
+          tql[kk][1] = l1;
+        }
+        if (in_table) {
+#pragma unroll
+          for (int i = 0; i < (D / 2 + 31) / 32; ++i)
+            if (lane + 32 * i < D / 2) kcs.w[i] = cs_row[lane + 32 * i];
+        }
+      } else {
+#pragma unroll
+        for (int kk = 0; kk < (kMma ? D / 16 : 1); ++kk) {
+          tq[kk][0] = slot_g < G ? q32[(slot_g * D + 16 * kk + t2) / 2] : 0u;
+          tq[kk][1] = slot_g < G ? q32[(slot_g * D + 16 * kk + t2 + 8) / 2] : 0u;
+        }
+      }
+#pragma unroll
+      for (int kk = 0; kk < (kMma ? D / 16 : 1); ++kk)
 #pragma unroll
         for (int j = 0; j < 4; ++j) to[kk][j] = 0.f;
-      }
       tm[0] = tm[1] = -INFINITY;
       tl[0] = tl[1] = 0.f;
     } else if (h.flags & kFirst) {
@@ -860,7 +915,12 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
         // fused step: the new token's rows came beside the stage; put them in
         // row new_row of the blocks (the box brought that slot's stale row)
         // and store them to their cache slot
-        const unsigned char* side = smem + PC::kOffSide + slot * PC::kSideBytes;
+        unsigned char* side = smem + PC::kOffSide + slot * PC::kSideBytes;
+        if constexpr (kRope) {
+          // with RoPE the new K row turns by its position first
+          rope_row<T, D>(reinterpret_cast<T*>(side), kcs, a.rope_max_pos, h.pos, lane);
+          __syncwarp();
+        }
         const size_t dst = (((size_t)h.new_phys * a.Hkv + h.kvh) * kBlockSize + h.new_row) * D;
         for (int i = lane; i < 2 * kRowChunks; i += 32) {
           const bool is_v = i >= kRowChunks;
@@ -883,9 +943,14 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
         fence_proxy_async_smem();  // the stage is refilled by tensor copies later
         __syncwarp();
       }
-      if constexpr (kMma)
-        attend_block_mma<T, D>(smem_addr(kb), smem_addr(vb), n_valid, a.qscale, tq, tm, tl, to,
-                               lane);
+      if constexpr (kMma) {
+        if constexpr (kRope)
+          attend_block_mma<T, D, true>(smem_addr(kb), smem_addr(vb), n_valid, a.qscale, tq, tql,
+                                       tm, tl, to, lane);
+        else
+          attend_block_mma<T, D, false>(smem_addr(kb), smem_addr(vb), n_valid, a.qscale, tq, tq,
+                                        tm, tl, to, lane);
+      }
     } else if (warp < h.nblk && ((h.flags >> (8 + warp)) & 1)) {
       const T* stage = reinterpret_cast<const T*>(smem + PC::kOffKV + slot * PC::kStageBytes);
       const int n_valid = min(kBlockSize, h.tok_end - (h.blk0 + warp) * kBlockSize);
@@ -1213,7 +1278,7 @@ cudaError_t launch_decode_impl(const DecodeArgs& a0, cudaStream_t stream) {
   bool mma = false;
   if constexpr (sizeof(T) == 2) {
     const int choice = g_decode_consumer.load(std::memory_order_relaxed);  // 0: by group size, 1: CUDA cores, 2: tensor cores
-    mma = !rope && (choice == 2 || (choice == 0 && G >= PHOTON_MMA_MIN_G)) &&
+    mma = (choice == 2 || (choice == 0 && G >= PHOTON_MMA_MIN_G)) &&
           (int64_t)a.NB * a.Hkv * kBlockSize <= INT32_MAX;
     const int dt = std::is_same<T, __half>::value ? 1 : 2;
     if (mma && (make_pool_map(&tk, a.k_cache, dt, a.NB, a.Hkv, D) != cudaSuccess ||
@@ -1223,13 +1288,14 @@ cudaError_t launch_decode_impl(const DecodeArgs& a0, cudaStream_t stream) {
 
   if (a.ev_start) cudaEventRecord(a.ev_start, stream);
   cudaError_t err;
-  if (rope) {
-    err = launch_attention<T, D, G, NC, S, true, false>(a, tk, tv, stream);
-  } else if (mma) {
+  if (mma) {
     if constexpr (sizeof(T) == 2)
-      err = launch_attention<T, D, G, NC, S, false, true>(a, tk, tv, stream);
+      err = rope ? launch_attention<T, D, G, NC, S, true, true>(a, tk, tv, stream)
+                 : launch_attention<T, D, G, NC, S, false, true>(a, tk, tv, stream);
     else
       err = cudaErrorInvalidValue;
+  } else if (rope) {
+    err = launch_attention<T, D, G, NC, S, true, false>(a, tk, tv, stream);
   } else {
     err = launch_attention<T, D, G, NC, S, false, false>(a, tk, tv, stream);
   }

@@ -25,3 +25,14 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture(params=[1, 2], ids=["cuda_cores", "tensor_cores"])
+def consumer(request):
+    """Runs a decode test on each attention consumer of the library: 1 = the
+    CUDA-core one, 2 = the tensor-core one (16-bit storage; f32 stays on CUDA
+    cores).  Restores the default selection afterwards."""
+    import paged_kv_attention_photon_gb300 as P
+    P.photon_debug_set_decode_consumer(request.param)
+    yield request.param
+    P.photon_debug_set_decode_consumer(0)

@@ -36,13 +36,6 @@ def _lib():
     assert st == 0
 
 
-@pytest.fixture(params=[1, 2], ids=["cuda_cores", "tensor_cores"])
-def consumer(request):
-    P.photon_debug_set_decode_consumer(request.param)
-    yield request.param
-    P.photon_debug_set_decode_consumer(0)
-
-
 _ORACLE_CACHE = {}
 
 

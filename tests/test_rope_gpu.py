@@ -11,6 +11,8 @@
   every other byte of the pool unchanged, bit for bit;
 * a position beyond the table: flagged with device error bit 16, that
   sequence handled unrotated, the others rotated.
+
+Each step test runs on both attention consumers (CUDA cores, tensor cores).
 """
 import os
 
@@ -93,6 +95,15 @@ CASES = {
 }
 
 
+_ORACLE = {}
+
+
+def _rope_oracle(key, wl: W.Workload, base: float):
+    if key not in _ORACLE:
+        _ORACLE[key] = oracle.rope_step(wl, base, THREADS)
+    return _ORACLE[key]
+
+
 def _check_rows(dwl: DeviceWorkload, kc: np.ndarray, vc: np.ndarray, wl: W.Workload,
                 small_pool: bool) -> None:
     live = (wl.slot_mapping >= 0) & (wl.context_lens > 0)
@@ -113,9 +124,9 @@ def _check_rows(dwl: DeviceWorkload, kc: np.ndarray, vc: np.ndarray, wl: W.Workl
 
 @pytest.mark.parametrize("base", [1e4, 1e6])
 @pytest.mark.parametrize("name", sorted(CASES))
-def test_rope_step_matches_oracle(name, base):
+def test_rope_step_matches_oracle(name, base, consumer):
     wl = CASES[name]()
-    kc, vc, want = oracle.rope_step(wl, base, THREADS)
+    kc, vc, want = _rope_oracle((name, base), wl, base)
     d = DeviceWorkload(wl)
     max_pos = int(wl.context_lens.max()) + 1
     table = rope_table(base, max_pos, wl.head_dim)
@@ -127,11 +138,11 @@ def test_rope_step_matches_oracle(name, base):
     _check_rows(d, kc, vc, wl, small_pool=True)
 
 
-def test_rope_step_qwen_b64_full_size():
+def test_rope_step_qwen_b64_full_size(consumer):
     """The benchmark's batch-64 workload (contexts up to 8192, 40 000-block
     pool) with a Qwen-style base of 10^6, every output row against the oracle."""
     wl = W.qwen_b64()
-    kc, vc, want = oracle.rope_step(wl, 1e6, THREADS)
+    kc, vc, want = _rope_oracle(("qwen_b64", 1e6), wl, 1e6)
     d = DeviceWorkload(wl)
     table = rope_table(1e6, 8192, wl.head_dim)
     d.step_rope(table, 8192)
@@ -142,7 +153,7 @@ def test_rope_step_qwen_b64_full_size():
     _check_rows(d, kc, vc, wl, small_pool=False)
 
 
-def test_position_beyond_the_table_is_flagged_and_left_unrotated():
+def test_position_beyond_the_table_is_flagged_and_left_unrotated(consumer):
     wl = W.random_small(87, batch=4, num_q_heads=8, num_kv_heads=2, head_dim=128, max_ctx=300,
                         dtype=W.DTYPE_F16, context_lens=[10, 100, 200, 300])
     max_pos = 150          # positions 199 and 299 are outside the table
