@@ -180,7 +180,19 @@ def multi_query_side(P, torch, stream, flush_l2, K, hbm_peak, only: str = "",
             return sum(a.elapsed_time(b) for a, b in ev) / K
 
         ms = timed(0)
-        ms_tc = timed(2) if with_tc else ms
+        g = p.num_q_heads // p.num_kv_heads
+        default = ("decode kernel, few-token mode" if mq.max_query_len * g <= 8 else
+                   "tcgen05" if nws == 0 else "warp-level mma.sync with key split")
+        per_kernel = {}
+        if with_tc:
+            for which, key in ((1, "warp_level_mma_sync"), (2, "tcgen05"),
+                               (3, "decode_few_token")):
+                if which == 3 and mq.max_query_len * g > 8:
+                    continue
+                t = timed(which)
+                per_kernel[key] = {"ms_per_call": round(t, 5),
+                                   "TFLOPs": round(mq.flops() / (t / 1e3) / 1e12, 2),
+                                   "kv_GBps": round(mq.kv_bytes() / (t / 1e3) / 1e9, 1)}
         gbs = mq.kv_bytes() / (ms / 1e3) / 1e9
         tfs = mq.flops() / (ms / 1e3) / 1e12
         achieved, peak, unit = (gbs, hbm_peak, "GB/s") if bound == "hbm" else \
@@ -192,11 +204,8 @@ def multi_query_side(P, torch, stream, flush_l2, K, hbm_peak, only: str = "",
                                   "frac": round(achieved / peak, 4),
                                   "peak_source": "measured" if bound == "hbm" else tkind},
                      "algorithmic_bytes": mq.kv_bytes(), "flops": mq.flops(),
-                     "split_kv_workspace_bytes": int(nws),
-                     "tcgen05_kernel": {"ms_per_call": round(ms_tc, 5),
-                                        "TFLOPs": round(mq.flops() / (ms_tc / 1e3) / 1e12, 2),
-                                        "kv_GBps": round(mq.kv_bytes() / (ms_tc / 1e3) / 1e9,
-                                                         1)}}
+                     "workspace_bytes": int(nws), "kernel": default,
+                     "per_kernel": per_kernel}
         del q, kc, vc, bt, cl, qs, out, ws
     return res
 

@@ -247,13 +247,17 @@ size_t photon_paged_multi_query_workspace_size(const photon_paged_shape_t* shape
 photon_status_t photon_debug_set_decode_consumer(int32_t which);
 
 /* Test and tuning hook: which kernel photon_paged_multi_query runs.
- * 0 (default) = chosen by the plan: the tcgen05/TMEM kernel (256-row
- * tiles, no key split) when the query tiles fill the device without a split,
- * the warp-level mma.sync kernel with its key split otherwise; 1 = always the
- * warp-level kernel (with the plan's split); 2 = always the tcgen05 kernel
- * (no split, workspace unused).  Results
- * agree within the documented tolerance, not bit for bit.  Process-wide;
- * PHOTON_ERR_INVALID_ARG for another value. */
+ * 0 (default) = chosen by the plan: when max_query_len x G <= 8 (a few draft
+ * tokens per sequence), the decode attention kernel in its few-token mode
+ * (every (token, head) pair of a sequence's KV head is one of its 8 query
+ * slots, with its own causal limit; decode partitions and merge); otherwise
+ * the tcgen05/TMEM kernel (256-row tiles, no key split) when the query tiles
+ * fill the device without a split, the warp-level mma.sync kernel with its
+ * key split when they do not; 1 = always the warp-level kernel (with the
+ * plan's split); 2 = always the tcgen05 kernel (no split, workspace unused);
+ * 3 = the few-token mode where max_query_len x G <= 8, the plan elsewhere.
+ * Results agree within the documented tolerance, not bit for bit.
+ * Process-wide; PHOTON_ERR_INVALID_ARG for another value. */
 photon_status_t photon_debug_set_multi_query_kernel(int32_t which);
 
 /* Failure-detection self-test: launches one thread that waits on a barrier

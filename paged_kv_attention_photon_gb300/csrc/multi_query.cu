@@ -306,18 +306,25 @@ __global__ void __launch_bounds__(MqCfg<T, D>::kThreads, 2)
       const int kb = it.part_idx * a.part;
       const int ke = min(kb + a.part, kend);
       const int nchunks = (ke - kb + kMqKeys - 1) / kMqKeys;
-      // the partition's block ids, read once (lane j: blocks j, j + 32, ...)
+      // the partition's block ids, a window of 256 at a time (lane j: blocks
+      // w + j, w + j + 32, ...); one window covers a 4096-key partition, a
+      // longer (unsplit) one reloads it every 64 chunks
       const int32_t* table = a.block_tables + (size_t)it.b * a.MBS + kb / kBlockSize;
       const int nblk = (ke - kb + kBlockSize - 1) / kBlockSize;
-      constexpr int kTblPerLane = 4096 / kBlockSize / 32;   // partitions of up to 4096 keys
+      constexpr int kTblPerLane = 4096 / kBlockSize / 32;
+      constexpr int kWindow = kTblPerLane * 32;              // blocks per window
       int tbl[kTblPerLane];
+      auto load_window = [&](int w) {
 #pragma unroll
-      for (int k = 0; k < kTblPerLane; ++k) {
-        const int j = k * 32 + lane;
-        tbl[k] = j < nblk ? __ldg(table + j) : -1;
-      }
+        for (int k = 0; k < kTblPerLane; ++k) {
+          const int j = w + k * 32 + lane;
+          tbl[k] = j < nblk ? __ldg(table + j) : -1;
+        }
+      };
+      load_window(0);
       bool ok = true;
       for (int c = 0; c < nchunks; ++c, ++g) {
+        if (c > 0 && (4 * c) % kWindow == 0) load_window(4 * c);
         const int st = g % S;
         if (g >= S) {   // the 4 compute warps are done with the stage's previous chunk
           ok = __shfl_sync(0xffffffffu, mbar_wait_bounded(&empty[st], ((g / S) - 1) & 1) ? 1 : 0,
@@ -328,11 +335,12 @@ __global__ void __launch_bounds__(MqCfg<T, D>::kThreads, 2)
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int j = c * 4 + i;   // block of the partition
+          const int jw = j % kWindow;  // its place in the current window
           int v = -1;
 #pragma unroll
           for (int k = 0; k < kTblPerLane; ++k) {
-            const int t = __shfl_sync(0xffffffffu, tbl[k], j & 31);
-            if ((j >> 5) == k) v = t;
+            const int t = __shfl_sync(0xffffffffu, tbl[k], jw & 31);
+            if ((jw >> 5) == k) v = t;
           }
           phys[i] = j < nblk ? v : -2;   // -2: past the partition (nothing to load)
         }

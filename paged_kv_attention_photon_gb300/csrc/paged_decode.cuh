@@ -81,7 +81,8 @@ struct StageHdr {
   // fused step: the stage block (new_warp) whose row new_row is this
   // sequence's new token, to be stored at physical block new_phys; -1 if none
   int new_warp, new_phys, new_row;
-  int pos;             // the sequence's new-token position, ctx - 1 (RoPE angle)
+  int pos;             // the sequence's new-token position, ctx - 1 (RoPE angle, causal limit)
+  int q0, nq;          // query rows of the item's sequence (decode: b and 1)
 };
 enum : int { kFirst = 1, kLast = 2, kDone = 4 };
 
@@ -94,13 +95,16 @@ constexpr int kMaxRuns = 10;
 // copies: every block starts on a 1024-byte swizzle atom (the dynamic
 // shared-memory base is aligned up at run time, hence kAlignPad), and the
 // fused step's new K/V row lands in a side slot of its stage.
-template <typename T, int D, int G, int NC, int S, bool R = false, bool M = false>
+// X: few-token multi-query mode (tensor-core consumer only): up to 8 query
+// slots (token, head) per item instead of the G heads of one token.
+template <typename T, int D, int G, int NC, int S, bool R = false, bool M = false, bool X = false>
 struct PersistCfg {
   using C = DecodeCfg<T, D, G>;
   static constexpr int kThreads = (NC + 1) * 32;
   static constexpr int kBlockElems = kBlockSize * D;
   static constexpr int kBlockBytes = kBlockElems * (int)sizeof(T);
-  static constexpr int kQBytes = G * D * (int)sizeof(T);
+  static constexpr int kSlots = X ? 8 : G;                      // query rows per item
+  static constexpr int kQBytes = kSlots * D * (int)sizeof(T);
   // with RoPE the item's (cos, sin) row, D/2 float pairs, follows its q rows
   static constexpr int kCsBytes = R ? 4 * D : 0;
   static constexpr int kQStride = (kQBytes + kCsBytes + 127) / 128 * 128;
@@ -120,11 +124,12 @@ struct PersistCfg {
   // Per-warp (m, l) at an item's end, double-buffered by item parity.  The
   // warps' o rows (G x D fp32 each) go to their own K block areas of the
   // item's last stage, which is released only after the combine.
-  static constexpr int kOffPm = kOffSide + kSideBytes * S;      // float[2][NC][G]
-  static constexpr int kOffPl = kOffPm + 4 * 2 * NC * G;        // float[2][NC][G]
+  static constexpr int kOffPm = kOffSide + kSideBytes * S;      // float[2][NC][kSlots]
+  static constexpr int kOffPl = kOffPm + 4 * 2 * NC * kSlots;   // float[2][NC][kSlots]
   static constexpr int kAlignPad = M ? 1024 : 0;
-  static constexpr int kSmemBytes = kOffPl + 4 * 2 * NC * G + kAlignPad;
-  static_assert(G * D * 4 <= kBlockBytes, "a warp's o rows must fit its K block area");
+  static constexpr int kSmemBytes = kOffPl + 4 * 2 * NC * kSlots + kAlignPad;
+  static_assert(kSlots * D * 4 <= kBlockBytes, "a warp's o rows must fit its K block area");
+  static_assert(!X || (M && !R), "the few-token mode runs on the tensor-core consumer, no RoPE");
   static_assert(!M || (kBlockBytes % 1024 == 0 && sizeof(T) == 2), "swizzled blocks");
 };
 
@@ -234,12 +239,17 @@ __device__ __forceinline__ uint32_t blk_chunk(int row, int chunk) {
 // to the storage type and the residual, so S^T takes two products per step.
 // Rows >= n_valid: their scores are set to -inf and their V rows must be
 // zero (0 * NaN would otherwise reach the accumulators).
-template <typename T, int D, bool kQLo>
+// kCausal (few-token multi-query mode): the lane's two slots see keys up to
+// positions lim[0], lim[1] (key0 = position of the block's row 0); a slot can
+// then have no key in a block, or in a whole item, so the max and rescale
+// steps guard against -inf - -inf.
+template <typename T, int D, bool kQLo, bool kCausal>
 __device__ __forceinline__ void attend_block_mma(uint32_t kblk, uint32_t vblk, int n_valid,
                                                  float qscale, const uint32_t (&bq)[D / 16][2],
                                                  const uint32_t (&bql)[D / 16][2],
                                                  float (&m)[2], float (&l)[2],
-                                                 float (&o)[D / 16][4], int lane) {
+                                                 float (&o)[D / 16][4], int lane, int key0,
+                                                 const int (&lim)[2]) {
   const int r = lane >> 2;
   float s[4] = {0.f, 0.f, 0.f, 0.f};
   {
@@ -255,20 +265,31 @@ __device__ __forceinline__ void attend_block_mma(uint32_t kblk, uint32_t vblk, i
     }
   }
   const bool v0 = r < n_valid, v1 = r + 8 < n_valid;
-  const float x0 = v0 ? s[0] * qscale : -INFINITY;   // key r,     slot 2t
-  const float x1 = v0 ? s[1] * qscale : -INFINITY;   // key r,     slot 2t + 1
-  const float x2 = v1 ? s[2] * qscale : -INFINITY;   // key r + 8, slot 2t
-  const float x3 = v1 ? s[3] * qscale : -INFINITY;   // key r + 8, slot 2t + 1
+  bool ok[4] = {v0, v0, v1, v1};
+  if constexpr (kCausal) {
+    ok[0] = ok[0] && key0 + r <= lim[0];
+    ok[1] = ok[1] && key0 + r <= lim[1];
+    ok[2] = ok[2] && key0 + r + 8 <= lim[0];
+    ok[3] = ok[3] && key0 + r + 8 <= lim[1];
+  }
+  const float x0 = ok[0] ? s[0] * qscale : -INFINITY;   // key r,     slot 2t
+  const float x1 = ok[1] ? s[1] * qscale : -INFINITY;   // key r,     slot 2t + 1
+  const float x2 = ok[2] ? s[2] * qscale : -INFINITY;   // key r + 8, slot 2t
+  const float x3 = ok[3] ? s[3] * qscale : -INFINITY;   // key r + 8, slot 2t + 1
   float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
 #pragma unroll
   for (int off = 4; off < 32; off <<= 1) {
     mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
     mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
   }
-  // key 0 is always valid, so the block maxima are finite
+  // decode: key 0 is always valid, so the block maxima are finite
   const float n0 = fmaxf(m[0], mx0), n1 = fmaxf(m[1], mx1);
   if (__any_sync(0xffffffffu, n0 > m[0] || n1 > m[1])) {
-    const float c0 = softmax_exp2(m[0] - n0), c1 = softmax_exp2(m[1] - n1);
+    float c0 = softmax_exp2(m[0] - n0), c1 = softmax_exp2(m[1] - n1);
+    if constexpr (kCausal) {
+      c0 = n0 > m[0] ? c0 : 1.f;   // also covers m = n = -inf
+      c1 = n1 > m[1] ? c1 : 1.f;
+    }
     l[0] *= c0;
     l[1] *= c1;
 #pragma unroll
@@ -281,8 +302,11 @@ __device__ __forceinline__ void attend_block_mma(uint32_t kblk, uint32_t vblk, i
     m[0] = n0;
     m[1] = n1;
   }
-  const float p0 = softmax_exp2(x0 - m[0]), p1 = softmax_exp2(x1 - m[1]);
-  const float p2 = softmax_exp2(x2 - m[0]), p3 = softmax_exp2(x3 - m[1]);
+  // a slot with no key so far has m = -inf and only -inf scores: weights 0
+  const float mr0 = kCausal && m[0] == -INFINITY ? 0.f : m[0];
+  const float mr1 = kCausal && m[1] == -INFINITY ? 0.f : m[1];
+  const float p0 = softmax_exp2(x0 - mr0), p1 = softmax_exp2(x1 - mr1);
+  const float p2 = softmax_exp2(x2 - mr0), p3 = softmax_exp2(x3 - mr1);
   l[0] += p0 + p2;
   l[1] += p1 + p3;
   const uint32_t h01 = Mma<T>::pack(p0, p1), h23 = Mma<T>::pack(p2, p3);
@@ -413,11 +437,14 @@ static __device__ unsigned long long g_probe[kProbeCtas][kProbeSlots];
 // tensor-map copies (tmk, tmv: the pools as rows of D elements, boxes of 16
 // rows x 64 elements, 128-byte swizzle).  The other instantiations take the
 // maps but never read them.
-template <typename T, int D, int G, int NC, int S, bool kRope, bool kMma>
+// kMulti: the few-token multi-query mode (photon_paged_multi_query with
+// max_query_len * G <= 8): an item's query slots are the (token, head) pairs
+// of its sequence's n query tokens, each with its causal limit.
+template <typename T, int D, int G, int NC, int S, bool kRope, bool kMma, bool kMulti>
 __global__ void __launch_bounds__((NC + 1) * 32, 1)
     paged_decode_attention_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
                                   const __grid_constant__ CUtensorMap tmv) {
-  using PC = PersistCfg<T, D, G, NC, S, kRope, kMma>;
+  using PC = PersistCfg<T, D, G, NC, S, kRope, kMma, kMulti>;
   using C = DecodeCfg<T, D, G>;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   // swizzled tensor copies want their 1024-byte atoms aligned in the shared window
@@ -460,6 +487,14 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
   const int span = a.MBS * kBlockSize;
   auto ctx_of = [&](int b) -> int {
     const int c = b < a.B ? __ldg(a.context_lens + b) : 0;
+    if constexpr (kMulti) {
+      // sequences without query tokens, or whose rows or lengths the merge
+      // kernel rejects, get no items
+      if (b >= a.B) return 0;
+      const int q0 = __ldg(a.query_start + b), n = __ldg(a.query_start + b + 1) - q0;
+      if (n <= 0 || n > a.max_q || q0 < 0 || q0 > a.num_tokens - n || c < n || c > span) return 0;
+      return c;
+    }
     return (c < 0 || c > span) ? 0 : c;  // rejected lengths count as empty
   };
   auto fail = [&](void) {
@@ -584,7 +619,12 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
       it.p = run == 0 ? rel - excl : nfull;
       it.tok_end = run == 0 ? (it.p + 1) * a.part : ctxj;
       it.nparts = nfull + (ctxj % a.part != 0 ? 1 : 0);
-      if constexpr (kRope) it.ctx = ctxj;
+      if constexpr (kRope || kMulti) it.ctx = ctxj;
+      if constexpr (kMulti) {
+        // first used two items later: the loads stay off this path
+        it.q0 = __ldg(a.query_start + it.b);
+        it.nq = __ldg(a.query_start + it.b + 1) - it.q0;
+      }
       return true;
     };
     // Lane j holds the physical block of logical block (chunk*32 + j) of the item.
@@ -688,10 +728,13 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
           h.new_warp = new_lane;
           h.new_phys = new_lane >= 0 ? new_phys : -1;
           h.new_row = new_lane >= 0 ? new_rows - 1 : -1;
-          h.pos = kRope ? it0.ctx - 1 : 0;
+          h.pos = (kRope || kMulti) ? it0.ctx - 1 : 0;
+          h.q0 = kMulti ? it0.q0 : it0.b;
+          h.nq = kMulti ? it0.nq : 1;
           hdr[slot] = h;
           const bool cs_copy = kRope && first && h.pos >= 0 && h.pos < a.rope_max_pos;
-          mbar_arrive_expect_tx(&full[slot], (uint32_t)(bytes + (first ? PC::kQBytes : 0) +
+          const int qbytes = kMulti ? it0.nq * G * D * (int)sizeof(T) : PC::kQBytes;
+          mbar_arrive_expect_tx(&full[slot], (uint32_t)(bytes + (first ? qbytes : 0) +
                                                         (cs_copy ? PC::kCsBytes : 0)));
         }
         __syncwarp();
@@ -729,10 +772,17 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
                           static_cast<const T*>(a.v_new) + nsrc, rb, &full[slot]);
           }
         }
-        if (first && lane == 0)
+        if (kMulti) {
+          // token i's G q rows, one copy per token
+          if (first && lane < it0.nq)
+            bulk_copy_g2s(smem + PC::kOffQ + slot * PC::kQStride + lane * G * D * (int)sizeof(T),
+                          qbase + ((size_t)(it0.q0 + lane) * a.Hq + (size_t)kvh * G) * D,
+                          (uint32_t)(G * D * (int)sizeof(T)), &full[slot]);
+        } else if (first && lane == 0) {
           bulk_copy_g2s(smem + PC::kOffQ + slot * PC::kQStride,
                         qbase + ((size_t)it0.b * a.Hq + (size_t)kvh * G) * D, PC::kQBytes,
                         &full[slot]);
+        }
         if constexpr (kRope) {
           // the item's (cos, sin) row rides with its q rows
           const int pos = it0.ctx - 1;
@@ -793,6 +843,8 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
   uint32_t tq[kMma ? D / 16 : 1][2];
   uint32_t tql[kMma && kRope ? D / 16 : 1][2];  // RoPE: residual of the rotated q rows
   float tm[2], tl[2], to[kMma ? D / 16 : 1][4];
+  int tlim[2] = {0, 0};  // few-token mode: last key position each of the lane's slots sees
+  int nslots = G;        // query slots of the current item
   RopeLaneCs<D> kcs;  // RoPE only: this lane's (cos, sin) pairs of the current item
   float* const pm_buf = reinterpret_cast<float*>(smem + PC::kOffPm);
   float* const pl_buf = reinterpret_cast<float*>(smem + PC::kOffPl);
@@ -820,7 +872,17 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
     if (kMma && (h.flags & kFirst)) {
       const unsigned char* qarea = smem + PC::kOffQ + slot * PC::kQStride;
       const uint32_t* q32 = reinterpret_cast<const uint32_t*>(qarea);
-      const int slot_g = lane >> 2, t2 = 2 * (lane & 3);
+      const int t2 = 2 * (lane & 3);
+      // the lane's slot for the Q^T operand; decode: head g, few-token mode:
+      // (token slot / G, head slot % G), rows consecutive in shared memory
+      nslots = kMulti ? h.nq * G : G;
+      const int slot_g = (lane >> 2) < nslots ? (lane >> 2) : PC::kSlots;
+      if constexpr (kMulti) {
+        // token i sits at position ctx - nq + i = pos + 1 - nq + i
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+          tlim[j] = t2 + j < nslots ? h.pos + 1 - h.nq + (t2 + j) / G : -1;
+      }
       if constexpr (kRope && kMma) {
         // q rows turned by the token's position in fp32, then split into
         // their storage-type rounding and its residual
@@ -862,8 +924,8 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
       } else {
 #pragma unroll
         for (int kk = 0; kk < (kMma ? D / 16 : 1); ++kk) {
-          tq[kk][0] = slot_g < G ? q32[(slot_g * D + 16 * kk + t2) / 2] : 0u;
-          tq[kk][1] = slot_g < G ? q32[(slot_g * D + 16 * kk + t2 + 8) / 2] : 0u;
+          tq[kk][0] = slot_g < PC::kSlots ? q32[(slot_g * D + 16 * kk + t2) / 2] : 0u;
+          tq[kk][1] = slot_g < PC::kSlots ? q32[(slot_g * D + 16 * kk + t2 + 8) / 2] : 0u;
         }
       }
 #pragma unroll
@@ -944,12 +1006,13 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
         __syncwarp();
       }
       if constexpr (kMma) {
+        const int key0 = (h.blk0 + warp) * kBlockSize;
         if constexpr (kRope)
-          attend_block_mma<T, D, true>(smem_addr(kb), smem_addr(vb), n_valid, a.qscale, tq, tql,
-                                       tm, tl, to, lane);
+          attend_block_mma<T, D, true, false>(smem_addr(kb), smem_addr(vb), n_valid, a.qscale, tq,
+                                              tql, tm, tl, to, lane, key0, tlim);
         else
-          attend_block_mma<T, D, false>(smem_addr(kb), smem_addr(vb), n_valid, a.qscale, tq, tq,
-                                        tm, tl, to, lane);
+          attend_block_mma<T, D, false, kMulti>(smem_addr(kb), smem_addr(vb), n_valid, a.qscale,
+                                                tq, tq, tm, tl, to, lane, key0, tlim);
       }
     } else if (warp < h.nblk && ((h.flags >> (8 + warp)) & 1)) {
       const T* stage = reinterpret_cast<const T*>(smem + PC::kOffKV + slot * PC::kStageBytes);
@@ -991,10 +1054,11 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
     // between two buffers by item, so one barrier per item suffices: a warp
     // can only come back to a buffer after every warp has passed the next
     // item's barrier, i.e. finished reading it here.  Warp w's o rows sit in
-    // its K block area of this (last) stage, [G][D] fp32, and the stage is
+    // its K block area of this (last) stage, [slots][D] fp32, and the stage is
     // released once the combine has read them.
-    float* const pm = pm_buf + parity * NC * G;
-    float* const pl = pl_buf + parity * NC * G;
+    constexpr int kSl = PC::kSlots;
+    float* const pm = pm_buf + parity * NC * kSl;
+    float* const pl = pl_buf + parity * NC * kSl;
     unsigned char* const last_stage = smem + PC::kOffKV + slot * PC::kStageBytes;
     auto po_of = [&](int w) -> float* {
       return reinterpret_cast<float*>(last_stage + w * PC::kBlockBytes);
@@ -1010,16 +1074,16 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
       const int r = lane >> 2;
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
-        const int g = 2 * (lane & 3) + j;
-        if (g < G) {
+        const int g = 2 * (lane & 3) + j;   // the slot
+        if (g < nslots) {
 #pragma unroll
           for (int i = 0; i < (kMma ? D / 16 : 1); ++i) {
             po_of(warp)[g * D + 16 * i + r] = to[i][j];
             po_of(warp)[g * D + 16 * i + r + 8] = to[i][2 + j];
           }
           if (r == 0) {
-            pm[warp * G + g] = tm[j];
-            pl[warp * G + g] = tl[j];
+            pm[warp * kSl + g] = tm[j];
+            pl[warp * kSl + g] = tl[j];
           }
         }
       }
@@ -1043,8 +1107,8 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
           for (int e = 0; e < C::kChunk; ++e)
             po_of(warp)[g * D + (c + 8 * i) * C::kChunk + e] = o[g][i * C::kChunk + e];
         if (c == 0) {
-          pm[warp * G + g] = m[g];
-          pl[warp * G + g] = l[g];
+          pm[warp * kSl + g] = m[g];
+          pl[warp * kSl + g] = l[g];
         }
       }
     }
@@ -1053,29 +1117,45 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
       fail();
       return;
     }
-    for (int idx = ctid; idx < G * D; idx += NC * 32) {
-      const int g = idx / D, e = idx % D;
+    // four consecutive elements of one slot's row per thread and pass
+    for (int idx = ctid; idx < nslots * (D / 4); idx += NC * 32) {
+      const int g = idx / (D / 4), e = (idx % (D / 4)) * 4;   // slot (token g / G, head g % G)
       float M = -INFINITY;
 #pragma unroll
       for (int w = 0; w < NC; ++w)
-        if (pl[w * G + g] > 0.f) M = fmaxf(M, pm[w * G + g]);
-      float L = 0.f, O = 0.f;
+        if (pl[w * kSl + g] > 0.f) M = fmaxf(M, pm[w * kSl + g]);
+      float L = 0.f;
+      float4 O = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
       for (int w = 0; w < NC; ++w) {
-        const float lw = pl[w * G + g];
+        const float lw = pl[w * kSl + g];
         if (lw > 0.f) {
-          const float wt = exp2f(pm[w * G + g] - M);
+          const float wt = exp2f(pm[w * kSl + g] - M);
+          const float4 v = *reinterpret_cast<const float4*>(po_of(w) + g * D + e);
           L = fmaf(wt, lw, L);
-          O = fmaf(wt, po_of(w)[g * D + e], O);
+          O.x = fmaf(wt, v.x, O.x);
+          O.y = fmaf(wt, v.y, O.y);
+          O.z = fmaf(wt, v.z, O.z);
+          O.w = fmaf(wt, v.w, O.w);
         }
       }
-      const int hq = h.kvh * G + g;
+      const int hq = h.kvh * G + g % G;
+      const size_t qrow = kMulti ? (size_t)h.q0 + g / G : (size_t)h.b;   // row of q / out
       if (h.nparts == 1) {
-        T* out = static_cast<T*>(a.out) + ((size_t)h.b * a.Hq + hq) * D;
-        out[e] = Elem<T>::narrow(L > 0.f ? O / L : 0.f);
+        T* out = static_cast<T*>(a.out) + (qrow * a.Hq + hq) * D + e;
+        const float4 r = L > 0.f ? make_float4(O.x / L, O.y / L, O.z / L, O.w / L)
+                                 : make_float4(0.f, 0.f, 0.f, 0.f);
+        if constexpr (sizeof(T) == 2) {
+          uint2 u;
+          u.x = Mma<T>::pack(r.x, r.y);
+          u.y = Mma<T>::pack(r.z, r.w);
+          *reinterpret_cast<uint2*>(out) = u;
+        } else {
+          *reinterpret_cast<float4*>(out) = r;
+        }
       } else {
-        const size_t row = ((size_t)h.b * a.Hq + hq) * a.pmax + h.p;
-        a.ws_o[row * D + e] = O;
+        const size_t row = (qrow * a.Hq + hq) * a.pmax + h.p;
+        *reinterpret_cast<float4*>(a.ws_o + row * D + e) = O;
         if (e == 0) {
           a.ws_m[row] = M;
           a.ws_l[row] = L;
@@ -1092,8 +1172,9 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
 }
 
 // ------------------------------------------------------------------ merge kernel
-// One warp per (sequence, q head).  Empty (or rejected) contexts get a zero
-// row; sequences with two or more partitions get the merge:
+// One warp per (sequence, q head) -- per (sequence, q head, query token) in
+// the few-token mode.  Empty (or rejected) contexts get a zero row;
+// sequences with two or more partitions get the merge:
 //   M = max_p m_p,  w_p = 2^(m_p - M) (0 for an empty partition),
 //   out = sum_p w_p o_p / sum_p w_p l_p.
 // Built for latency: a lane owns D/32 consecutive output elements, and the
@@ -1115,21 +1196,51 @@ template <typename T, int D>
 __global__ void __launch_bounds__(kMergeWarps * 32) paged_decode_merge_kernel(const DecodeArgs a) {
   constexpr int EPL = D / 32;
   // This kernel runs only after the attention kernel has passed its own wait
-  // for the kernel before it, so the context lengths (which the attention
-  // kernel does not write) can be read before waiting for the attention grid:
-  // one round trip off the merge's critical path.  Rows of empty or rejected
-  // contexts are not touched by the attention kernel either.
+  // for the kernel before it, so the context lengths and query starts (which
+  // the attention kernel does not write) can be read before waiting for the
+  // attention grid: one round trip off the merge's critical path.  Rows of
+  // empty or rejected sequences are not touched by the attention kernel
+  // either.
+  // item = (b * Hq + h) * max_q + i: sequence b, q head h, its query token
+  // i (decode: max_q = 1, one token)
+  const int mq = a.query_start ? a.max_q : 1;
   const int item = blockIdx.x * kMergeWarps + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  const int b = item < a.B * a.Hq ? item / a.Hq : 0;
-  const int ctx = item < a.B * a.Hq ? __ldg(a.context_lens + b) : 0;
-  T* out = static_cast<T*>(a.out) + (size_t)item * D + lane * EPL;
-  const bool zero_row = item < a.B * a.Hq && (ctx <= 0 || ctx > a.MBS * kBlockSize);
-  if (zero_row) {
-    // empty or rejected context: a zero row
-    if (ctx != 0 && lane == 0 && item % a.Hq == 0) raise_error(a.err, kErrContext);
+  const bool live = item < a.B * a.Hq * mq;
+  const int bh = item / mq, ti = item % mq;
+  const int b = live ? bh / a.Hq : 0, hq = live ? bh % a.Hq : 0;
+  const int ctx = live ? __ldg(a.context_lens + b) : 0;
+  const int span = a.MBS * kBlockSize;
+  // the sequence's output rows: decode, row b; few-token mode, rows q0 .. q0 + n - 1
+  int q0 = b, n = 1;
+  bool skip = !live;
+  if (a.query_start && live) {
+    q0 = __ldg(a.query_start + b);
+    n = __ldg(a.query_start + b + 1) - q0;
+    if (n < 0 || q0 < 0 || q0 > a.num_tokens - n) {
+      // rows outside q / out: flagged, nothing written
+      if (lane == 0 && hq == 0 && ti == 0) raise_error(a.err, kErrQuery);
+      skip = true;
+    } else if (n > a.max_q || ctx < n || ctx > span) {
+      // inconsistent lengths: flagged, the rows it may own zeroed
+      if (lane == 0 && hq == 0 && ti == 0)
+        raise_error(a.err, n > a.max_q ? kErrQuery : kErrContext);
+      if (ti < n) {
+        T* out = static_cast<T*>(a.out) + ((size_t)(q0 + ti) * a.Hq + hq) * D + lane * EPL;
+#pragma unroll
+        for (int e = 0; e < EPL; ++e) out[e] = Elem<T>::narrow(0.f);
+      }
+      skip = true;
+    } else if (ti >= n) {
+      skip = true;   // fewer tokens than max_q
+    }
+  } else if (live && (ctx <= 0 || ctx > span)) {
+    // decode: an empty or rejected context gives a zero row
+    if (ctx != 0 && lane == 0 && hq == 0) raise_error(a.err, kErrContext);
+    T* out = static_cast<T*>(a.out) + (size_t)item * D + lane * EPL;
 #pragma unroll
     for (int e = 0; e < EPL; ++e) out[e] = Elem<T>::narrow(0.f);
+    skip = true;
   }
   pdl_wait_primary();
   if (blockIdx.x == 0 && threadIdx.x == 0) {
@@ -1138,80 +1249,85 @@ __global__ void __launch_bounds__(kMergeWarps * 32) paged_decode_merge_kernel(co
     a.ws_ctrl[1] = 0ull;
     a.ws_ctrl[0] = kQueueReady;
   }
-  if (item >= a.B * a.Hq || zero_row) return;
+  if (skip) return;
   const int nparts = (ctx + a.part - 1) / a.part;
   if (nparts < 2) return;                             // the attention kernel wrote out
-  const size_t row0 = (size_t)item * a.pmax;          // item = b * Hq + h
-  const float* pm = a.ws_m + row0;
-  const float* pl = a.ws_l + row0;
-  const float* po = a.ws_o + row0 * D + lane * EPL;
 
-  float O[EPL];
+  {
+    const size_t orow = (size_t)(q0 + ti) * a.Hq + hq;   // row of out
+    const size_t row0 = orow * a.pmax;
+    T* out = static_cast<T*>(a.out) + orow * D + lane * EPL;
+    const float* pm = a.ws_m + row0;
+    const float* pl = a.ws_l + row0;
+    const float* po = a.ws_o + row0 * D + lane * EPL;
+
+    float O[EPL];
 #pragma unroll
-  for (int e = 0; e < EPL; ++e) O[e] = 0.f;
-  float M = -INFINITY, L = 0.f;
-  for (int p0 = 0; p0 < nparts; p0 += 32) {
-    const int n = min(32, nparts - p0);
-    float v[kMergeRows][EPL];
-#pragma unroll
-    for (int u = 0; u < kMergeRows; ++u)
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) v[u][e] = u < n ? po[(size_t)(p0 + u) * D + e] : 0.f;
-    const float lp = lane < n ? pl[p0 + lane] : 0.f;
-    const float mp = lane < n && lp > 0.f ? pm[p0 + lane] : -INFINITY;
-    // running max over the chunks; rescale what was accumulated so far
-    float mc = mp;
-#pragma unroll
-    for (int s = 16; s > 0; s >>= 1) mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, s));
-    const float Mn = fmaxf(M, mc);
-    if (Mn == -INFINITY) continue;                    // nothing in this chunk or before
-    const float scale_old = exp2f(M - Mn);            // 0 when M = -inf
-    const float w = lp > 0.f ? exp2f(mp - Mn) : 0.f;
-    float lw = w * lp;
-#pragma unroll
-    for (int s = 16; s > 0; s >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, s);
-    L = L * scale_old + lw;
-#pragma unroll
-    for (int e = 0; e < EPL; ++e) O[e] *= scale_old;
-#pragma unroll
-    for (int u = 0; u < kMergeRows; ++u) {
-      const float wu = __shfl_sync(0xffffffffu, w, u);
-#pragma unroll
-      for (int e = 0; e < EPL; ++e) O[e] = fmaf(wu, v[u][e], O[e]);
-    }
-#pragma unroll
-    for (int u0 = kMergeRows; u0 < 32; u0 += kMergeRows) {  // rest of the chunk, if any
-      if (u0 >= n) break;
+    for (int e = 0; e < EPL; ++e) O[e] = 0.f;
+    float M = -INFINITY, L = 0.f;
+    for (int p0 = 0; p0 < nparts; p0 += 32) {
+      const int np = min(32, nparts - p0);
+      float v[kMergeRows][EPL];
 #pragma unroll
       for (int u = 0; u < kMergeRows; ++u)
 #pragma unroll
-        for (int e = 0; e < EPL; ++e)
-          v[u][e] = u0 + u < n ? po[(size_t)(p0 + u0 + u) * D + e] : 0.f;
+        for (int e = 0; e < EPL; ++e) v[u][e] = u < np ? po[(size_t)(p0 + u) * D + e] : 0.f;
+      const float lp = lane < np ? pl[p0 + lane] : 0.f;
+      const float mp = lane < np && lp > 0.f ? pm[p0 + lane] : -INFINITY;
+      // running max over the chunks; rescale what was accumulated so far
+      float mc = mp;
+#pragma unroll
+      for (int s = 16; s > 0; s >>= 1) mc = fmaxf(mc, __shfl_xor_sync(0xffffffffu, mc, s));
+      const float Mn = fmaxf(M, mc);
+      if (Mn == -INFINITY) continue;                    // nothing in this chunk or before
+      const float scale_old = exp2f(M - Mn);            // 0 when M = -inf
+      const float w = lp > 0.f ? exp2f(mp - Mn) : 0.f;
+      float lw = w * lp;
+#pragma unroll
+      for (int s = 16; s > 0; s >>= 1) lw += __shfl_xor_sync(0xffffffffu, lw, s);
+      L = L * scale_old + lw;
+#pragma unroll
+      for (int e = 0; e < EPL; ++e) O[e] *= scale_old;
 #pragma unroll
       for (int u = 0; u < kMergeRows; ++u) {
-        const float wu = __shfl_sync(0xffffffffu, w, u0 + u);
+        const float wu = __shfl_sync(0xffffffffu, w, u);
 #pragma unroll
         for (int e = 0; e < EPL; ++e) O[e] = fmaf(wu, v[u][e], O[e]);
       }
-    }
-    M = Mn;
-  }
-  const float inv = L > 0.f ? 1.f / L : 0.f;
 #pragma unroll
-  for (int e = 0; e < EPL; ++e) out[e] = Elem<T>::narrow(O[e] * inv);
+      for (int u0 = kMergeRows; u0 < 32; u0 += kMergeRows) {  // rest of the chunk, if any
+        if (u0 >= np) break;
+#pragma unroll
+        for (int u = 0; u < kMergeRows; ++u)
+#pragma unroll
+          for (int e = 0; e < EPL; ++e)
+            v[u][e] = u0 + u < np ? po[(size_t)(p0 + u0 + u) * D + e] : 0.f;
+#pragma unroll
+        for (int u = 0; u < kMergeRows; ++u) {
+          const float wu = __shfl_sync(0xffffffffu, w, u0 + u);
+#pragma unroll
+          for (int e = 0; e < EPL; ++e) O[e] = fmaf(wu, v[u][e], O[e]);
+        }
+      }
+      M = Mn;
+    }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+    for (int e = 0; e < EPL; ++e) out[e] = Elem<T>::narrow(O[e] * inv);
+  }
 }
 
 // Resident CTAs per SM of an attention-kernel instantiation (queried once per
 // device, after raising its dynamic shared-memory limit).
-template <typename T, int D, int G, int NC, int S, bool kRope, bool kMma>
+template <typename T, int D, int G, int NC, int S, bool kRope, bool kMma, bool kMulti>
 int attention_ctas_per_sm() {
-  using PC = PersistCfg<T, D, G, NC, S, kRope, kMma>;
+  using PC = PersistCfg<T, D, G, NC, S, kRope, kMma, kMulti>;
   constexpr int kMaxDev = 64;
   static int cache[kMaxDev];  // 0 = not yet queried
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
   if (cache[dev] > 0) return cache[dev];
-  auto kern = paged_decode_attention_kernel<T, D, G, NC, S, kRope, kMma>;
+  auto kern = paged_decode_attention_kernel<T, D, G, NC, S, kRope, kMma, kMulti>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PC::kSmemBytes) !=
       cudaSuccess)
     return 0;
@@ -1251,13 +1367,13 @@ constexpr int stages_for(int nc) {
 #define PHOTON_MMA_MIN_G 2
 #endif
 
-template <typename T, int D, int G, int NC, int S, bool kRope, bool kMma>
+template <typename T, int D, int G, int NC, int S, bool kRope, bool kMma, bool kMulti = false>
 cudaError_t launch_attention(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
                              cudaStream_t stream) {
-  using PC = PersistCfg<T, D, G, NC, S, kRope, kMma>;
-  const int per_sm = attention_ctas_per_sm<T, D, G, NC, S, kRope, kMma>();
+  using PC = PersistCfg<T, D, G, NC, S, kRope, kMma, kMulti>;
+  const int per_sm = attention_ctas_per_sm<T, D, G, NC, S, kRope, kMma, kMulti>();
   if (per_sm <= 0) return cudaErrorInvalidConfiguration;
-  return launch_pdl(paged_decode_attention_kernel<T, D, G, NC, S, kRope, kMma>,
+  return launch_pdl(paged_decode_attention_kernel<T, D, G, NC, S, kRope, kMma, kMulti>,
                     dim3(per_sm * a.num_sms), dim3(PC::kThreads), PC::kSmemBytes, stream, a, tk,
                     tv);
 }
@@ -1272,14 +1388,19 @@ cudaError_t launch_decode_impl(const DecodeArgs& a0, cudaStream_t stream) {
       !a.ws_m || !a.ws_l || !a.ws_o || !a.ws_ctrl || !a.err)
     return cudaErrorInvalidValue;
   const bool rope = a.rope_cs != nullptr;
+  // few-token multi-query mode: tensor-core consumer only, at most 8 slots
+  const bool multi = a.query_start != nullptr;
+  if (multi && (sizeof(T) != 2 || rope || a.max_q < 1 || a.max_q * G > 8))
+    return cudaErrorInvalidValue;
   CUtensorMap tk, tv;
   memset(&tk, 0, sizeof(tk));
   memset(&tv, 0, sizeof(tv));
   bool mma = false;
   if constexpr (sizeof(T) == 2) {
     const int choice = g_decode_consumer.load(std::memory_order_relaxed);  // 0: by group size, 1: CUDA cores, 2: tensor cores
-    mma = (choice == 2 || (choice == 0 && G >= PHOTON_MMA_MIN_G)) &&
+    mma = (multi || choice == 2 || (choice == 0 && G >= PHOTON_MMA_MIN_G)) &&
           (int64_t)a.NB * a.Hkv * kBlockSize <= INT32_MAX;
+    if (multi && !mma) return cudaErrorInvalidValue;
     const int dt = std::is_same<T, __half>::value ? 1 : 2;
     if (mma && (make_pool_map(&tk, a.k_cache, dt, a.NB, a.Hkv, D) != cudaSuccess ||
                 make_pool_map(&tv, a.v_cache, dt, a.NB, a.Hkv, D) != cudaSuccess))
@@ -1290,8 +1411,9 @@ cudaError_t launch_decode_impl(const DecodeArgs& a0, cudaStream_t stream) {
   cudaError_t err;
   if (mma) {
     if constexpr (sizeof(T) == 2)
-      err = rope ? launch_attention<T, D, G, NC, S, true, true>(a, tk, tv, stream)
-                 : launch_attention<T, D, G, NC, S, false, true>(a, tk, tv, stream);
+      err = multi  ? launch_attention<T, D, G, NC, S, false, true, true>(a, tk, tv, stream)
+            : rope ? launch_attention<T, D, G, NC, S, true, true>(a, tk, tv, stream)
+                   : launch_attention<T, D, G, NC, S, false, true>(a, tk, tv, stream);
     else
       err = cudaErrorInvalidValue;
   } else if (rope) {
@@ -1300,7 +1422,7 @@ cudaError_t launch_decode_impl(const DecodeArgs& a0, cudaStream_t stream) {
     err = launch_attention<T, D, G, NC, S, false, false>(a, tk, tv, stream);
   }
   if (err != cudaSuccess) return err;
-  const int items = a.B * a.Hq;
+  const int items = a.B * a.Hq * (multi ? a.max_q : 1);
   err = launch_pdl(paged_decode_merge_kernel<T, D>, dim3((items + kMergeWarps - 1) / kMergeWarps),
                    dim3(kMergeWarps * 32), 0, stream, a);
   if (err != cudaSuccess) return err;

@@ -6,6 +6,7 @@
 // Result-style values, buffers are used in place without copies): every call
 // returns a status, nothing throws across the boundary, and the library never
 // allocates or copies the caller's data.
+#include <algorithm>
 #include <atomic>
 #include <climits>
 #include <cmath>
@@ -94,15 +95,17 @@ int max_partitions_of(const photon_paged_shape_t* s) {
   return (int)((span + part - 1) / part);
 }
 
-// Workspace: [queue control][m][l][o] (the last three per sequence, q head
-// and partition), each section 256-byte aligned.
+// Workspace: [queue control][m][l][o] (the last three per query row, q head
+// and partition; a decode has one query row per sequence, the few-token
+// multi-query path one per query token), each section 256-byte aligned.
 struct WorkspaceLayout {
   size_t off_ctrl, off_m, off_l, off_o, total;
 };
 
-WorkspaceLayout layout_of(const photon_paged_shape_t* s) {
+WorkspaceLayout layout_of(const photon_paged_shape_t* s, int64_t query_rows = -1) {
   WorkspaceLayout w{};
-  const size_t pairs = (size_t)s->num_seqs * (size_t)max_partitions_of(s);
+  if (query_rows < 0) query_rows = s->num_seqs;
+  const size_t pairs = (size_t)query_rows * (size_t)max_partitions_of(s);
   const size_t rows = pairs * s->num_q_heads;
   w.off_ctrl = 0;
   w.off_m = 256;
@@ -229,7 +232,9 @@ photon_status_t decode_common(const void* q, const void* k_cache, const void* v_
                               const photon_paged_shape_t* shape, photon_stream_t stream,
                               const void* k_new, const void* v_new,
                               const int64_t* slot_mapping, const void* rope_cos_sin,
-                              int32_t rope_max_positions) {
+                              int32_t rope_max_positions,
+                              const int32_t* query_start = nullptr, int32_t num_tokens = 0,
+                              int32_t max_query_len = 0) {
   photon_status_t st = check_shape(shape);
   if (st != PHOTON_OK) return st;
   if (!std::isfinite(scale)) return PHOTON_ERR_INVALID_ARG;
@@ -239,7 +244,7 @@ photon_status_t decode_common(const void* q, const void* k_cache, const void* v_
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(block_tables) ||
       !aligned16(context_lens) || !aligned16(out))
     return PHOTON_ERR_MISALIGNED;
-  const WorkspaceLayout wl = layout_of(shape);
+  const WorkspaceLayout wl = layout_of(shape, query_start ? (int64_t)num_tokens : -1);
   if (wl.total > 0) {
     if (!workspace || workspace_bytes < wl.total) return PHOTON_ERR_WORKSPACE;
     if (!aligned16(workspace)) return PHOTON_ERR_MISALIGNED;
@@ -279,8 +284,11 @@ photon_status_t decode_common(const void* q, const void* k_cache, const void* v_
   a.MBS = shape->max_blocks_per_seq;
   a.part = partition_of(shape);
   a.pmax = max_partitions_of(shape);
-  a.ev_start = g_ev_start.load(std::memory_order_acquire);
-  a.ev_stop = g_ev_stop.load(std::memory_order_acquire);
+  a.query_start = query_start;
+  a.num_tokens = num_tokens;
+  a.max_q = max_query_len;
+  a.ev_start = query_start ? nullptr : g_ev_start.load(std::memory_order_acquire);
+  a.ev_stop = query_start ? nullptr : g_ev_stop.load(std::memory_order_acquire);
   if (!a.ev_start || !a.ev_stop) a.ev_start = a.ev_stop = nullptr;
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -376,6 +384,14 @@ struct MqPlan {
 constexpr int kMqTileRows = 64;
 constexpr int kMqSplitBelow = 4 * 2 * 152;
 
+// Query batches whose every sequence fits the decode kernel's 8 query slots
+// per KV head (max_query_len x G <= 8: speculative verification with a few
+// draft tokens) can run as a decode over the same partitions: K/V streamed
+// once per (sequence, KV head) for all of its tokens.
+bool few_token(const photon_paged_shape_t* s, int32_t max_query_len) {
+  return (int64_t)max_query_len * (s->num_q_heads / s->num_kv_heads) <= 8;
+}
+
 MqPlan mq_plan(const photon_paged_shape_t* s, int32_t num_tokens, int32_t max_query_len) {
   MqPlan p{};
   const int64_t G = s->num_q_heads / s->num_kv_heads;
@@ -405,7 +421,10 @@ size_t photon_paged_multi_query_workspace_size(const photon_paged_shape_t* shape
   if (check_shape(shape) != PHOTON_OK || shape->dtype == PHOTON_F32 || num_tokens <= 0 ||
       max_query_len <= 0)
     return 0;
-  return mq_plan(shape, num_tokens, max_query_len).total;
+  size_t total = mq_plan(shape, num_tokens, max_query_len).total;
+  // enough for whichever kernel the call takes
+  if (few_token(shape, max_query_len)) total = std::max(total, layout_of(shape, num_tokens).total);
+  return total;
 }
 
 photon_status_t photon_paged_multi_query(const void* q, const void* k_cache, const void* v_cache,
@@ -429,6 +448,13 @@ photon_status_t photon_paged_multi_query(const void* q, const void* k_cache, con
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(block_tables) ||
       !aligned16(context_lens) || !aligned16(query_start) || !aligned16(out))
     return PHOTON_ERR_MISALIGNED;
+  // Few draft tokens per sequence: the decode kernel in its few-token mode
+  // (the default there; selector 3 asks for it, 1 and 2 for the others).
+  const int choice = g_mq_kernel.load(std::memory_order_relaxed);
+  if ((choice == 0 || choice == 3) && few_token(shape, max_query_len))
+    return decode_common(q, k_cache, v_cache, block_tables, context_lens, scale, out, workspace,
+                         workspace_bytes, shape, stream, nullptr, nullptr, nullptr, nullptr, 0,
+                         query_start, num_tokens, max_query_len);
   const MqPlan plan = mq_plan(shape, num_tokens, max_query_len);
   {
     const int64_t G = shape->num_q_heads / shape->num_kv_heads;
@@ -472,8 +498,7 @@ photon_status_t photon_paged_multi_query(const void* q, const void* k_cache, con
   // Query batches that fill the device without a key split (chunked prefill)
   // run on the tcgen05 kernel; split batches (a few tokens per sequence) on
   // the warp-level kernel and its merge.
-  const int choice = g_mq_kernel.load(std::memory_order_relaxed);
-  const bool tc = choice == 2 || (choice == 0 && plan.pmax == 1);
+  const bool tc = choice == 2 || ((choice == 0 || choice == 3) && plan.pmax == 1);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const cudaError_t e = tc ? photon::launch_multi_query_tc(a, s) : photon::launch_multi_query(a, s);
   return e == cudaSuccess ? PHOTON_OK : PHOTON_ERR_CUDA;
@@ -486,7 +511,7 @@ photon_status_t photon_debug_set_decode_consumer(int32_t which) {
 }
 
 photon_status_t photon_debug_set_multi_query_kernel(int32_t which) {
-  if (which < 0 || which > 2) return PHOTON_ERR_INVALID_ARG;
+  if (which < 0 || which > 3) return PHOTON_ERR_INVALID_ARG;
   g_mq_kernel.store(which, std::memory_order_relaxed);
   return PHOTON_OK;
 }

@@ -104,6 +104,7 @@ __device__ __forceinline__ uint4 ld_stream16(const void* p) {
 // partitions of the sequence.
 struct WorkItem {
   int b, p, tok_end, nparts, ctx;
+  int q0, nq;  // few-token multi-query mode: the sequence's first query row and count
 };
 
 struct DecodeArgs {
@@ -129,6 +130,13 @@ struct DecodeArgs {
   // pair, [rope_max_pos][D/2]; q rows and the new K rows turn by ctx - 1.
   const float2* rope_cs;
   int rope_max_pos;
+  // Few-token multi-query mode only (null otherwise): sequence b's query
+  // tokens are rows query_start[b] .. query_start[b+1]-1 of q and out, the
+  // last ones of its context (token i at position ctx - n + i, attending to
+  // keys 0 .. that position); max_q bounds their count, max_q * G <= 8; the
+  // workspace partials are per (token row, q head, partition).
+  const int32_t* query_start;
+  int max_q, num_tokens;
   uint32_t* err;      // sticky device error word
   float qscale;       // scale * log2(e): scores are kept in the log2 domain
   int B, Hq, Hkv, D, NB, MBS, part, pmax;

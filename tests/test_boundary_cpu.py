@@ -180,9 +180,9 @@ def test_multi_query_plan_splits_small_batches_only(lib):
 
 
 def test_multi_query_kernel_hook(lib):
-    assert lib.photon_debug_set_multi_query_kernel(3) == 1
+    assert lib.photon_debug_set_multi_query_kernel(4) == 1
     assert lib.photon_debug_set_multi_query_kernel(-1) == 1
-    for k in (1, 2, 0):
+    for k in (1, 2, 3, 0):
         assert lib.photon_debug_set_multi_query_kernel(k) == 0
 
 

@@ -16,7 +16,11 @@ oracle, through the C ABI.
 * inconsistent lengths are flagged (bits 4 / 32) and zero-filled, not faulted;
 * every case runs on both kernels -- the warp-level mma.sync one (with and
   without key splits) and the tcgen05/TMEM one -- chosen through
-  photon_debug_set_multi_query_kernel.
+  photon_debug_set_multi_query_kernel;
+* the few-token mode (max_query_len x G <= 8: the decode kernel with one
+  query slot per (token, head)): ragged token counts on every group size,
+  partitions that cut through a sequence's query tokens (a token then sees
+  none of the last partition's keys), the verify batch, and its error rules.
 """
 import os
 
@@ -41,7 +45,7 @@ def _lib():
     assert st == 0
 
 
-@pytest.fixture(params=[1, 2], ids=["mma_sync", "tcgen05"])
+@pytest.fixture(params=[1, 2, 3], ids=["mma_sync", "tcgen05", "few_token_else_plan"])
 def kernel(request):
     P.photon_debug_set_multi_query_kernel(request.param)
     yield request.param
@@ -54,7 +58,8 @@ def _workspace(shape, num_tokens, max_query_len):
     return torch.full((max(n, 16),), 0xFF, dtype=torch.uint8, device="cuda"), n
 
 
-def _run(mq: W.MultiQueryWorkload, max_query_len=None, partition=0, context_lens=None):
+def _run(mq: W.MultiQueryWorkload, max_query_len=None, partition=0, context_lens=None,
+         query_start=None):
     p = mq.pool
     shape = P.PagedShape.make(partition_size=partition, **p.shape_dict())
     mql = mq.max_query_len if max_query_len is None else max_query_len
@@ -62,8 +67,9 @@ def _run(mq: W.MultiQueryWorkload, max_query_len=None, partition=0, context_lens
     qd = dev(mq.q)
     out = torch.full(qd.shape, -1, dtype=qd.dtype, device="cuda")
     ctx = p.context_lens if context_lens is None else context_lens
+    qs = mq.query_start if query_start is None else query_start
     P.photon_paged_multi_query(qd, dev(p.k_cache), dev(p.v_cache), dev(p.block_tables),
-                               dev(ctx), dev(mq.query_start), mq.num_tokens, mql, p.scale, out,
+                               dev(ctx), dev(qs), mq.num_tokens, mql, p.scale, out,
                                ws, nws, shape)
     torch.cuda.synchronize()
     return out
@@ -117,12 +123,15 @@ def test_chunked_prefill_batch(kernel):
     assert_close(to_float64(out, W.DTYPE_F16), _want(mq), W.DTYPE_F16, "chunked prefill")
 
 
-def test_speculative_verify_batch(kernel):
+@pytest.mark.parametrize("which", [1, 2, 3], ids=["mma_sync", "tcgen05", "few_token"])
+def test_speculative_verify_batch(which):
+    P.photon_debug_set_multi_query_kernel(which)
     rng = np.random.Generator(np.random.PCG64(2))
     ctx = W.qwen_context_lens(rng, 64)
     mq = W.multi_query(311, query_lens=[4] * 64, prefix_lens=(ctx - 4).tolist(),
                        num_q_heads=16, num_kv_heads=8, head_dim=128, dtype=W.DTYPE_BF16)
     out = _run(mq)
+    P.photon_debug_set_multi_query_kernel(0)
     st, bits = P.photon_get_last_device_error()
     assert st == 0 and bits == 0, bits
     _check(to_float64(out, W.DTYPE_BF16), mq, "verify")
@@ -185,11 +194,12 @@ def test_split_partitions_match_oracle(partition):
 
 
 
-@pytest.mark.parametrize("which", [0, 2], ids=["default", "tcgen05"])
+@pytest.mark.parametrize("which", [0, 1, 2], ids=["default", "mma_sync", "tcgen05"])
 def test_prefill_without_split_matches(which):
     """A prefill batch big enough to skip the key split (no workspace), on
-    the default and the tcgen05 kernel: every row of four sequences against
-    the oracle."""
+    every kernel: every row of four sequences against the oracle.  Unsplit,
+    a sequence's keys (up to 5120) are one partition, longer than the
+    warp-level kernel's 256-block table window."""
     P.photon_debug_set_multi_query_kernel(which)
     mq = W.multi_query(330, query_lens=[1024] * 16, prefix_lens=[0] * 8 + [4096] * 8,
                        num_q_heads=16, num_kv_heads=8, head_dim=128, dtype=W.DTYPE_F16)
@@ -207,3 +217,65 @@ def test_prefill_without_split_matches(which):
                                   dtype=p.dtype, num_threads=THREADS)
         assert_close(got[qs[b]:qs[b + 1]], want, W.DTYPE_F16, f"prefill seq {b}")
     P.photon_debug_set_multi_query_kernel(0)
+
+
+@pytest.fixture
+def few_token():
+    P.photon_debug_set_multi_query_kernel(3)
+    yield 3
+    P.photon_debug_set_multi_query_kernel(0)
+
+
+@pytest.mark.parametrize("partition", [0, 64])
+@pytest.mark.parametrize("dtype", [W.DTYPE_F16, W.DTYPE_BF16])
+@pytest.mark.parametrize("Hq,Hkv,d", [(8, 8, 64), (16, 8, 128), (32, 8, 64), (16, 2, 128)])
+def test_few_token_matches_oracle(Hq, Hkv, d, dtype, partition, few_token):
+    """Token counts 1 .. 8/G per sequence on prefixes around block and
+    partition edges; with 64-key partitions the query tokens of several
+    sequences straddle a partition edge, so an early token sees no key of
+    the last partition."""
+    g = Hq // Hkv
+    nmax = 8 // g
+    lens = [(i % nmax) + 1 for i in range(10)]
+    prefix = [0, 1, 15, 16, 62, 63, 125, 200, 1000, 2000]
+    mq = W.multi_query(340 + Hq + d + dtype + partition, query_lens=lens, prefix_lens=prefix,
+                       num_q_heads=Hq, num_kv_heads=Hkv, head_dim=d, dtype=dtype)
+    out = _run(mq, partition=partition)
+    st, bits = P.photon_get_last_device_error()
+    assert st == 0 and bits == 0, bits
+    _check(to_float64(out, dtype), mq, f"few-token {Hq}/{Hkv}/{d} part {partition}")
+
+
+def test_few_token_errors_are_flagged(few_token):
+    """max_query_len 4 with 2 heads per KV head: the few-token mode.  A
+    sequence with more tokens than that (bit 32, its first 4 rows zeroed), a
+    context shorter than its token count (bit 4, rows zeroed), rows past
+    num_tokens (bit 32, rows untouched); the other sequences exact."""
+    mq = W.multi_query(350, query_lens=[3, 6, 2, 4], prefix_lens=[10, 10, 10, 30],
+                       num_q_heads=16, num_kv_heads=8, head_dim=64, dtype=W.DTYPE_F16)
+    qs = mq.query_start
+    want = _want(mq)
+
+    def good(got, seqs):
+        for b in seqs:
+            assert_close(got[qs[b]:qs[b + 1]], want[qs[b]:qs[b + 1]], W.DTYPE_F16, f"seq {b}")
+
+    got = to_float64(_run(mq, max_query_len=4), W.DTYPE_F16)
+    st, bits = P.photon_get_last_device_error()
+    assert st == 6 and bits == 32, bits
+    assert (got[qs[1]:qs[1] + 4] == 0).all()
+    good(got, (0, 2, 3))
+    bad_ctx = mq.pool.context_lens.copy()
+    bad_ctx[2] = 1
+    got = to_float64(_run(mq, max_query_len=4, context_lens=bad_ctx), W.DTYPE_F16)
+    st, bits = P.photon_get_last_device_error()
+    assert st == 6 and bits == 32 | 4, bits
+    assert (got[qs[2]:qs[3]] == 0).all()
+    good(got, (0, 3))
+    bad_qs = qs.copy()
+    bad_qs[4] = mq.num_tokens + 1
+    got = to_float64(_run(mq, max_query_len=4, query_start=bad_qs), W.DTYPE_F16)
+    st, bits = P.photon_get_last_device_error()
+    assert st == 6 and bits == 32, bits
+    assert (got[qs[3]:qs[4]] == -1).all()
+    good(got, (0, 2))
