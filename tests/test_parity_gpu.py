@@ -145,6 +145,13 @@ CASES = {
                                           head_dim=128, max_ctx=700, dtype=W.DTYPE_F32),
     "g1_d64_f32": lambda: W.random_small(46, batch=5, num_q_heads=3, num_kv_heads=3,
                                          head_dim=64, max_ctx=300, dtype=W.DTYPE_F32),
+    # more sequences than the producer caches (512): its walk reads the later
+    # 32-sequence windows from global memory
+    "b600_g4_d64_f16": lambda: W.random_small(47, batch=600, num_q_heads=8, num_kv_heads=2,
+                                              head_dim=64, max_ctx=120, dtype=W.DTYPE_F16),
+    "b1100_g2_d128_bf16": lambda: W.random_small(48, batch=1100, num_q_heads=4,
+                                                 num_kv_heads=2, head_dim=128, max_ctx=90,
+                                                 dtype=W.DTYPE_BF16),
 }
 
 
