@@ -232,8 +232,12 @@ photon_status_t photon_paged_multi_query(const void* q, const void* k_cache, con
  * that run in parallel and are merged by their log-sum-exp weights; a nonzero
  * partition_size forces the split.  The workspace then holds the partials
  * (m, l, o) of num_tokens x num_q_heads rows x ceil(max_blocks_per_seq *
- * block_size / partition) partitions.  0 for an invalid shape, f32,
- * num_tokens <= 0 or max_query_len <= 0. */
+ * block_size / partition) partitions.  When max_query_len x G <= 8 the call
+ * runs the decode kernel's few-token mode instead, with the decode's
+ * partitions (as photon_paged_decode_workspace_size) per query token; the
+ * size returned is the larger of the two, so a workspace of that size serves
+ * whichever kernel runs.  0 for an invalid shape, f32, num_tokens <= 0 or
+ * max_query_len <= 0. */
 size_t photon_paged_multi_query_workspace_size(const photon_paged_shape_t* shape,
                                                int32_t num_tokens, int32_t max_query_len);
 

@@ -129,6 +129,8 @@ struct PersistCfg {
   static constexpr int kAlignPad = M ? 1024 : 0;
   static constexpr int kSmemBytes = kOffPl + 4 * 2 * NC * kSlots + kAlignPad;
   static_assert(kSlots * D * 4 <= kBlockBytes, "a warp's o rows must fit its K block area");
+  // the producer's 32-entry block-table slices must split into whole stages
+  static_assert(NC >= 1 && NC <= 32 && 32 % NC == 0, "consumer warps must divide 32");
   static_assert(!X || (M && !R), "the few-token mode runs on the tensor-core consumer, no RoPE");
   static_assert(!M || (kBlockBytes % 1024 == 0 && sizeof(T) == 2), "swizzled blocks");
 };

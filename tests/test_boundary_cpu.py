@@ -179,6 +179,18 @@ def test_multi_query_plan_splits_small_batches_only(lib):
     assert P.photon_paged_multi_query_workspace_size(s2, 64 * 1024, 1024) > 0
 
 
+def test_multi_query_workspace_covers_the_few_token_path():
+    # 608 sequences x 2 KV heads x one 64-row tile fill the device without a
+    # key split (the warp-level and tcgen05 plans need no workspace), but
+    # max_query_len x G = 4 x 2 <= 8 runs the decode kernel's few-token mode,
+    # whose split-KV partials are per query token
+    s = _shape(num_seqs=608, num_q_heads=4, num_kv_heads=2, max_blocks_per_seq=64)
+    need = P.photon_paged_multi_query_workspace_size(s, 608 * 4, 4)
+    assert need >= 608 * 4 * 4 * (128 + 2) * 4     # (m, l, o) per token, head, partition >= 1
+    # 5 tokens x 2 heads > 8 slots: the plans without a split need none
+    assert P.photon_paged_multi_query_workspace_size(s, 608 * 5, 5) == 0
+
+
 def test_multi_query_kernel_hook(lib):
     assert lib.photon_debug_set_multi_query_kernel(4) == 1
     assert lib.photon_debug_set_multi_query_kernel(-1) == 1
