@@ -150,12 +150,13 @@ __device__ __forceinline__ uint32_t sw_chunk(int r, int c) {
 }
 
 // Shared-memory plan of the warp-specialised kernel: two Q tiles of 128 rows,
-// a ring of kStages K/V chunks (filled by the tensor memory accelerator), one
-// P buffer per Q tile.
+// a ring of kStages K/V chunks (filled by the tensor memory accelerator), two
+// P buffers per Q tile (chunk c uses buffer c % 2, so the softmax of chunk c
+// writes its weights while the product of chunk c - 1 still reads the other).
 template <typename T, int D>
 struct TcCfg {
   static constexpr int kTiles = 2;
-  static constexpr int kStages = 4;
+  static constexpr int kStages = 3;
   static constexpr int kQBytes = kTcRows * D * 2;     // one Q tile
   static constexpr int kKBytes = kTcKeys * D * 2;     // one K chunk
   static constexpr int kVBytes = kTcKeys * D * 2;     // one V chunk
@@ -163,8 +164,8 @@ struct TcCfg {
   static constexpr int kOffQ = 0;                               // [kTiles]
   static constexpr int kOffK = kOffQ + kTiles * kQBytes;        // [kStages]
   static constexpr int kOffV = kOffK + kStages * kKBytes;       // [kStages]
-  static constexpr int kOffP = kOffV + kStages * kVBytes;       // [kTiles]
-  static constexpr int kUsed = kOffP + kTiles * kPBytes;
+  static constexpr int kOffP = kOffV + kStages * kVBytes;       // [kTiles][2]
+  static constexpr int kUsed = kOffP + kTiles * 2 * kPBytes;
   static constexpr int kSmem = kUsed + 1024;   // + alignment of the base to a swizzle atom
   // softmax warps, then the copy warp and the MMA warp
   static constexpr int kThreads = kTiles * kTcThreads + 64;
@@ -199,8 +200,10 @@ __device__ __forceinline__ void mbar_arrive_cnt(uint64_t* bar) { mbar_arrive(bar
 //   kv_free[s]     the P V products reading stage s finished (MMA commit)
 //   s_full[t][b]   S of a chunk is in tile t's TMEM buffer b (MMA commit)
 //   s_free[t][b]   tile t's 4 softmax warps have read that buffer (4 arrivals)
-//   p_full[t]      tile t's P of a chunk is in its shared buffer (128 arrivals)
-//   p_done[t]      the P V product reading that buffer finished (MMA commit)
+//   p_full[t][b]   tile t's P of a chunk is in its shared buffer b (128 arrivals)
+//   p_done[t][b]   the P V product reading that buffer finished (MMA commit)
+// The b-indexed barriers serve chunks b, b + 2, ...: chunk c's use of one has
+// parity (c / 2) & 1.
 template <typename T, int D>
 __global__ void __launch_bounds__(TcCfg<T, D>::kThreads)
     paged_multi_query_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
@@ -211,7 +214,7 @@ __global__ void __launch_bounds__(TcCfg<T, D>::kThreads)
   constexpr int kSuper = NT * kTcRows;
   extern __shared__ unsigned char tc_smem_raw[];
   __shared__ __align__(8) uint64_t kv_full[S], kv_free[S], s_full[NT][2], s_free[NT][2],
-      p_full[NT], p_done[NT];
+      p_full[NT][2], p_done[NT][2];
   __shared__ uint32_t tmem_slot;
   __shared__ int tail_rows[S];   // per stage: first V row to zero (64 = none)
   unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -263,9 +266,9 @@ __global__ void __launch_bounds__(TcCfg<T, D>::kThreads)
       for (int i = 0; i < 2; ++i) {
         mbar_init(&s_full[t][i], 1);
         mbar_init(&s_free[t][i], 4);
+        mbar_init(&p_full[t][i], kTcThreads);
+        mbar_init(&p_done[t][i], 1);
       }
-      mbar_init(&p_full[t], kTcThreads);
-      mbar_init(&p_done[t], 1);
     }
     mbar_init_fence();
   }
@@ -382,18 +385,19 @@ __global__ void __launch_bounds__(TcCfg<T, D>::kThreads)
       }
       if (c >= 1) {
         // P V of the previous chunk, tile by tile, once its weights are written
-        const int pc = c - 1, pst = pc % S;
+        const int pc = c - 1, pst = pc % S, pb = pc & 1;
         for (int t = 0; t < ntiles && ok; ++t) {
-          ok = lane0_ok(mbar_wait_bounded(&p_full[t], pc & 1));
+          ok = lane0_ok(mbar_wait_bounded(&p_full[t][pb], (pc >> 1) & 1));
           if (!ok) break;
           if (lane == 0) {
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < kTcKeys / 16; ++kk)
-              tc_mma(tmem + t * kTmemCols + kTmemO, sw128_desc(sP + t * C::kPBytes + kk * 32),
+              tc_mma(tmem + t * kTmemCols + kTmemO,
+                     sw128_desc(sP + (t * 2 + pb) * C::kPBytes + kk * 32),
                      sw128_mn_desc(sV + pst * C::kVBytes + kk * 2048), id_o,
                      (pc > 0 || kk > 0) ? 1u : 0u);
-            tc_commit(&p_done[t]);
+            tc_commit(&p_done[t][pb]);
           }
         }
         if (!ok) break;
@@ -453,14 +457,17 @@ __global__ void __launch_bounds__(TcCfg<T, D>::kThreads)
       const float corr = moved ? softmax_exp2(m_run - mx) : 1.f;   // 0 on the first chunk
       l_run *= corr;
       if (moved) m_run = mx;
-      // the product of chunk c - 1 reads this tile's P buffer and updates O:
-      // it must be done before O is rescaled or P overwritten
-      if (c > 0) {
-        ok = mbar_wait_bounded(&p_done[t], (c - 1) & 1);
+      // the product of chunk c - 2 read the P buffer this chunk writes; the
+      // product of chunk c - 1 updates O, so a rescale waits for it too
+      if (c >= 2) {
+        ok = mbar_wait_bounded(&p_done[t][c & 1], ((c - 2) >> 1) & 1);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
       }
       if (c > 0 && __any_sync(0xffffffffu, moved)) {
+        ok = mbar_wait_bounded(&p_done[t][(c - 1) & 1], ((c - 1) >> 1) & 1);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        tc_fence_after();
 #pragma unroll 1
         for (int col = 0; col < D; col += 32) {
           float o[32];
@@ -472,7 +479,7 @@ __global__ void __launch_bounds__(TcCfg<T, D>::kThreads)
         tc_fence_before();
       }
       float sum4[4] = {0.f, 0.f, 0.f, 0.f};
-      unsigned char* prow = smem + C::kOffP + t * C::kPBytes;
+      unsigned char* prow = smem + C::kOffP + (t * 2 + (c & 1)) * C::kPBytes;
 #pragma unroll
       for (int ch = 0; ch < kTcKeys / 8; ++ch) {
         uint32_t w[4];
@@ -494,12 +501,12 @@ __global__ void __launch_bounds__(TcCfg<T, D>::kThreads)
       }
       l_run += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
       fence_async_smem();
-      mbar_arrive_cnt(&p_full[t]);
+      mbar_arrive_cnt(&p_full[t][c & 1]);
     }
     // ---- the last product, then O / l
     if (tile_used) {
       if (ok) {
-        ok = mbar_wait_bounded(&p_done[t], (nchunks - 1) & 1);
+        ok = mbar_wait_bounded(&p_done[t][(nchunks - 1) & 1], ((nchunks - 1) >> 1) & 1);
         ok = __all_sync(0xffffffffu, ok);
       }
       if (!ok) {
