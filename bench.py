@@ -357,8 +357,9 @@ def ncu_traffic(workload: str):
     or None if the summary is missing or was taken on other kernel sources."""
     path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
     try:
-        d = json.load(open(path))
-    except Exception:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
         return None
     e = d.get(workload)
     if not e or e.get("kernel_source_sha") != kernel_source_hash():
