@@ -264,6 +264,80 @@ def multi_query(q, k_cache, v_cache, block_tables, context_lens, query_start, sc
                         num_threads=num_threads)
 
 
+# ------------------------------------------------------------------ fp8 (e4m3) KV cache
+# The further step of the bf16 row (README "Roadmap": lower-precision KV):
+# K and V stored as OCP e4m3 codes -- 1 sign bit, 4 exponent bits (bias 7),
+# 3 mantissa bits; exponent field 0 is subnormal (m * 2^-9); exponent 15 with
+# mantissa 7 is NaN; no infinities; the largest finite value is 448 -- each
+# with one per-tensor scale: value = decode(code) * scale.
+
+def e4m3_decode(codes) -> np.ndarray:
+    """float64 values of e4m3 codes (NaN for 0x7F / 0xFF), read off the bit
+    fields as defined above."""
+    c = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(c >> 7, -1.0, 1.0)
+    e = (c >> 3) & 0xF
+    m = c & 7
+    mag = np.where(e == 0, m * 2.0 ** -9, (1.0 + m / 8.0) * np.power(2.0, e - 7))
+    mag = np.where((e == 15) & (m == 7), np.nan, mag)
+    return sign * mag
+
+
+_E4M3_POS = e4m3_decode(np.arange(0x7F, dtype=np.uint8))   # codes 0x00 .. 0x7E, increasing
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """e4m3 codes of float values: round to the nearest finite e4m3 value,
+    ties to the even code (even mantissa), magnitudes beyond 448 saturate to
+    448 (the finite-saturating conversion), NaN -> 0x7F.  A brute-force search
+    over the 127 non-negative finite values."""
+    v = np.asarray(x, dtype=np.float64)
+    a = np.abs(v)
+    i = np.clip(np.searchsorted(_E4M3_POS, a), 1, len(_E4M3_POS) - 1)   # a in (pos[i-1], pos[i]]
+    lo, hi = _E4M3_POS[i - 1], _E4M3_POS[i]
+    pick_hi = (hi - a < a - lo) | ((hi - a == a - lo) & (i % 2 == 0))
+    code = np.where(pick_hi, i, i - 1)
+    code = np.where(a >= _E4M3_POS[-1], 0x7E, code)                  # saturate
+    code = np.where(a == 0, 0, code)
+    code = code.astype(np.int64) | np.where(np.signbit(v), 0x80, 0)
+    code = np.where(np.isnan(v), 0x7F, code)
+    return code.astype(np.uint8)
+
+
+def cache_write_fp8(k_new, v_new, slot_mapping, k_cache8, v_cache8, k_scale: float,
+                    v_scale: float, *, block_size: int) -> None:
+    """Quantising cache write: row t of k_new / v_new (fp16) goes to slot_t as
+    e4m3 codes of x * (1 / scale), the product taken in fp32 (the reciprocal
+    rounded to fp32 first), in place on the uint8 pools.  Negative slots are
+    padding."""
+    NB, Hkv, bs, d = k_cache8.shape
+    assert bs == block_size
+    for src, dst, scale in ((k_new, k_cache8, k_scale), (v_new, v_cache8, v_scale)):
+        inv = np.float32(1.0) / np.float32(scale)
+        for t, slot in enumerate(np.asarray(slot_mapping, dtype=np.int64)):
+            if slot < 0:
+                continue
+            if slot >= NB * bs:
+                raise OracleError("slot out of range")
+            x = np.asarray(src[t], dtype=np.float16).astype(np.float32) * inv
+            dst[slot // bs, :, slot % bs, :] = e4m3_encode(x)
+
+
+def paged_decode_fp8(q, k_cache8, v_cache8, block_tables, context_lens, scale: float,
+                     k_scale: float, v_scale: float, *, num_threads: int = 1) -> np.ndarray:
+    """Paged decode over an e4m3 cache: attention over K = decode(code) *
+    k_scale and V = decode(code) * v_scale, in fp64.  Written through the
+    identity softmax(scale q.(s_k K)) (s_v V) = s_v softmax((scale s_k) q.K) V
+    so that the fp64 decode above reads the codes' values exactly (as fp32
+    pools); float64 [B][Hq][d]."""
+    k32 = e4m3_decode(k_cache8).astype(np.float32)
+    v32 = e4m3_decode(v_cache8).astype(np.float32)
+    q32 = np.asarray(q, dtype=np.float16).astype(np.float32)
+    out = paged_decode(q32, k32, v32, block_tables, context_lens, float(scale) * float(k_scale),
+                       dtype=0, num_threads=num_threads)
+    return out * float(v_scale)
+
+
 def narrow(x64: np.ndarray, dtype: int) -> np.ndarray:
     """float64 -> storage dtype, round to nearest even (bf16 through fp32)."""
     if dtype == 0:

@@ -604,3 +604,75 @@ def test_multi_query_first_token_of_a_fresh_prompt_returns_its_v():
         blk = p.block_tables[b, 0]
         v0 = p.v_cache[blk, :, 0].astype(np.float64)              # [Hkv][d], position 0
         np.testing.assert_array_equal(out[mq.query_start[b]], np.repeat(v0, 2, axis=0))
+
+
+# ------------------------------------------------------------------ fp8 (e4m3) cache
+def test_e4m3_decode_matches_torch_for_every_code():
+    codes = np.arange(256, dtype=np.uint8)
+    got = oracle.e4m3_decode(codes)
+    want = torch.from_numpy(codes).view(torch.float8_e4m3fn).float().double().numpy()
+    assert np.array_equal(np.isnan(got), np.isnan(want))
+    ok = ~np.isnan(want)
+    assert np.array_equal(got[ok], want[ok])
+    # closed forms: largest finite, smallest subnormal, one, the NaN codes
+    assert oracle.e4m3_decode([0x7E, 0x01, 0x38, 0xB8])[:4].tolist() == [448.0, 2.0 ** -9,
+                                                                      1.0, -1.0]
+    assert np.isnan(oracle.e4m3_decode([0x7F, 0xFF])).all()
+
+
+def test_e4m3_encode_matches_torch_in_range():
+    rng = np.random.default_rng(7)
+    x = (rng.standard_normal(100000) * np.exp(rng.uniform(-12, 6, 100000))).astype(np.float32)
+    x = x[np.abs(x) <= 448]
+    want = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(oracle.e4m3_encode(x), want)
+
+
+def test_e4m3_encode_ties_saturation_and_round_trip():
+    # halfway between 1.0 and 1.125 -> the even code (1.0); between 1.125 and 1.25 -> 1.25
+    assert oracle.e4m3_encode([1.0625, 1.1875, -1.0625]).tolist() == [0x38, 0x3A, 0xB8]
+    # beyond the largest finite value: saturates to +-448; NaN stays NaN
+    assert oracle.e4m3_encode([449.0, 500.0, 1e30, -1e30]).tolist() == [0x7E, 0x7E, 0x7E, 0xFE]
+    assert oracle.e4m3_encode([np.nan]).tolist() == [0x7F]
+    finite = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], dtype=np.uint8)
+    back = oracle.e4m3_encode(oracle.e4m3_decode(finite))
+    assert np.array_equal(back[finite != 0x80], finite[finite != 0x80])   # -0 may become +0
+
+
+def test_fp8_cache_write_quantises_each_row_at_its_slot():
+    wl = W.random_small(61, batch=3, num_q_heads=4, num_kv_heads=2, head_dim=64, max_ctx=40,
+                        dtype=W.DTYPE_F16)
+    k8, v8 = W.fp8_cache(wl, 5)
+    k0, v0 = k8.copy(), v8.copy()
+    oracle.cache_write_fp8(wl.k_new, wl.v_new, wl.slot_mapping, k8, v8, 0.5, 0.25,
+                           block_size=16)
+    for t, slot in enumerate(wl.slot_mapping):
+        blk, off = slot // 16, slot % 16
+        want = oracle.e4m3_encode(wl.k_new[t].astype(np.float32) * np.float32(2.0))
+        assert np.array_equal(k8[blk, :, off], want)
+        k0[blk, :, off] = k8[blk, :, off]
+        v0[blk, :, off] = v8[blk, :, off]
+    assert np.array_equal(k0, k8) and np.array_equal(v0, v8)   # nothing else changed
+
+
+def test_fp8_decode_equals_brute_force_on_dequantised_values():
+    """The definition written out: dequantise every cached K/V element
+    (code value x scale) and take softmax(scale q.K) V per head in numpy."""
+    wl = W.random_small(62, batch=3, num_q_heads=8, num_kv_heads=2, head_dim=64, max_ctx=70,
+                        dtype=W.DTYPE_F16, context_lens=[1, 33, 70])
+    k8, v8 = W.fp8_cache(wl, 6)
+    ks, vs = 0.5, 0.25
+    got = oracle.paged_decode_fp8(wl.q, k8, v8, wl.block_tables, wl.context_lens, wl.scale,
+                                  ks, vs)
+    G = wl.num_q_heads // wl.num_kv_heads
+    for b in range(3):
+        c = int(wl.context_lens[b])
+        blocks = wl.block_tables[b, :(c + 15) // 16]
+        for h in range(wl.num_q_heads):
+            kv = h // G
+            K = np.concatenate([oracle.e4m3_decode(k8[p, kv]) for p in blocks])[:c] * ks
+            V = np.concatenate([oracle.e4m3_decode(v8[p, kv]) for p in blocks])[:c] * vs
+            s_ = wl.scale * (K @ wl.q[b, h].astype(np.float64))
+            w = np.exp(s_ - s_.max())
+            want = (w[:, None] * V).sum(0) / w.sum()
+            assert np.abs(got[b, h] - want).max() <= 1e-12

@@ -293,6 +293,33 @@ def random_small(seed: int, *, batch: int, num_q_heads: int, num_kv_heads: int,
                  block_size=block_size, max_blocks_per_seq=mbs, seed=seed)
 
 
+# e4m3 code of NaN: fills the unreferenced blocks of an fp8 pool (stray-read detector)
+E4M3_NAN = 0x7F
+# per-tensor scales of the synthetic fp8 caches
+FP8_K_SCALE, FP8_V_SCALE = 0.5, 0.25
+
+
+def fp8_cache(wl: Workload, seed: int):
+    """e4m3 K and V pools for the sequences of `wl` (its tables and lengths):
+    every block a table names gets random finite codes -- random sign,
+    exponent field 5 .. 8, random mantissa, i.e. magnitudes 0.25 .. 3.75 --
+    the other blocks the NaN code.  Bytes only; the scales are FP8_K_SCALE /
+    FP8_V_SCALE.  Returns (k8, v8), uint8 [NB][Hkv][bs][d]."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    shape = (wl.num_blocks, wl.num_kv_heads, wl.block_size, wl.head_dim)
+    pools = []
+    used = np.unique(wl.block_tables[wl.block_tables >= 0])
+    for _ in range(2):
+        pool = np.full(shape, E4M3_NAN, dtype=np.uint8)
+        n = used.shape[0] * int(np.prod(shape[1:]))
+        sign = rng.integers(0, 2, size=n, dtype=np.uint8) << np.uint8(7)
+        expo = rng.integers(5, 9, size=n, dtype=np.uint8) << np.uint8(3)
+        mant = rng.integers(0, 8, size=n, dtype=np.uint8)
+        pool[used] = (sign | expo | mant).reshape((used.shape[0],) + shape[1:])
+        pools.append(pool)
+    return pools[0], pools[1]
+
+
 def request_trace(seed: int, num_requests: int, *, max_prompt: int, max_new: int,
                   pool_tokens: int, long_frac: float = 0.2,
                   arrivals_per_step: float = 1.0) -> List[tuple]:
