@@ -68,6 +68,7 @@ def parse():
     ap.add_argument("--mq-case", default="", choices=["", "verify_b64x4", "prefill_b16x1024"],
                     help="profiling aid: run only this multi-query case (default kernel "
                          "choice, --steps calls) and print its timing")
+    ap.add_argument("--no-fp8", action="store_true", help="skip the e4m3-cache decode line")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the side measurements of the other decode configurations")
     ap.add_argument("--decode-consumer", type=int, default=0, choices=[0, 1, 2],
@@ -208,6 +209,55 @@ def multi_query_side(P, torch, stream, flush_l2, K, hbm_peak, only: str = "",
                      "per_kernel": per_kernel}
         del q, kc, vc, bt, cl, qs, out, ws
     return res
+
+
+def fp8_side(P, torch, stream, flush_l2, K, peak):
+    """The same batch-64 long-context decode over an e4m3 K/V cache
+    (photon_paged_decode_fp8): the codes of the synthetic fp8 pools, fp16 q
+    and out.  Algorithmic bytes as the fp16 decode's with one byte per cached
+    element."""
+    wl = W.qwen_b64()
+    k8, v8 = W.fp8_cache(wl, 2)
+    shape = P.PagedShape.make(**wl.shape_dict())
+
+    def dev(a):
+        return torch.from_numpy(np.ascontiguousarray(a)).cuda()
+
+    q, kc, vc = dev(wl.q), dev(k8), dev(v8)
+    bt, cl = dev(wl.block_tables), dev(wl.context_lens)
+    out = torch.empty_like(q)
+    nws = P.photon_paged_decode_fp8_workspace_size(shape)
+    ws = torch.empty(max(nws, 16), dtype=torch.uint8, device="cuda")
+
+    def call():
+        P.photon_paged_decode_fp8(q, kc, vc, bt, cl, wl.scale, W.FP8_K_SCALE, W.FP8_V_SCALE,
+                                  out, ws, nws, shape, stream)
+
+    for _ in range(3):
+        flush_l2()
+        call()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(K)]
+    for i in range(K):
+        flush_l2()
+        ev[i][0].record(stream)
+        call()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    st, bits = P.photon_get_last_device_error(stream)
+    if st != 0:
+        raise RuntimeError(f"device error word {bits} in the fp8 decode")
+    ms = sum(a.elapsed_time(b) for a, b in ev) / K
+    ctx = wl.context_lens.astype(np.int64)
+    nbytes = (int(ctx.sum()) * wl.num_kv_heads * wl.head_dim * 2
+              + 2 * wl.num_seqs * wl.num_q_heads * wl.head_dim * 2
+              + 4 * int(((ctx + 15) // 16).sum()) + 4 * wl.num_seqs)
+    gbs = nbytes / (ms / 1e3) / 1e9
+    return {"workload": "qwen_b64 with an e4m3 K/V cache (k_scale 0.5, v_scale 0.25)",
+            "ms_per_call": round(ms, 5), "algorithmic_bytes": int(nbytes),
+            "GBps": round(gbs, 1), "hbm_fraction": round(gbs / peak, 4),
+            "tokens_attended_per_s": round(wl.tokens_attended() / (ms / 1e3), 1),
+            "decode_tokens_per_s_per_layer": round(wl.num_seqs / (ms / 1e3), 1)}
 
 
 def consumer_name(choice: int, wl: W.Workload) -> str:
@@ -745,6 +795,9 @@ def run_ours(args):
     if not args.no_mq:
         mq_side = multi_query_side(P, torch, stream, flush_l2, K, peak)
     host_sched = scheduler_side(P) if rank == 0 and not args.no_mq else None
+    fp8 = None
+    if not args.no_fp8 and args.workload == "qwen_b64":
+        fp8 = fp8_side(P, torch, stream, flush_l2, K, peak)
     other_configs = None
     if not args.no_configs:
         other_configs = configs_side(P, torch, stream, flush_l2, K, peak, args.decode_consumer)
@@ -786,6 +839,7 @@ def run_ours(args):
             "multi_query": mq_side,
             "host_scheduler": host_sched,
             "other_configs": other_configs,
+            "fp8_kv_decode": fp8,
             "gpu_launches": K * plan["kernels_per_call"],
             "clocks": clocks,
             "wall_ms_per_step_incl_flush": round(1e3 * t_wall / K, 4),

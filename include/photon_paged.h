@@ -241,6 +241,43 @@ photon_status_t photon_paged_multi_query(const void* q, const void* k_cache, con
 size_t photon_paged_multi_query_workspace_size(const photon_paged_shape_t* shape,
                                                int32_t num_tokens, int32_t max_query_len);
 
+/* ---- fp8 (e4m3) KV cache: the further step of the bf16 variant (README
+ * "Roadmap": lower-precision KV).  The pools hold OCP e4m3 codes, one byte per
+ * element, in the same layout [num_blocks][Hkv][16][head_dim]; element value
+ * = code value x scale, one scale for K and one for V (per tensor).  q, out
+ * and the new rows stay fp16: shape->dtype must be PHOTON_F16
+ * (PHOTON_ERR_UNSUPPORTED otherwise); k_scale and v_scale must be finite and
+ * positive (PHOTON_ERR_INVALID_ARG).  Cache pointers 16-byte aligned. */
+
+/* Quantising batched cache write: row t of k / v ([num_tokens][Hkv][d] fp16)
+ * is stored at slot_mapping[t] as the e4m3 codes of x * (1 / scale) -- the
+ * reciprocal rounded to fp32, the product in fp32, then rounded to the
+ * nearest e4m3 value (ties to even), magnitudes beyond 448 saturating to 448.
+ * Slots as photon_cache_write (negative = padding, out of range: device
+ * error bit 2). */
+photon_status_t photon_cache_write_fp8(const void* k, const void* v,
+                                       const int64_t* slot_mapping, int32_t num_tokens,
+                                       void* k_cache, void* v_cache, float k_scale,
+                                       float v_scale, const photon_paged_shape_t* shape,
+                                       photon_stream_t stream);
+
+/* Workspace bytes of photon_paged_decode_fp8 (0 for an invalid shape or a
+ * dtype other than PHOTON_F16).  Its partitions hold twice the tokens of the
+ * fp16 decode's (the same bytes per work item). */
+size_t photon_paged_decode_fp8_workspace_size(const photon_paged_shape_t* shape);
+
+/* photon_paged_decode over an e4m3 cache: out = softmax(scale * q . K) V with
+ * K = code value x k_scale and V = code value x v_scale, fp32 arithmetic on
+ * the tensor cores (the codes widen exactly to fp16), out rounded to fp16.
+ * Layouts, context lengths, block tables, errors and workspace rules as
+ * photon_paged_decode. */
+photon_status_t photon_paged_decode_fp8(const void* q, const void* k_cache, const void* v_cache,
+                                        const int32_t* block_tables, const int32_t* context_lens,
+                                        float scale, float k_scale, float v_scale, void* out,
+                                        void* workspace, size_t workspace_bytes,
+                                        const photon_paged_shape_t* shape,
+                                        photon_stream_t stream);
+
 /* Test and tuning hook: which consumer the decode attention kernel runs
  * (photon_paged_decode, _step, _step_rope, _noalloc).  0 (default) = by the group size: the tensor-core consumer
  * (mma.sync over tensor-map copies of the blocks) for fp16/bf16 storage and

@@ -29,7 +29,8 @@ __all__ = [
     "photon_paged_decode_noalloc", "photon_paged_decode_step",
     "photon_rope_cos_sin", "photon_paged_decode_step_rope", "photon_paged_multi_query",
     "photon_paged_multi_query_workspace_size", "photon_debug_set_multi_query_kernel",
-    "photon_debug_set_decode_consumer",
+    "photon_debug_set_decode_consumer", "photon_cache_write_fp8",
+    "photon_paged_decode_fp8_workspace_size", "photon_paged_decode_fp8",
     "photon_debug_wait_probe", "Scheduler",
     "F32", "F16", "BF16", "STATUS",
 ]
@@ -112,6 +113,15 @@ def _load() -> ctypes.CDLL:
     lib.photon_debug_set_multi_query_kernel.restype = ctypes.c_int
     lib.photon_debug_set_decode_consumer.argtypes = [I32]
     lib.photon_debug_set_decode_consumer.restype = ctypes.c_int
+    F32 = ctypes.c_float
+    lib.photon_cache_write_fp8.argtypes = [P, P, P, I32, P, P, F32, F32,
+                                           ctypes.POINTER(PagedShape), P]
+    lib.photon_cache_write_fp8.restype = ctypes.c_int
+    lib.photon_paged_decode_fp8_workspace_size.argtypes = [ctypes.POINTER(PagedShape)]
+    lib.photon_paged_decode_fp8_workspace_size.restype = SZ
+    lib.photon_paged_decode_fp8.argtypes = [P, P, P, P, P, F32, F32, F32, P, P, SZ,
+                                            ctypes.POINTER(PagedShape), P]
+    lib.photon_paged_decode_fp8.restype = ctypes.c_int
     lib.photon_paged_multi_query.restype = ctypes.c_int
     # host scheduler (include/photon_scheduler.h)
     lib.photon_scheduler_create.argtypes = [P, ctypes.POINTER(P)]
@@ -270,6 +280,33 @@ def photon_debug_set_decode_consumer(which: int) -> None:
     cores (fp16/bf16 storage)."""
     _check(_load().photon_debug_set_decode_consumer(int(which)),
            "photon_debug_set_decode_consumer")
+
+
+def photon_cache_write_fp8(k, v, slot_mapping, num_tokens: int, k_cache, v_cache,
+                           k_scale: float, v_scale: float, shape: PagedShape,
+                           stream=None) -> None:
+    """Quantising cache write into e4m3 pools (uint8 tensors)."""
+    _check(_load().photon_cache_write_fp8(_ptr(k), _ptr(v), _ptr(slot_mapping), int(num_tokens),
+                                          _ptr(k_cache), _ptr(v_cache), float(k_scale),
+                                          float(v_scale), ctypes.byref(shape),
+                                          _stream(stream)),
+           "photon_cache_write_fp8")
+
+
+def photon_paged_decode_fp8_workspace_size(shape: PagedShape) -> int:
+    return int(_load().photon_paged_decode_fp8_workspace_size(ctypes.byref(shape)))
+
+
+def photon_paged_decode_fp8(q, k_cache, v_cache, block_tables, context_lens, scale: float,
+                            k_scale: float, v_scale: float, out, workspace,
+                            workspace_bytes: int, shape: PagedShape, stream=None) -> None:
+    """Paged decode over e4m3 K/V pools (uint8 tensors) with fp16 q and out."""
+    _check(_load().photon_paged_decode_fp8(_ptr(q), _ptr(k_cache), _ptr(v_cache),
+                                           _ptr(block_tables), _ptr(context_lens),
+                                           float(scale), float(k_scale), float(v_scale),
+                                           _ptr(out), _ptr(workspace), int(workspace_bytes),
+                                           ctypes.byref(shape), _stream(stream)),
+           "photon_paged_decode_fp8")
 
 
 def photon_paged_decode_noalloc(q, k_cache, v_cache, block_tables, context_lens, scale: float,

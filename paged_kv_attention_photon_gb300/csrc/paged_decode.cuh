@@ -53,6 +53,8 @@
 #include <math.h>
 #include <string.h>
 
+#include <cuda_fp8.h>
+
 #include <type_traits>
 
 #include "photon_common.cuh"
@@ -97,12 +99,19 @@ constexpr int kMaxRuns = 10;
 // fused step's new K/V row lands in a side slot of its stage.
 // X: few-token multi-query mode (tensor-core consumer only): up to 8 query
 // slots (token, head) per item instead of the G heads of one token.
-template <typename T, int D, int G, int NC, int S, bool R = false, bool M = false, bool X = false>
+// F: the cache holds e4m3 codes (one byte per element; q and out stay fp16):
+// the stages carry the fp8 blocks, moved by plain bulk copies, and each
+// consumer warp widens its K and V block to fp16 in a swizzled scratch of its
+// own that the tensor-core math reads.
+template <typename T, int D, int G, int NC, int S, bool R = false, bool M = false, bool X = false,
+          bool F = false>
 struct PersistCfg {
   using C = DecodeCfg<T, D, G>;
   static constexpr int kThreads = (NC + 1) * 32;
   static constexpr int kBlockElems = kBlockSize * D;
-  static constexpr int kBlockBytes = kBlockElems * (int)sizeof(T);
+  static constexpr int kElemBytes = F ? 1 : (int)sizeof(T);       // one cache element
+  static constexpr int kBlockBytes = kBlockElems * kElemBytes;    // one cache block (a stage slot)
+  static constexpr int kWideBytes = kBlockElems * (int)sizeof(T);  // F: one block widened to T
   static constexpr int kSlots = X ? 8 : G;                      // query rows per item
   static constexpr int kQBytes = kSlots * D * (int)sizeof(T);
   // with RoPE the item's (cos, sin) row, D/2 float pairs, follows its q rows
@@ -119,20 +128,26 @@ struct PersistCfg {
   static constexpr int kKVAlign = M ? 1024 : 128;
   static constexpr int kOffKV = (kOffQ + kQStride * S + kKVAlign - 1) / kKVAlign * kKVAlign;
   // M only: the new token's K row then V row, per stage
-  static constexpr int kSideBytes = M ? 2 * D * (int)sizeof(T) : 0;
+  static constexpr int kSideBytes = M && !F ? 2 * D * (int)sizeof(T) : 0;
   static constexpr int kOffSide = kOffKV + kStageBytes * S;
+  // F only: each consumer warp's widened K block, then V block
+  static constexpr int kOffWide = (kOffSide + kSideBytes * S + 1023) / 1024 * 1024;
+  static constexpr int kWideTotal = F ? NC * 2 * kWideBytes : 0;
   // Per-warp (m, l) at an item's end, double-buffered by item parity.  The
-  // warps' o rows (G x D fp32 each) go to their own K block areas of the
-  // item's last stage, which is released only after the combine.
-  static constexpr int kOffPm = kOffSide + kSideBytes * S;      // float[2][NC][kSlots]
+  // warps' o rows (kSlots x D fp32 each) go to their own K (then V) block
+  // areas of the item's last stage, which is released only after the combine.
+  static constexpr int kOffPm = F ? kOffWide + kWideTotal : kOffSide + kSideBytes * S;
   static constexpr int kOffPl = kOffPm + 4 * 2 * NC * kSlots;   // float[2][NC][kSlots]
   static constexpr int kAlignPad = M ? 1024 : 0;
   static constexpr int kSmemBytes = kOffPl + 4 * 2 * NC * kSlots + kAlignPad;
-  static_assert(kSlots * D * 4 <= kBlockBytes, "a warp's o rows must fit its K block area");
+  static constexpr int kPoRowsPerBlock = kBlockBytes / (D * 4);  // o rows in one block area
+  static_assert(kSlots <= 2 * kPoRowsPerBlock, "a warp's o rows must fit its K and V block areas");
   // the producer's 32-entry block-table slices must split into whole stages
   static_assert(NC >= 1 && NC <= 32 && 32 % NC == 0, "consumer warps must divide 32");
   static_assert(!X || (M && !R), "the few-token mode runs on the tensor-core consumer, no RoPE");
   static_assert(!M || (kBlockBytes % 1024 == 0 && sizeof(T) == 2), "swizzled blocks");
+  static_assert(!F || (M && !R && !X && std::is_same<T, __half>::value),
+                "the fp8 cache: plain decode on the tensor-core consumer, fp16 q and out");
 };
 
 // ------------------------------------------------------------------ consumer math
@@ -330,6 +345,20 @@ __device__ __forceinline__ void attend_block_mma(uint32_t kblk, uint32_t vblk, i
   }
 }
 
+// Two e4m3 codes (the low byte first) widened exactly to an fp16 pair, and
+// sixteen codes of a 16-byte load (code 0 at the lowest address) to elements
+// 0-7 (lo) and 8-15 (hi).  Every e4m3 value is an fp16 value.
+__device__ __forceinline__ uint32_t widen_e4m3x2(uint32_t pair) {
+  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)pair, __NV_E4M3);
+  return (uint32_t)h.x | ((uint32_t)h.y << 16);
+}
+__device__ __forceinline__ void widen_e4m3x16(const uint4 q, uint4& lo, uint4& hi) {
+  lo = make_uint4(widen_e4m3x2(q.x & 0xFFFFu), widen_e4m3x2(q.x >> 16),
+                  widen_e4m3x2(q.y & 0xFFFFu), widen_e4m3x2(q.y >> 16));
+  hi = make_uint4(widen_e4m3x2(q.z & 0xFFFFu), widen_e4m3x2(q.z >> 16),
+                  widen_e4m3x2(q.w & 0xFFFFu), widen_e4m3x2(q.w >> 16));
+}
+
 // ------------------------------------------------------------------ RoPE
 // Rotate-half rotary embedding: for k < D/2 the pair (x[k], x[k + D/2]) turns
 // by the table's (cos, sin) for (pos, k).  Positions outside the table are
@@ -442,11 +471,15 @@ static __device__ unsigned long long g_probe[kProbeCtas][kProbeSlots];
 // kMulti: the few-token multi-query mode (photon_paged_multi_query with
 // max_query_len * G <= 8): an item's query slots are the (token, head) pairs
 // of its sequence's n query tokens, each with its causal limit.
-template <typename T, int D, int G, int NC, int S, bool kRope, bool kMma, bool kMulti>
+// kFp8: the e4m3 cache (photon_paged_decode_fp8): K/V blocks arrive by bulk
+// copy as codes, each consumer warp widens its pair into its fp16 scratch;
+// the K scale is folded into qscale, the V scale into the item's combine.
+template <typename T, int D, int G, int NC, int S, bool kRope, bool kMma, bool kMulti,
+          bool kFp8 = false>
 __global__ void __launch_bounds__((NC + 1) * 32, 1)
     paged_decode_attention_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
                                   const __grid_constant__ CUtensorMap tmv) {
-  using PC = PersistCfg<T, D, G, NC, S, kRope, kMma, kMulti>;
+  using PC = PersistCfg<T, D, G, NC, S, kRope, kMma, kMulti, kFp8>;
   using C = DecodeCfg<T, D, G>;
   extern __shared__ __align__(128) unsigned char smem_raw[];
   // swizzled tensor copies want their 1024-byte atoms aligned in the shared window
@@ -712,7 +745,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
         const int new_phys = __shfl_sync(0xffffffffu, phys, new_lane >= 0 ? new_lane : 0);
         const int new_rows = __shfl_sync(0xffffffffu, rows, new_lane >= 0 ? new_lane : 0);
         // tensor-map copies move whole 16-row boxes; the new row rides beside them
-        int bytes = valid ? 2 * (kMma ? kBlockSize : rows) * D * (int)sizeof(T) : 0;
+        int bytes = valid ? 2 * ((kMma && !kFp8) ? kBlockSize : rows) * D * PC::kElemBytes : 0;
         if (kMma && new_here) bytes += 2 * D * (int)sizeof(T);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
@@ -741,7 +774,15 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
         }
         __syncwarp();
         unsigned char* stage = smem + PC::kOffKV + slot * PC::kStageBytes;
-        if (kMma && valid) {
+        if (kFp8 && valid) {
+          // the block's valid code rows, one contiguous run per K and V
+          const size_t src = ((size_t)phys * a.Hkv + kvh) * PC::kBlockBytes;
+          const uint32_t nbytes = (uint32_t)(rows * D);
+          bulk_copy_g2s(stage + lane * PC::kBlockBytes,
+                        static_cast<const unsigned char*>(a.k_cache) + src, nbytes, &full[slot]);
+          bulk_copy_g2s(stage + (NC + lane) * PC::kBlockBytes,
+                        static_cast<const unsigned char*>(a.v_cache) + src, nbytes, &full[slot]);
+        } else if (kMma && valid) {
           const int y = (phys * a.Hkv + kvh) * kBlockSize;
           const uint32_t kd = smem_addr(stage + lane * PC::kBlockBytes);
           const uint32_t vd = smem_addr(stage + (NC + lane) * PC::kBlockBytes);
@@ -969,7 +1010,38 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
           for (int e = 0; e < C::kEPL; ++e) qf[g][e] *= a.qscale;
       }
     }
-    if (kMma && warp < h.nblk && ((h.flags >> (8 + warp)) & 1)) {
+    if (kFp8 && warp < h.nblk && ((h.flags >> (8 + warp)) & 1)) {
+      // fp8 cache: widen this warp's K and V code block into its fp16 scratch
+      // (the swizzled layout the tensor-core math reads); rows past the
+      // context become zeros (their V must not carry NaN into the sums)
+      const unsigned char* const k8 =
+          smem + PC::kOffKV + slot * PC::kStageBytes + warp * PC::kBlockBytes;
+      const unsigned char* const v8 = k8 + NC * PC::kBlockBytes;
+      unsigned char* const kw = smem + PC::kOffWide + warp * 2 * PC::kWideBytes;
+      unsigned char* const vw = kw + PC::kWideBytes;
+      const int n_valid = min(kBlockSize, h.tok_end - (h.blk0 + warp) * kBlockSize);
+      const int row = lane >> 1, half = lane & 1;   // lane: half of one row's D codes
+#pragma unroll
+      for (int j = 0; j < D / 32; ++j) {
+        const int col = half * (D / 2) + 16 * j;     // first code of this 16-byte load
+        uint4 kq = make_uint4(0u, 0u, 0u, 0u), vq = make_uint4(0u, 0u, 0u, 0u);
+        if (row < n_valid) {
+          kq = *reinterpret_cast<const uint4*>(k8 + row * D + col);
+          vq = *reinterpret_cast<const uint4*>(v8 + row * D + col);
+        }
+        uint4 lo, hi;
+        widen_e4m3x16(kq, lo, hi);
+        *reinterpret_cast<uint4*>(kw + blk_chunk(row, col / 8)) = lo;
+        *reinterpret_cast<uint4*>(kw + blk_chunk(row, col / 8 + 1)) = hi;
+        widen_e4m3x16(vq, lo, hi);
+        *reinterpret_cast<uint4*>(vw + blk_chunk(row, col / 8)) = lo;
+        *reinterpret_cast<uint4*>(vw + blk_chunk(row, col / 8 + 1)) = hi;
+      }
+      __syncwarp();
+      if constexpr (kFp8)
+        attend_block_mma<T, D, false, false>(smem_addr(kw), smem_addr(vw), n_valid, a.qscale, tq,
+                                             tq, tm, tl, to, lane, 0, tlim);
+    } else if (kMma && warp < h.nblk && ((h.flags >> (8 + warp)) & 1)) {
       unsigned char* const kb = smem + PC::kOffKV + slot * PC::kStageBytes + warp * PC::kBlockBytes;
       unsigned char* const vb = kb + NC * PC::kBlockBytes;
       const int n_valid = min(kBlockSize, h.tok_end - (h.blk0 + warp) * kBlockSize);
@@ -1062,8 +1134,12 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
     float* const pm = pm_buf + parity * NC * kSl;
     float* const pl = pl_buf + parity * NC * kSl;
     unsigned char* const last_stage = smem + PC::kOffKV + slot * PC::kStageBytes;
-    auto po_of = [&](int w) -> float* {
-      return reinterpret_cast<float*>(last_stage + w * PC::kBlockBytes);
+    // o row of slot g of warp w: its K block area holds the first
+    // kPoRowsPerBlock rows, its V block area the rest
+    auto po_row = [&](int w, int g) -> float* {
+      constexpr int kPer = PC::kPoRowsPerBlock;
+      const int area = g < kPer ? w : NC + w;
+      return reinterpret_cast<float*>(last_stage + area * PC::kBlockBytes) + (g % kPer) * D;
     };
     parity ^= 1;
     if constexpr (kMma) {
@@ -1080,8 +1156,8 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
         if (g < nslots) {
 #pragma unroll
           for (int i = 0; i < (kMma ? D / 16 : 1); ++i) {
-            po_of(warp)[g * D + 16 * i + r] = to[i][j];
-            po_of(warp)[g * D + 16 * i + r + 8] = to[i][2 + j];
+            po_row(warp, g)[16 * i + r] = to[i][j];
+            po_row(warp, g)[16 * i + r + 8] = to[i][2 + j];
           }
           if (r == 0) {
             pm[warp * kSl + g] = tm[j];
@@ -1107,7 +1183,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
         for (int i = 0; i < C::kPPL; ++i)
 #pragma unroll
           for (int e = 0; e < C::kChunk; ++e)
-            po_of(warp)[g * D + (c + 8 * i) * C::kChunk + e] = o[g][i * C::kChunk + e];
+            po_row(warp, g)[(c + 8 * i) * C::kChunk + e] = o[g][i * C::kChunk + e];
         if (c == 0) {
           pm[warp * kSl + g] = m[g];
           pl[warp * kSl + g] = l[g];
@@ -1133,13 +1209,20 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
         const float lw = pl[w * kSl + g];
         if (lw > 0.f) {
           const float wt = exp2f(pm[w * kSl + g] - M);
-          const float4 v = *reinterpret_cast<const float4*>(po_of(w) + g * D + e);
+          const float4 v = *reinterpret_cast<const float4*>(po_row(w, g) + e);
           L = fmaf(wt, lw, L);
           O.x = fmaf(wt, v.x, O.x);
           O.y = fmaf(wt, v.y, O.y);
           O.z = fmaf(wt, v.z, O.z);
           O.w = fmaf(wt, v.w, O.w);
         }
+      }
+      if constexpr (kFp8) {
+        // the V scale of the e4m3 cache (the K scale is in qscale)
+        O.x *= a.v_scale;
+        O.y *= a.v_scale;
+        O.z *= a.v_scale;
+        O.w *= a.v_scale;
       }
       const int hq = h.kvh * G + g % G;
       const size_t qrow = kMulti ? (size_t)h.q0 + g / G : (size_t)h.b;   // row of q / out
@@ -1321,15 +1404,16 @@ __global__ void __launch_bounds__(kMergeWarps * 32) paged_decode_merge_kernel(co
 
 // Resident CTAs per SM of an attention-kernel instantiation (queried once per
 // device, after raising its dynamic shared-memory limit).
-template <typename T, int D, int G, int NC, int S, bool kRope, bool kMma, bool kMulti>
+template <typename T, int D, int G, int NC, int S, bool kRope, bool kMma, bool kMulti,
+          bool kFp8 = false>
 int attention_ctas_per_sm() {
-  using PC = PersistCfg<T, D, G, NC, S, kRope, kMma, kMulti>;
+  using PC = PersistCfg<T, D, G, NC, S, kRope, kMma, kMulti, kFp8>;
   constexpr int kMaxDev = 64;
   static int cache[kMaxDev];  // 0 = not yet queried
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
   if (cache[dev] > 0) return cache[dev];
-  auto kern = paged_decode_attention_kernel<T, D, G, NC, S, kRope, kMma, kMulti>;
+  auto kern = paged_decode_attention_kernel<T, D, G, NC, S, kRope, kMma, kMulti, kFp8>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PC::kSmemBytes) !=
       cudaSuccess)
     return 0;
@@ -1369,13 +1453,14 @@ constexpr int stages_for(int nc) {
 #define PHOTON_MMA_MIN_G 2
 #endif
 
-template <typename T, int D, int G, int NC, int S, bool kRope, bool kMma, bool kMulti = false>
+template <typename T, int D, int G, int NC, int S, bool kRope, bool kMma, bool kMulti = false,
+          bool kFp8 = false>
 cudaError_t launch_attention(const DecodeArgs& a, const CUtensorMap& tk, const CUtensorMap& tv,
                              cudaStream_t stream) {
-  using PC = PersistCfg<T, D, G, NC, S, kRope, kMma, kMulti>;
-  const int per_sm = attention_ctas_per_sm<T, D, G, NC, S, kRope, kMma, kMulti>();
+  using PC = PersistCfg<T, D, G, NC, S, kRope, kMma, kMulti, kFp8>;
+  const int per_sm = attention_ctas_per_sm<T, D, G, NC, S, kRope, kMma, kMulti, kFp8>();
   if (per_sm <= 0) return cudaErrorInvalidConfiguration;
-  return launch_pdl(paged_decode_attention_kernel<T, D, G, NC, S, kRope, kMma, kMulti>,
+  return launch_pdl(paged_decode_attention_kernel<T, D, G, NC, S, kRope, kMma, kMulti, kFp8>,
                     dim3(per_sm * a.num_sms), dim3(PC::kThreads), PC::kSmemBytes, stream, a, tk,
                     tv);
 }
@@ -1430,6 +1515,45 @@ cudaError_t launch_decode_impl(const DecodeArgs& a0, cudaStream_t stream) {
   if (err != cudaSuccess) return err;
   if (a.ev_stop) cudaEventRecord(a.ev_stop, stream);
   return cudaSuccess;
+}
+
+// The e4m3 cache: stages of 4 fp8 blocks per K and V (8 KB at d = 64, 16 KB at
+// d = 128) in a 64 KB ring, which leaves room for the consumers' fp16
+// scratch at two CTAs per SM.
+constexpr int kRingBytesFp8 = 64 * 1024;
+
+template <int D, int G>
+cudaError_t launch_decode_fp8_impl(const DecodeArgs& a, cudaStream_t stream) {
+  constexpr int NC = PHOTON_CONSUMER_WARPS;
+  constexpr int kStage = 2 * NC * kBlockSize * D;
+  constexpr int S = kRingBytesFp8 / kStage < 2 ? 2 : kRingBytesFp8 / kStage;
+  if (!a.q || !a.k_cache || !a.v_cache || !a.block_tables || !a.context_lens || !a.out ||
+      !a.ws_m || !a.ws_l || !a.ws_o || !a.ws_ctrl || !a.err || a.k_new || a.rope_cs ||
+      a.query_start)
+    return cudaErrorInvalidValue;
+  CUtensorMap unused;
+  memset(&unused, 0, sizeof(unused));
+  if (a.ev_start) cudaEventRecord(a.ev_start, stream);
+  cudaError_t err = launch_attention<__half, D, G, NC, S, false, true, false, true>(
+      a, unused, unused, stream);
+  if (err != cudaSuccess) return err;
+  err = launch_pdl(paged_decode_merge_kernel<__half, D>,
+                   dim3((a.B * a.Hq + kMergeWarps - 1) / kMergeWarps), dim3(kMergeWarps * 32), 0,
+                   stream, a);
+  if (err != cudaSuccess) return err;
+  if (a.ev_stop) cudaEventRecord(a.ev_stop, stream);
+  return cudaSuccess;
+}
+
+template <int D>
+cudaError_t launch_decode_fp8_d(const DecodeArgs& a, cudaStream_t stream) {
+  switch (a.Hq / a.Hkv) {
+    case 1: return launch_decode_fp8_impl<D, 1>(a, stream);
+    case 2: return launch_decode_fp8_impl<D, 2>(a, stream);
+    case 4: return launch_decode_fp8_impl<D, 4>(a, stream);
+    case 8: return launch_decode_fp8_impl<D, 8>(a, stream);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 template <typename T, int D>

@@ -5,6 +5,13 @@ namespace photon {
 cudaError_t launch_paged_decode_f16(const DecodeArgs& a, cudaStream_t stream) {
   return launch_decode_t<__half>(a, stream);
 }
+cudaError_t launch_paged_decode_fp8(const DecodeArgs& a, cudaStream_t stream) {
+  switch (a.D) {
+    case 64: return launch_decode_fp8_d<64>(a, stream);
+    case 128: return launch_decode_fp8_d<128>(a, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
 }  // namespace photon
 
 #ifdef PHOTON_PROBE

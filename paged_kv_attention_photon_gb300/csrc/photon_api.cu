@@ -70,9 +70,11 @@ photon_status_t check_shape(const photon_paged_shape_t* s) {
   return PHOTON_OK;
 }
 
-int partition_of(const photon_paged_shape_t* s) {
+// kv_bytes: bytes per cached element (0: the shape's dtype; 1: an e4m3 cache)
+int partition_of(const photon_paged_shape_t* s, int kv_bytes = 0) {
   if (s->partition_size) return s->partition_size;
-  const int per_token = 2 * s->head_dim * (int)elem_bytes(s->dtype);  // K + V bytes
+  const int eb = kv_bytes > 0 ? kv_bytes : (int)elem_bytes(s->dtype);
+  const int per_token = 2 * s->head_dim * eb;  // K + V bytes
   int part = kItemBytes / per_token / s->block_size * s->block_size;
   // A small batch has too few such items to keep the grid busy, and one
   // item's latency then sets the call's time: shrink the partition so that
@@ -89,9 +91,9 @@ int partition_of(const photon_paged_shape_t* s) {
   return part;
 }
 
-int max_partitions_of(const photon_paged_shape_t* s) {
+int max_partitions_of(const photon_paged_shape_t* s, int kv_bytes = 0) {
   const int64_t span = (int64_t)s->max_blocks_per_seq * s->block_size;
-  const int part = partition_of(s);
+  const int part = partition_of(s, kv_bytes);
   return (int)((span + part - 1) / part);
 }
 
@@ -102,10 +104,11 @@ struct WorkspaceLayout {
   size_t off_ctrl, off_m, off_l, off_o, total;
 };
 
-WorkspaceLayout layout_of(const photon_paged_shape_t* s, int64_t query_rows = -1) {
+WorkspaceLayout layout_of(const photon_paged_shape_t* s, int64_t query_rows = -1,
+                          int kv_bytes = 0) {
   WorkspaceLayout w{};
   if (query_rows < 0) query_rows = s->num_seqs;
-  const size_t pairs = (size_t)query_rows * (size_t)max_partitions_of(s);
+  const size_t pairs = (size_t)query_rows * (size_t)max_partitions_of(s, kv_bytes);
   const size_t rows = pairs * s->num_q_heads;
   w.off_ctrl = 0;
   w.off_m = 256;
@@ -201,6 +204,48 @@ size_t photon_paged_decode_workspace_size(const photon_paged_shape_t* shape) {
   return layout_of(shape).total;
 }
 
+photon_status_t photon_cache_write_fp8(const void* k, const void* v,
+                                       const int64_t* slot_mapping, int32_t num_tokens,
+                                       void* k_cache, void* v_cache, float k_scale,
+                                       float v_scale, const photon_paged_shape_t* shape,
+                                       photon_stream_t stream) {
+  photon_status_t st = check_shape(shape);
+  if (st != PHOTON_OK) return st;
+  if (shape->dtype != PHOTON_F16) return PHOTON_ERR_UNSUPPORTED;
+  if (!(k_scale > 0.f) || !(v_scale > 0.f) || !std::isfinite(k_scale) || !std::isfinite(v_scale))
+    return PHOTON_ERR_INVALID_ARG;
+  if (num_tokens < 0) return PHOTON_ERR_INVALID_ARG;
+  if (num_tokens == 0) return PHOTON_OK;
+  if (!k || !v || !slot_mapping || !k_cache || !v_cache) return PHOTON_ERR_INVALID_ARG;
+  if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache) ||
+      (reinterpret_cast<uintptr_t>(slot_mapping) & 7u))
+    return PHOTON_ERR_MISALIGNED;
+  uint32_t* err = nullptr;
+  if ((st = error_word(&err)) != PHOTON_OK) return st;
+  photon::CacheWriteFp8Args a{};
+  a.k = k;
+  a.v = v;
+  a.slot_mapping = slot_mapping;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.err = err;
+  a.k_inv = 1.0f / k_scale;   // fp32 reciprocal, then an fp32 product per element
+  a.v_inv = 1.0f / v_scale;
+  a.T = num_tokens;
+  a.Hkv = shape->num_kv_heads;
+  a.D = shape->head_dim;
+  a.block_size = shape->block_size;
+  a.NB = shape->num_blocks;
+  return photon::launch_cache_write_fp8(a, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? PHOTON_OK
+             : PHOTON_ERR_CUDA;
+}
+
+size_t photon_paged_decode_fp8_workspace_size(const photon_paged_shape_t* shape) {
+  if (check_shape(shape) != PHOTON_OK || shape->dtype != PHOTON_F16) return 0;
+  return layout_of(shape, -1, 1).total;
+}
+
 photon_status_t photon_paged_decode_plan(const photon_paged_shape_t* shape,
                                          int32_t* partition_size, int32_t* max_partitions,
                                          int32_t* attention_ctas, int32_t* kernels_per_call) {
@@ -234,17 +279,26 @@ photon_status_t decode_common(const void* q, const void* k_cache, const void* v_
                               const int64_t* slot_mapping, const void* rope_cos_sin,
                               int32_t rope_max_positions,
                               const int32_t* query_start = nullptr, int32_t num_tokens = 0,
-                              int32_t max_query_len = 0) {
+                              int32_t max_query_len = 0, bool fp8 = false, float k_scale = 1.f,
+                              float v_scale = 1.f) {
   photon_status_t st = check_shape(shape);
   if (st != PHOTON_OK) return st;
   if (!std::isfinite(scale)) return PHOTON_ERR_INVALID_ARG;
+  if (fp8) {
+    // e4m3 K/V, fp16 q and out; the scales turn codes into values
+    if (shape->dtype != PHOTON_F16) return PHOTON_ERR_UNSUPPORTED;
+    if (!(k_scale > 0.f) || !(v_scale > 0.f) || !std::isfinite(k_scale) ||
+        !std::isfinite(v_scale))
+      return PHOTON_ERR_INVALID_ARG;
+  }
   if (shape->num_seqs == 0) return PHOTON_OK;
   if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
     return PHOTON_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(block_tables) ||
       !aligned16(context_lens) || !aligned16(out))
     return PHOTON_ERR_MISALIGNED;
-  const WorkspaceLayout wl = layout_of(shape, query_start ? (int64_t)num_tokens : -1);
+  const int kv_bytes = fp8 ? 1 : 0;
+  const WorkspaceLayout wl = layout_of(shape, query_start ? (int64_t)num_tokens : -1, kv_bytes);
   if (wl.total > 0) {
     if (!workspace || workspace_bytes < wl.total) return PHOTON_ERR_WORKSPACE;
     if (!aligned16(workspace)) return PHOTON_ERR_MISALIGNED;
@@ -275,15 +329,17 @@ photon_status_t decode_common(const void* q, const void* k_cache, const void* v_
   a.rope_cs = static_cast<const float2*>(rope_cos_sin);
   a.rope_max_pos = rope_cos_sin ? rope_max_positions : 0;
   a.err = err;
-  a.qscale = (float)((double)scale * 1.4426950408889634);  // scale * log2(e)
+  // scale * log2(e) (times the K scale of an e4m3 cache)
+  a.qscale = (float)((double)scale * (double)k_scale * 1.4426950408889634);
+  a.v_scale = v_scale;
   a.B = shape->num_seqs;
   a.Hq = shape->num_q_heads;
   a.Hkv = shape->num_kv_heads;
   a.D = shape->head_dim;
   a.NB = shape->num_blocks;
   a.MBS = shape->max_blocks_per_seq;
-  a.part = partition_of(shape);
-  a.pmax = max_partitions_of(shape);
+  a.part = partition_of(shape, kv_bytes);
+  a.pmax = max_partitions_of(shape, kv_bytes);
   a.query_start = query_start;
   a.num_tokens = num_tokens;
   a.max_q = max_query_len;
@@ -293,6 +349,10 @@ photon_status_t decode_common(const void* q, const void* k_cache, const void* v_
 
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
+  if (fp8) {
+    e = photon::launch_paged_decode_fp8(a, s);
+    return e == cudaSuccess ? PHOTON_OK : PHOTON_ERR_CUDA;
+  }
   switch (shape->dtype) {
     case PHOTON_F32: e = photon::launch_paged_decode_f32(a, s); break;
     case PHOTON_F16: e = photon::launch_paged_decode_f16(a, s); break;
@@ -312,6 +372,17 @@ photon_status_t photon_paged_decode(const void* q, const void* k_cache, const vo
                                     photon_stream_t stream) {
   return decode_common(q, k_cache, v_cache, block_tables, context_lens, scale, out, workspace,
                        workspace_bytes, shape, stream, nullptr, nullptr, nullptr, nullptr, 0);
+}
+
+photon_status_t photon_paged_decode_fp8(const void* q, const void* k_cache, const void* v_cache,
+                                        const int32_t* block_tables, const int32_t* context_lens,
+                                        float scale, float k_scale, float v_scale, void* out,
+                                        void* workspace, size_t workspace_bytes,
+                                        const photon_paged_shape_t* shape,
+                                        photon_stream_t stream) {
+  return decode_common(q, k_cache, v_cache, block_tables, context_lens, scale, out, workspace,
+                       workspace_bytes, shape, stream, nullptr, nullptr, nullptr, nullptr, 0,
+                       nullptr, 0, 0, true, k_scale, v_scale);
 }
 
 photon_status_t photon_paged_decode_step(const void* k_new, const void* v_new,

@@ -139,6 +139,7 @@ struct DecodeArgs {
   int max_q, num_tokens;
   uint32_t* err;      // sticky device error word
   float qscale;       // scale * log2(e): scores are kept in the log2 domain
+  float v_scale;      // e4m3 cache only: the V scale (applied in each item's combine)
   int B, Hq, Hkv, D, NB, MBS, part, pmax;
   int num_sms;        // SMs of the current device
   cudaEvent_t ev_start, ev_stop;  // optional timing hook around the decode kernels
@@ -153,6 +154,21 @@ struct CacheWriteArgs {
   uint32_t* err;
   int T, Hkv, row_bytes, block_size, NB;
 };
+
+// Quantising cache write into an e4m3 cache: row t of k / v (fp16) is stored
+// at slot_mapping[t] as the codes of x * inv_scale (fp32 product, round to
+// nearest even, saturating at +-448).
+struct CacheWriteFp8Args {
+  const void* k;
+  const void* v;
+  const int64_t* slot_mapping;
+  void* k_cache;
+  void* v_cache;
+  uint32_t* err;
+  float k_inv, v_inv;
+  int T, Hkv, D, block_size, NB;
+};
+cudaError_t launch_cache_write_fp8(const CacheWriteFp8Args& a, cudaStream_t stream);
 
 struct GatherArgs {
   const void* k_cache;
@@ -178,6 +194,9 @@ extern std::atomic<int> g_decode_consumer;
 
 cudaError_t launch_paged_decode_f32(const DecodeArgs& a, cudaStream_t stream);
 cudaError_t launch_paged_decode_f16(const DecodeArgs& a, cudaStream_t stream);
+// e4m3 K/V cache, fp16 q and out (photon_paged_decode_fp8): a.qscale holds
+// scale * k_scale * log2(e), a.v_scale the V scale.
+cudaError_t launch_paged_decode_fp8(const DecodeArgs& a, cudaStream_t stream);
 cudaError_t launch_paged_decode_bf16(const DecodeArgs& a, cudaStream_t stream);
 
 // Multi-query (causal) paged attention: query_start[b] .. query_start[b+1]-1

@@ -82,6 +82,37 @@ def test_cache_write_validation(lib):
     assert f(FAKE, FAKE, FAKE, 4, FAKE, FAKE, ctypes.byref(_shape(head_dim=80)), None) == 2
 
 
+def test_fp8_validation(lib):
+    s = _shape()
+    w = lib.photon_cache_write_fp8
+    assert w(FAKE, FAKE, FAKE, 0, FAKE, FAKE, 0.5, 0.5, ctypes.byref(s), None) == 0   # no rows
+    assert w(FAKE, FAKE, FAKE, -1, FAKE, FAKE, 0.5, 0.5, ctypes.byref(s), None) == 1
+    assert w(FAKE, FAKE, FAKE, 4, FAKE, FAKE, 0.0, 0.5, ctypes.byref(s), None) == 1
+    assert w(FAKE, FAKE, FAKE, 4, FAKE, FAKE, 0.5, math.nan, ctypes.byref(s), None) == 1
+    assert w(FAKE, FAKE, FAKE, 4, FAKE, FAKE, 0.5, -1.0, ctypes.byref(s), None) == 1
+    assert w(FAKE, FAKE, FAKE, 4, FAKE + 8, FAKE, 0.5, 0.5, ctypes.byref(s), None) == 3
+    assert w(FAKE, FAKE, FAKE, 4, FAKE, FAKE, 0.5, 0.5,
+             ctypes.byref(_shape(dtype=P.BF16)), None) == 2          # fp16 rows only
+    d = lib.photon_paged_decode_fp8
+
+    def dec(shape, *, q=FAKE, ks=0.5, vs=0.5, ws_bytes=1 << 40, scale=0.1):
+        return d(q, FAKE, FAKE, FAKE, FAKE, scale, ks, vs, FAKE2, FAKE2, ws_bytes,
+                 ctypes.byref(shape), None)
+    assert dec(_shape(dtype=P.F32)) == 2
+    assert dec(_shape(dtype=P.BF16)) == 2
+    assert dec(s, ks=0.0) == 1
+    assert dec(s, vs=math.inf) == 1
+    assert dec(s, scale=math.nan) == 1
+    assert dec(s, q=None) == 1
+    assert dec(s, ws_bytes=16) == 4
+    assert dec(_shape(num_seqs=0)) == 0
+    # fp8 partitions hold twice the tokens: half the fp16 decode's partials
+    big = _shape(num_seqs=64, max_blocks_per_seq=512)
+    assert 2 * lib.photon_paged_decode_fp8_workspace_size(ctypes.byref(big)) \
+        <= lib.photon_paged_decode_workspace_size(ctypes.byref(big)) + 1024
+    assert lib.photon_paged_decode_fp8_workspace_size(ctypes.byref(_shape(dtype=P.BF16))) == 0
+
+
 def test_gather_validation(lib):
     s = _shape()
     f = lib.photon_paged_gather
