@@ -69,6 +69,8 @@ def parse():
                     help="profiling aid: run only this multi-query case (default kernel "
                          "choice, --steps calls) and print its timing")
     ap.add_argument("--no-fp8", action="store_true", help="skip the e4m3-cache decode line")
+    ap.add_argument("--fp8-case", default="", choices=["", "qwen_b64", "qwen_b64_pool10k"],
+                    help="profiling aid: run only the e4m3-cache decode on this workload")
     ap.add_argument("--no-configs", action="store_true",
                     help="skip the side measurements of the other decode configurations")
     ap.add_argument("--decode-consumer", type=int, default=0, choices=[0, 1, 2],
@@ -211,12 +213,12 @@ def multi_query_side(P, torch, stream, flush_l2, K, hbm_peak, only: str = "",
     return res
 
 
-def fp8_side(P, torch, stream, flush_l2, K, peak):
+def fp8_side(P, torch, stream, flush_l2, K, peak, workload: str = "qwen_b64"):
     """The same batch-64 long-context decode over an e4m3 K/V cache
     (photon_paged_decode_fp8): the codes of the synthetic fp8 pools, fp16 q
     and out.  Algorithmic bytes as the fp16 decode's with one byte per cached
     element."""
-    wl = W.qwen_b64()
+    wl = make_workload(workload, 0)
     k8, v8 = W.fp8_cache(wl, 2)
     shape = P.PagedShape.make(**wl.shape_dict())
 
@@ -253,7 +255,7 @@ def fp8_side(P, torch, stream, flush_l2, K, peak):
               + 2 * wl.num_seqs * wl.num_q_heads * wl.head_dim * 2
               + 4 * int(((ctx + 15) // 16).sum()) + 4 * wl.num_seqs)
     gbs = nbytes / (ms / 1e3) / 1e9
-    return {"workload": "qwen_b64 with an e4m3 K/V cache (k_scale 0.5, v_scale 0.25)",
+    return {"workload": f"{workload} with an e4m3 K/V cache (k_scale 0.5, v_scale 0.25)",
             "ms_per_call": round(ms, 5), "algorithmic_bytes": int(nbytes),
             "GBps": round(gbs, 1), "hbm_fraction": round(gbs / peak, 4),
             "tokens_attended_per_s": round(wl.tokens_attended() / (ms / 1e3), 1),
@@ -875,12 +877,32 @@ def run_mq_case(args):
     return 0
 
 
+def run_fp8_case(args):
+    """Only the e4m3-cache decode (profiling aid)."""
+    import torch
+    import paged_kv_attention_photon_gb300 as P
+    torch.cuda.set_device(0)
+    P.build()
+    flush_w = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+
+    def flush_l2():
+        flush_w.zero_()
+
+    peak, _ = measured_peaks()
+    res = fp8_side(P, torch, torch.cuda.current_stream(), flush_l2, args.steps,
+                   peak or FALLBACK_HBM_GBS, workload=args.fp8_case)
+    print(json.dumps(res), flush=True)
+    return 0
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         return run_reference(args)
     if args.mq_case:
         return run_mq_case(args)
+    if args.fp8_case:
+        return run_fp8_case(args)
     return run_ours(args)
 
 

@@ -1020,10 +1020,16 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
       unsigned char* const kw = smem + PC::kOffWide + warp * 2 * PC::kWideBytes;
       unsigned char* const vw = kw + PC::kWideBytes;
       const int n_valid = min(kBlockSize, h.tok_end - (h.blk0 + warp) * kBlockSize);
-      const int row = lane >> 1, half = lane & 1;   // lane: half of one row's D codes
+      // lane: row lane / 2, and in every group of 32 codes of that row the 16
+      // at 16 * (lane % 2); step j takes group jj, rotated by the row (and
+      // the lane's half at d = 128) so that the eight lanes of each quarter
+      // warp hit eight different bank groups with their 16-byte loads and
+      // with both scratch stores
+      const int row = lane >> 1, half = lane & 1;
 #pragma unroll
       for (int j = 0; j < D / 32; ++j) {
-        const int col = half * (D / 2) + 16 * j;     // first code of this 16-byte load
+        const int jj = D == 128 ? (j + row + half) & 3 : (j + (row >> 1)) & 1;
+        const int col = 32 * jj + 16 * half;         // first code of this 16-byte load
         uint4 kq = make_uint4(0u, 0u, 0u, 0u), vq = make_uint4(0u, 0u, 0u, 0u);
         if (row < n_valid) {
           kq = *reinterpret_cast<const uint4*>(k8 + row * D + col);
