@@ -3,7 +3,6 @@ run out on purpose (a barrier phase nothing completes), the kernel reports it
 through device error bit 8 and returns, and the context keeps working."""
 import time
 
-import numpy as np
 import pytest
 import torch
 

@@ -11,7 +11,6 @@ every other test when it gets here; it also passes alone in a fresh process.
 """
 import ctypes
 
-import numpy as np
 import pytest
 import torch
 
