@@ -58,6 +58,14 @@ class Scheduler:
         self._tables = np.full((max_seqs, max_blocks_per_seq), -1, np.int32)
         self._slots = np.zeros(max_step_tokens, np.int64)
         self._fin = np.zeros(max_seqs, np.int64)
+        # the buffers never move: their addresses, and the result structs, once
+        self._out_ptrs = tuple(_p(a) for a in (self._ids, self._qlen, self._ctx, self._tables,
+                                               self._slots))
+        self._fin_ptr = _p(self._fin)
+        self._res = ScheduleResult()
+        self._res_ref = ctypes.byref(self._res)
+        self._nf = ctypes.c_int32(0)
+        self._nf_ref = ctypes.byref(self._nf)
 
     def close(self) -> None:
         if getattr(self, "_h", None) is not None and self._h.value:
@@ -81,10 +89,9 @@ class Scheduler:
                     "photon_scheduler_add_request")
 
     def schedule(self) -> Dict[str, object]:
-        res = ScheduleResult()
-        self._check(self._lib.photon_scheduler_schedule(
-            self._h, _p(self._ids), _p(self._qlen), _p(self._ctx), _p(self._tables),
-            _p(self._slots), ctypes.byref(res)), "photon_scheduler_schedule")
+        res = self._res
+        self._check(self._lib.photon_scheduler_schedule(self._h, *self._out_ptrs, self._res_ref),
+                    "photon_scheduler_schedule")
         n, t = res.num_rows, res.num_tokens
         return {"request_ids": self._ids[:n], "query_lens": self._qlen[:n],
                 "context_lens": self._ctx[:n], "block_tables": self._tables[:n],
@@ -93,12 +100,11 @@ class Scheduler:
                 "num_preempted": res.num_preempted, "free_blocks": res.free_blocks}
 
     def update(self, stop: Optional[np.ndarray] = None) -> np.ndarray:
-        nf = ctypes.c_int32(0)
         stop_arr = None if stop is None else np.ascontiguousarray(stop, np.uint8)
         self._check(self._lib.photon_scheduler_update(
-            self._h, None if stop_arr is None else _p(stop_arr), _p(self._fin),
-            ctypes.byref(nf)), "photon_scheduler_update")
-        return self._fin[:nf.value].copy()
+            self._h, None if stop_arr is None else _p(stop_arr), self._fin_ptr, self._nf_ref),
+            "photon_scheduler_update")
+        return self._fin[:self._nf.value].copy()
 
     def stats(self) -> Dict[str, int]:
         v = [ctypes.c_int32(0) for _ in range(4)]
