@@ -676,3 +676,16 @@ def test_fp8_decode_equals_brute_force_on_dequantised_values():
             w = np.exp(s_ - s_.max())
             want = (w[:, None] * V).sum(0) / w.sum()
             assert np.abs(got[b, h] - want).max() <= 1e-12
+
+
+def test_fp8_pools_hold_finite_codes_only_where_tables_point():
+    wl = W.random_small(63, batch=5, num_q_heads=8, num_kv_heads=2, head_dim=64, max_ctx=90,
+                        dtype=W.DTYPE_F16, extra_blocks=4)
+    k8, v8 = W.fp8_cache(wl, 9)
+    used = np.zeros(wl.num_blocks, bool)
+    used[wl.block_tables[wl.block_tables >= 0]] = True
+    for pool in (k8, v8):
+        assert (pool[~used] == W.E4M3_NAN).all()                  # the stray-read detector
+        vals = np.abs(oracle.e4m3_decode(pool[used]))
+        assert np.isfinite(vals).all() and vals.min() >= 0.25 and vals.max() <= 3.75
+    assert not np.array_equal(k8, v8)
