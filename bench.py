@@ -520,6 +520,13 @@ def cpu_baseline(wl: W.Workload, budget_s: float = 20.0):
                       f"cache write + decode, fp64, {threads} threads, one run of {dt:.2f} s"}
 
 
+def workload_config(wl: W.Workload) -> dict:
+    """The keys naming the workload, shared by both arms' JSON lines."""
+    return {"workload": wl.name, "batch": wl.num_seqs, "q_heads": wl.num_q_heads,
+            "kv_heads": wl.num_kv_heads, "head_dim": wl.head_dim, "block_size": wl.block_size,
+            "num_blocks": wl.num_blocks, "tokens_attended": wl.tokens_attended()}
+
+
 def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
@@ -544,7 +551,8 @@ def run_reference(args):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.workload, "sample_sequences": n},
+            "config": dict(workload_config(wl), sample_sequences=n,
+                           parallelism="one host process (the oracle on all host cores)"),
             "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": threads,
                              "kind": "oracle", "sample": sample},
             "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -822,10 +830,7 @@ def run_ours(args):
             "steps": K, "warmup": max(3, args.warmup), "ms_per_step": round(ms_max, 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": W.DTYPE_NAMES[wl.dtype], "data": "synthetic",
-            "config": {"workload": wl.name, "batch": wl.num_seqs,
-                       "q_heads": wl.num_q_heads, "kv_heads": wl.num_kv_heads,
-                       "head_dim": wl.head_dim, "block_size": wl.block_size,
-                       "num_blocks": wl.num_blocks, "tokens_attended": wl.tokens_attended(),
+            "config": {**workload_config(wl),
                        "partition_size": plan["partition_size"],
                        "decode_consumer": consumer_name(args.decode_consumer, wl),
                        "l2": "flushed before every step (512 MB write + 256 MB read of another buffer), outside the timed events; step working set 478 MB > L2",
