@@ -7,6 +7,19 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
+# The mutation check (test_oracle_mutations.py) runs the pins against a copy
+# of the oracle package with one planted mistake: this variable names that
+# copy's directory, which is then imported as `oracle` in place of ROOT/oracle.
+_UNDER_TEST = os.environ.get("PHOTON_ORACLE_UNDER_TEST")
+if _UNDER_TEST:
+    import importlib.util
+    _spec = importlib.util.spec_from_file_location(
+        "oracle", os.path.join(_UNDER_TEST, "__init__.py"),
+        submodule_search_locations=[_UNDER_TEST])
+    _mod = importlib.util.module_from_spec(_spec)
+    sys.modules["oracle"] = _mod
+    _spec.loader.exec_module(_mod)
+
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (runs the CUDA library)")

@@ -644,12 +644,23 @@ def test_fp8_cache_write_quantises_each_row_at_its_slot():
                         dtype=W.DTYPE_F16)
     k8, v8 = W.fp8_cache(wl, 5)
     k0, v0 = k8.copy(), v8.copy()
+    # K and V take different scales (0.5 and 0.25), so a swapped or shared
+    # scale, or rows written to the other pool, fails below.  The expected
+    # codes come from torch's float8_e4m3fn conversion (a library routine, not
+    # the oracle's encoder): the scaled fp16 N(0,1) rows stay far inside +-448,
+    # where that conversion rounds to nearest even like the e4m3 definition.
     oracle.cache_write_fp8(wl.k_new, wl.v_new, wl.slot_mapping, k8, v8, 0.5, 0.25,
                            block_size=16)
+
+    def codes(rows, inv_scale):
+        x = torch.from_numpy(rows.astype(np.float32)) * inv_scale
+        assert float(x.abs().max()) < 448
+        return x.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
     for t, slot in enumerate(wl.slot_mapping):
         blk, off = slot // 16, slot % 16
-        want = oracle.e4m3_encode(wl.k_new[t].astype(np.float32) * np.float32(2.0))
-        assert np.array_equal(k8[blk, :, off], want)
+        assert np.array_equal(k8[blk, :, off], codes(wl.k_new[t], 2.0))
+        assert np.array_equal(v8[blk, :, off], codes(wl.v_new[t], 4.0))
         k0[blk, :, off] = k8[blk, :, off]
         v0[blk, :, off] = v8[blk, :, off]
     assert np.array_equal(k0, k8) and np.array_equal(v0, v8)   # nothing else changed

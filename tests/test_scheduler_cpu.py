@@ -134,6 +134,50 @@ def test_library_equals_oracle_on_random_traces(seed, cfg, n_req, stop_p):
     _run_trace(seed, cfg, n_req, steps=20000, stop_p=stop_p)
 
 
+@pytest.mark.parametrize("seed,cfg", [
+    (2, dict(num_blocks=24, block_size=4, max_blocks_per_seq=12, max_seqs=6,
+             max_step_tokens=16)),
+    (5, dict(num_blocks=12, block_size=4, max_blocks_per_seq=10, max_seqs=4,
+             max_step_tokens=6)),
+])
+def test_oracle_invariants_on_tight_random_traces(seed, cfg):
+    """The oracle alone on traces tight enough to preempt: the invariants above,
+    every request finishes and every block comes back, a step that preempts
+    admits nobody (the second phase is skipped in such a step), and service is
+    first come first served across preemptions: after every step each request
+    that holds a running slot arrived before each request still waiting."""
+    trace = W.request_trace(seed, 40, max_prompt=cfg["max_blocks_per_seq"] * cfg["block_size"]
+                            // 2, max_new=cfg["max_blocks_per_seq"] * cfg["block_size"] // 2,
+                            pool_tokens=cfg["num_blocks"] * cfg["block_size"])
+    ora = OracleScheduler(**cfg)
+    held, nxt, preempting_steps = {}, 0, 0
+    for t in range(20000):
+        while nxt < len(trace) and trace[nxt][0] <= t:
+            ora.add_request(*trace[nxt][1:])
+            nxt += 1
+        st = ora.schedule()
+        if st["num_preempted"]:
+            preempting_steps += 1
+            assert st["num_admitted"] == 0, (seed, t)
+        for rid in list(held):
+            if ora.request_state(rid)["blocks"] == 0:
+                del held[rid]
+        _check_invariants(st, cfg, held)
+        order = [tr[1] for tr in trace[:nxt]]                  # arrival order of the ids
+        states = [ora.request_state(rid)["state"] for rid in order]
+        running = [i for i, x in enumerate(states) if x == 1]
+        waiting = [i for i, x in enumerate(states) if x in (0, 2)]
+        if running and waiting:
+            assert max(running) < min(waiting), (seed, t)
+        for rid in ora.update():
+            held.pop(rid, None)
+        s = ora.stats()
+        if nxt == len(trace) and s["running"] == 0 and s["waiting"] == 0:
+            break
+    assert ora.stats() == dict(waiting=0, running=0, finished=40, free_blocks=cfg["num_blocks"])
+    assert preempting_steps > 0
+
+
 def test_tight_pool_preempts():
     cfg = dict(num_blocks=24, block_size=4, max_blocks_per_seq=12, max_seqs=6,
                max_step_tokens=16)
