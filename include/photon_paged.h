@@ -309,6 +309,24 @@ photon_status_t photon_debug_set_multi_query_kernel(int32_t which);
  * PHOTON_ERR_INVALID_ARG for a limit outside the range. */
 photon_status_t photon_debug_wait_probe(uint64_t limit_ns, photon_stream_t stream);
 
+/* Measuring aid: the decode's K/V data movement with no arithmetic.  For each
+ * byte offset in chunk_offsets[0 .. num_chunks) (device memory, int64), the
+ * chunk_bytes bytes at that offset of k_cache and of v_cache are copied into
+ * shared memory with the bulk copies the decode kernel uses, by a persistent
+ * grid of two CTAs per SM that takes runs of chunks_per_run consecutive
+ * offsets round robin; nothing reads the copies.  With the offsets of the
+ * (block, KV head) runs a decode reads, in its order (README "Key features /
+ * GPU-optimized kernels": the batched paged attention's block-table reads),
+ * the call's time is the practical read ceiling of that decode.  chunk_bytes:
+ * 16 .. 4096, a multiple of 16; offsets must be multiples of 16 with
+ * offset + chunk_bytes <= pool_bytes, others are skipped and flagged (device
+ * error bit 1); a bounded wait that runs out sets bit 8.  Nothing is written
+ * to global memory. */
+photon_status_t photon_debug_read_probe(const void* k_cache, const void* v_cache,
+                                       uint64_t pool_bytes, const int64_t* chunk_offsets,
+                                       int64_t num_chunks, int32_t chunk_bytes,
+                                       int32_t chunks_per_run, photon_stream_t stream);
+
 /* photon_paged_decode without a caller-provided workspace.  The pages have no
  * counterpart of this call; it exists for callers that cannot allocate device
  * memory for the decode: an engine that reserved nearly all of HBM for its KV
@@ -322,8 +340,10 @@ photon_status_t photon_debug_wait_probe(uint64_t limit_ns, photon_stream_t strea
  *     photon_paged_decode_workspace_size() exceeds 32 MiB is rejected with
  *     PHOTON_ERR_WORKSPACE before anything is launched;
  *   - the first call made with a given device current looks up the array's
- *     device address for that device (cudaGetSymbolAddress); make that first
- *     call before starting any stream capture;
+ *     device address for that device (cudaGetSymbolAddress) and keeps it for
+ *     the life of the process; make that first call before starting any
+ *     stream capture, and do not use this entry point on a device after a
+ *     cudaDeviceReset of it (the kept address would then be stale);
  *   - every call on a device uses the same array and leaves its last contents
  *     there; nothing in it needs to be cleared between calls, but calls whose
  *     kernels may overlap on the GPU (different streams, no ordering) race on

@@ -31,7 +31,7 @@ __all__ = [
     "photon_paged_multi_query_workspace_size", "photon_debug_set_multi_query_kernel",
     "photon_debug_set_decode_consumer", "photon_cache_write_fp8",
     "photon_paged_decode_fp8_workspace_size", "photon_paged_decode_fp8",
-    "photon_debug_wait_probe", "Scheduler",
+    "photon_debug_wait_probe", "photon_debug_read_probe", "Scheduler",
     "F32", "F16", "BF16", "STATUS",
 ]
 
@@ -109,6 +109,8 @@ def _load() -> ctypes.CDLL:
     lib.photon_paged_multi_query_workspace_size.restype = SZ
     lib.photon_debug_wait_probe.argtypes = [ctypes.c_uint64, P]
     lib.photon_debug_wait_probe.restype = ctypes.c_int
+    lib.photon_debug_read_probe.argtypes = [P, P, ctypes.c_uint64, P, ctypes.c_int64, I32, I32, P]
+    lib.photon_debug_read_probe.restype = ctypes.c_int
     lib.photon_debug_set_multi_query_kernel.argtypes = [I32]
     lib.photon_debug_set_multi_query_kernel.restype = ctypes.c_int
     lib.photon_debug_set_decode_consumer.argtypes = [I32]
@@ -267,6 +269,15 @@ def photon_debug_wait_probe(limit_ns: int, stream=None) -> None:
     """Runs the bounded-wait self-test kernel (sets device error bit 8)."""
     _check(_load().photon_debug_wait_probe(int(limit_ns), _stream(stream)),
            "photon_debug_wait_probe")
+
+
+def photon_debug_read_probe(k_cache, v_cache, pool_bytes: int, chunk_offsets, num_chunks: int,
+                            chunk_bytes: int, chunks_per_run: int, stream=None) -> None:
+    """Copies the K and V chunks at chunk_offsets (device int64 byte offsets)
+    into shared memory and nothing else: the decode's read pattern alone."""
+    _check(_load().photon_debug_read_probe(
+        _ptr(k_cache), _ptr(v_cache), int(pool_bytes), _ptr(chunk_offsets), int(num_chunks),
+        int(chunk_bytes), int(chunks_per_run), _stream(stream)), "photon_debug_read_probe")
 
 
 def photon_debug_set_multi_query_kernel(which: int) -> None:

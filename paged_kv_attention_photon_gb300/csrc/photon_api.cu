@@ -18,6 +18,10 @@
 namespace photon {
 // selftest.cu
 cudaError_t launch_wait_probe(unsigned long long limit_ns, uint32_t* err, cudaStream_t stream);
+// read_probe.cu
+cudaError_t launch_read_probe(const void* k, const void* v, const int64_t* offs, int64_t n,
+                              uint32_t chunk_bytes, int run, uint64_t pool_bytes, int num_sms,
+                              uint32_t* err, cudaStream_t stream);
 std::atomic<int> g_decode_consumer{0};
 }  // namespace photon
 
@@ -639,6 +643,29 @@ photon_status_t photon_debug_wait_probe(uint64_t limit_ns, photon_stream_t strea
   if (st != PHOTON_OK) return st;
   return photon::launch_wait_probe(limit_ns, err, reinterpret_cast<cudaStream_t>(stream)) ==
                  cudaSuccess
+             ? PHOTON_OK
+             : PHOTON_ERR_CUDA;
+}
+
+photon_status_t photon_debug_read_probe(const void* k_cache, const void* v_cache,
+                                       uint64_t pool_bytes, const int64_t* chunk_offsets,
+                                       int64_t num_chunks, int32_t chunk_bytes,
+                                       int32_t chunks_per_run, photon_stream_t stream) {
+  if (num_chunks < 0 || chunk_bytes <= 0 || chunk_bytes > 4096 || chunk_bytes % 16 != 0 ||
+      chunks_per_run <= 0)
+    return PHOTON_ERR_INVALID_ARG;
+  if (num_chunks == 0) return PHOTON_OK;
+  if (!k_cache || !v_cache || !chunk_offsets) return PHOTON_ERR_INVALID_ARG;
+  if (!aligned16(k_cache) || !aligned16(v_cache) || !aligned16(chunk_offsets))
+    return PHOTON_ERR_MISALIGNED;
+  uint32_t* err = nullptr;
+  photon_status_t st = error_word(&err);
+  if (st != PHOTON_OK) return st;
+  int sms = 0;
+  if ((st = num_sms(&sms)) != PHOTON_OK) return st;
+  return photon::launch_read_probe(k_cache, v_cache, chunk_offsets, num_chunks,
+                                   (uint32_t)chunk_bytes, chunks_per_run, pool_bytes, sms, err,
+                                   reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
              ? PHOTON_OK
              : PHOTON_ERR_CUDA;
 }

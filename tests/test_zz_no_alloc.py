@@ -4,8 +4,12 @@ photon_paged_decode_noalloc serves callers that cannot allocate device memory
 for the decode (an engine that reserved nearly all of HBM for its KV pool, a
 plugin with no allocator, a path that must not call cudaMalloc); it takes its
 split-KV scratch from a 32 MiB array built into the library.  Its output must
-match photon_paged_decode's, within the tolerance the other decode tests use,
-on two calls in a row (the second finds the scratch as the first left it).
+match photon_paged_decode's, and the fp64 oracle's, within the tolerance the
+other decode tests use, on two calls in a row (the second finds the scratch as
+the first left it), on both attention consumers.  The first call of the file
+finds the array as the process loaded it, zero and without the guard word the
+merge kernel leaves, so it takes the fixed work order; the calls after it take
+the dynamic queue.
 This file is collected last so that a stop-at-first-failure run has already run
 every other test when it gets here; it also passes alone in a fresh process.
 """
@@ -14,6 +18,7 @@ import ctypes
 import pytest
 import torch
 
+import oracle
 import paged_kv_attention_photon_gb300 as P
 import workloads as W
 from gpu_util import DeviceWorkload, assert_close, to_float64
@@ -27,14 +32,31 @@ def _lib():
     torch.cuda.init()
 
 
+_ORACLE = {}
+
+
+def _oracle_out(wl: W.Workload):
+    """The fp64 oracle's decode after the workload's cache write (computed once
+    per workload)."""
+    if wl.name not in _ORACLE:
+        kc, vc = wl.k_cache.copy(), wl.v_cache.copy()
+        oracle.cache_write(wl.k_new, wl.v_new, wl.slot_mapping, kc, vc,
+                           block_size=wl.block_size, dtype=wl.dtype)
+        _ORACLE[wl.name] = oracle.paged_decode(wl.q, kc, vc, wl.block_tables, wl.context_lens,
+                                               wl.scale, dtype=wl.dtype, num_threads=16)
+    return _ORACLE[wl.name]
+
+
 @pytest.mark.parametrize("maker", [W.qwen_b64, W.llama_b16, W.tiny])
-def test_noalloc_matches_workspace_entry_point_twice(maker):
+def test_noalloc_matches_workspace_entry_point_twice(maker, consumer):
     wl = maker()
+    ref = _oracle_out(wl)
     d = DeviceWorkload(wl)
     d.cache_write()
     d.decode()                                   # regular entry point, caller workspace
     torch.cuda.synchronize()
     want = d.out_f64()
+    assert_close(want, ref, wl.dtype, f"{wl.name} regular entry point vs oracle")
     lib = P._load()
     for call in range(2):
         out = torch.full_like(d.out, -7)
@@ -45,7 +67,9 @@ def test_noalloc_matches_workspace_entry_point_twice(maker):
                                              torch.cuda.current_stream().cuda_stream)
         assert st == 0, P.photon_status_string(st)
         torch.cuda.synchronize()
-        assert_close(to_float64(out, wl.dtype), want, wl.dtype, f"{wl.name} call {call}")
+        got = to_float64(out, wl.dtype)
+        assert_close(got, want, wl.dtype, f"{wl.name} call {call} vs regular entry point")
+        assert_close(got, ref, wl.dtype, f"{wl.name} call {call} vs oracle")
     status, bits = P.photon_get_last_device_error()
     assert status == 0 and bits == 0
 
