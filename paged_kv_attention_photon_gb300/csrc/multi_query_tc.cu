@@ -8,15 +8,22 @@
 // cache, per-sequence offsets) and "Roadmap" (FlashAttention-2 style IO-aware
 // attention for long sequences).
 //
-// A CTA is (128-row query tile, KV head, sequence), 4 warps.  Row r of the
-// tile is (token r / G, head r % G of the KV head's group) and lives in TMEM
-// lane r, so thread r owns row r from the scores to the output: the softmax
+// A CTA owns 256 query rows of one (sequence, KV head) as two tiles of 128
+// and runs 11 warps in fixed roles: 8 softmax warps (4 per tile), a K copy
+// warp, a V copy warp and an MMA warp.  Row r of a tile is (token r / G, head
+// r % G of the KV head's group) and lives in TMEM lane r, so thread r of the
+// tile's softmax warps owns row r from the scores to the output: the softmax
 // needs no shuffles.  Per chunk of 64 keys:
-//   S = Q K^T    one thread issues D/16 MMAs (M=128, N=64, K=16) into TMEM
-//   softmax      each thread loads its 64 scores (tcgen05.ld), masks the keys
-//                after its position, updates (m, l), writes its 64 weights
-//                P as fp16/bf16 into a swizzled shared tile
-//   O += P V     4 MMAs (M=128, N=D, K=16) accumulate in TMEM
+//   K, V     2-D tensor-map copies (boxes of 16 rows x 64 elements, 128-byte
+//            swizzle) straight from the paged pool through the block table,
+//            into a K ring and a V ring of three stages each
+//   S = Q K^T    D/16 MMAs per tile (M=128, N=64, K=16), fp32 in TMEM, two S
+//                buffers per tile
+//   softmax  each thread loads its 64 scores (tcgen05.ld), masks the keys
+//            after its position, updates (m, l), writes its 64 weights P as
+//            fp16/bf16 into a swizzled shared tile (two P buffers per tile)
+//   O += P V     4 MMAs per tile (M=128, N=D, K=16) accumulate in TMEM, V read
+//                as an MN-major operand from the same swizzled rows
 // The running maximum only moves when a new score exceeds it by more than
 // 2^8 (log2 domain), and only then is the TMEM accumulator rescaled: between
 // rescales the weights use a stale maximum, which the final O / l cancels
@@ -25,9 +32,12 @@
 // Operands are K-major with the 128-byte swizzle: a tile of R rows and 64
 // 16-bit elements per row is R/8 atoms of 8 rows x 128 bytes, 16-byte chunk c
 // of row r stored at chunk c ^ (r % 8); rows past 64 elements continue in the
-// next 64-element block of R x 128 bytes.  K rows arrive with cp.async; V is
-// needed transposed (d rows, key columns), so each thread loads 16-byte V
-// pieces into registers one chunk ahead and scatters them as 2-byte stores.
+// next 64-element block of R x 128 bytes.  The Q tiles are loaded once per
+// CTA with cp.async into the same layout.
+//
+// CTAs start in the order of their linear index, which is mapped onto the
+// (sequence, KV head, tile) items sorted by the length of their causal key
+// range, longest first (tc_item_of).
 #include <cuda.h>
 
 #include <type_traits>
@@ -156,19 +166,20 @@ __device__ __forceinline__ uint32_t sw_chunk(int r, int c) {
 template <typename T, int D>
 struct TcCfg {
   static constexpr int kTiles = 2;
-  static constexpr int kStages = 3;
+  static constexpr int kKStages = 3;   // K ring: a stage is free once S of its chunk is done
+  static constexpr int kVStages = 3;   // V ring: free once the P V product of its chunk is done
   static constexpr int kQBytes = kTcRows * D * 2;     // one Q tile
   static constexpr int kKBytes = kTcKeys * D * 2;     // one K chunk
   static constexpr int kVBytes = kTcKeys * D * 2;     // one V chunk
   static constexpr int kPBytes = kTcRows * kTcKeys * 2;
   static constexpr int kOffQ = 0;                               // [kTiles]
-  static constexpr int kOffK = kOffQ + kTiles * kQBytes;        // [kStages]
-  static constexpr int kOffV = kOffK + kStages * kKBytes;       // [kStages]
-  static constexpr int kOffP = kOffV + kStages * kVBytes;       // [kTiles][2]
+  static constexpr int kOffK = kOffQ + kTiles * kQBytes;        // [kKStages]
+  static constexpr int kOffV = kOffK + kKStages * kKBytes;      // [kVStages]
+  static constexpr int kOffP = kOffV + kVStages * kVBytes;      // [kTiles][2]
   static constexpr int kUsed = kOffP + kTiles * 2 * kPBytes;
   static constexpr int kSmem = kUsed + 1024;   // + alignment of the base to a swizzle atom
-  // softmax warps, then the copy warp and the MMA warp
-  static constexpr int kThreads = kTiles * kTcThreads + 64;
+  // softmax warps, then the K copy warp, the V copy warp and the MMA warp
+  static constexpr int kThreads = kTiles * kTcThreads + 96;
 };
 
 // MN-major (V) operand: the same 128-byte-swizzled rows of 64 elements as the
@@ -187,17 +198,144 @@ __device__ __forceinline__ uint64_t sw128_mn_desc(uint32_t saddr) {
 
 __device__ __forceinline__ void mbar_arrive_cnt(uint64_t* bar) { mbar_arrive(bar); }
 
+// Work class of the CTA of (sequence b, tile): 1 + floor(log2(key chunks))
+// for a CTA with rows, 0 for one without (or one whose arguments the kernel
+// rejects, which only writes zero rows).
+template <int kSuperRows>
+__device__ __forceinline__ int tc_work_class(const MultiQueryArgs& a, int b, int tile, int G) {
+  const int q0 = __ldg(a.query_start + b);
+  const int n = __ldg(a.query_start + b + 1) - q0;
+  const int ctx = __ldg(a.context_lens + b);
+  if (n <= 0 || q0 < 0 || q0 + n > a.num_tokens || n > a.max_query_len || ctx < n ||
+      ctx > a.MBS * kBlockSize)
+    return 0;
+  const int row0 = tile * kSuperRows;
+  const int rows = min(kSuperRows, n * G - row0);
+  if (rows <= 0) return 0;
+  const int kend = ctx - n + (row0 + rows - 1) / G + 1;
+  const int chunks = (kend + kTcKeys - 1) / kTcKeys;
+  return 32 - __clz(chunks);
+}
+
+// The (sequence, KV head, tile) of this CTA.  CTAs are started in the order
+// of their linear index, so the index is mapped onto the items sorted by
+// work class, largest first (the longest causal key ranges start first and
+// the short ones fill in behind them); inside a class the natural order
+// (sequence, KV head, tile) keeps the tiles of one sequence's KV head
+// together, so its K/V rows are read from HBM once and then hit L2.  Every
+// thread of the CTA takes part; the scratch is shared memory.
+template <int kSuperRows>
+__device__ __forceinline__ void tc_item_of(const MultiQueryArgs& a, int G, int& b_out,
+                                           int& kvh_out, int& tile_out, int* hist, int* wsum,
+                                           int* sel) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nthr = blockDim.x, nwarps = (nthr + 31) / 32;
+  const int T = gridDim.x, B = a.B, H = a.Hkv;
+  const int L = (int)((blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x);
+  for (int i = tid; i < 33; i += nthr) hist[i] = 0;
+  __syncthreads();
+  for (int p = tid; p < B * T; p += nthr)
+    atomicAdd(&hist[tc_work_class<kSuperRows>(a, p / T, p % T, G)], 1);
+  __syncthreads();
+  if (tid == 0) {
+    int acc = 0, C = 0, j = 0;
+    for (int c = 32; c >= 0; --c) {
+      const int items = hist[c] * H;
+      if (L < acc + items) {
+        C = c;
+        j = L - acc;
+        break;
+      }
+      acc += items;
+    }
+    sel[0] = C;
+    sel[1] = j;
+  }
+  __syncthreads();
+  const int C = sel[0], j = sel[1];
+  // items of class C in natural order: find the sequence by a running
+  // (chunked) block scan of its item count
+  int carry = 0;
+  for (int base = 0; base < B; base += nthr) {
+    const int b = base + tid;
+    int cnt = 0;
+    if (b < B)
+      for (int t = 0; t < T; ++t) cnt += tc_work_class<kSuperRows>(a, b, t, G) == C ? 1 : 0;
+    const int items = cnt * H;
+    int v = items;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += y;
+    }
+    if (lane == 31) wsum[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+      int w = lane < nwarps ? wsum[lane] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += y;
+      }
+      if (lane < nwarps) wsum[32 + lane] = w;   // inclusive over warps
+    }
+    __syncthreads();
+    const int excl = carry + (warp > 0 ? wsum[32 + warp - 1] : 0) + v - items;
+    if (items > 0 && j >= excl && j < excl + items) {
+      const int r = j - excl;
+      int k = r % cnt;
+      int tile = 0;
+      for (int t = 0; t < T; ++t) {
+        if (tc_work_class<kSuperRows>(a, b, t, G) != C) continue;
+        if (k-- == 0) {
+          tile = t;
+          break;
+        }
+      }
+      sel[2] = b;
+      sel[3] = r / cnt;
+      sel[4] = tile;
+    }
+    carry += wsum[32 + nwarps - 1];
+    __syncthreads();
+  }
+  b_out = sel[2];
+  kvh_out = sel[3];
+  tile_out = sel[4];
+}
+
+#ifdef PHOTON_PROBE
+// Tuning builds only (never compiled into the library by default): the
+// per-chunk timeline of one CTA (the last tile of KV head 0 of the last
+// sequence) and the start and end of every CTA.
+constexpr int kTcProbeChunks = 160;
+static __device__ unsigned long long g_tc_probe[kTcProbeChunks][8];
+static __device__ unsigned long long g_tc_cta[4096][2];
+#define TC_PROBE(c, i)                                                                \
+  do {                                                                               \
+    if (probe_cta && (c) < kTcProbeChunks) g_tc_probe[c][i] = global_timer_ns();      \
+  } while (0)
+#else
+#define TC_PROBE(c, i) do { } while (0)
+#endif
+
 // Warp roles: a CTA owns 256 query rows of one (sequence, KV head) as two
 // tiles of 128.  Warps 0-3 own tile 0 and warps 4-7 tile 1 (thread r of a
 // tile: TMEM lane r of that tile's columns): softmax, O rescale, epilogue.
-// Warp 8 copies: its lane 0 issues the bulk tensor copies of each chunk as
-// soon as the ring stage is free.  Warp 9 computes: its lanes zero the V rows
-// that lie past the last key, its lane 0 issues every MMA.  Both tiles use
-// every K/V chunk, so each chunk is fetched once for 256 rows.  TMEM: tile t
-// owns columns [256 t, 256 t + 256): two S buffers of 64, then O.
+// Warp 8 copies K and warp 9 copies V: each one's lane 0 issues the bulk
+// tensor copies of a chunk as soon as a stage of its ring is free.  The two
+// rings are separate because their stages are held for different spans: a
+// K chunk only until S of its chunk is computed, a V chunk until the P V
+// product, after the softmax; with one ring for both, the copy latency of
+// every chunk sat on the chain through the softmax.  Warp 10 computes: its
+// lanes zero the V rows that lie past the last key, its lane 0 issues every
+// MMA.  Both tiles use every K/V chunk, so each chunk is fetched once for 256
+// rows.  TMEM: tile t owns columns [256 t, 256 t + 256): two S buffers of 64,
+// then O.
 // Barriers (each completes once per use; a use's parity is its index & 1):
-//   kv_full[s]     K and V of a chunk landed in stage s (copy transaction bytes)
-//   kv_free[s]     the P V products reading stage s finished (MMA commit)
+//   k_full[s], v_full[s]  K (V) of a chunk landed in stage s (copy transaction bytes)
+//   k_free[s]      the S products reading K stage s finished (MMA commit)
+//   v_free[s]      the P V products reading V stage s finished (MMA commit)
 //   s_full[t][b]   S of a chunk is in tile t's TMEM buffer b (MMA commit)
 //   s_free[t][b]   tile t's 4 softmax warps have read that buffer (4 arrivals)
 //   p_full[t][b]   tile t's P of a chunk is in its shared buffer b (128 arrivals)
@@ -209,23 +347,32 @@ __global__ void __launch_bounds__(TcCfg<T, D>::kThreads)
     paged_multi_query_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
                                 const __grid_constant__ CUtensorMap tm_v, const MultiQueryArgs a) {
   using C = TcCfg<T, D>;
-  constexpr int S = C::kStages;
+  constexpr int SK = C::kKStages, SV = C::kVStages;
   constexpr int NT = C::kTiles;
   constexpr int kSuper = NT * kTcRows;
   extern __shared__ unsigned char tc_smem_raw[];
-  __shared__ __align__(8) uint64_t kv_full[S], kv_free[S], s_full[NT][2], s_free[NT][2],
-      p_full[NT][2], p_done[NT][2];
+  __shared__ __align__(8) uint64_t k_full[SK], k_free[SK], v_full[SV], v_free[SV],
+      s_full[NT][2], s_free[NT][2], p_full[NT][2], p_done[NT][2];
   __shared__ uint32_t tmem_slot;
-  __shared__ int tail_rows[S];   // per stage: first V row to zero (64 = none)
+  __shared__ int tail_rows[SV];   // per V stage: first V row to zero (64 = none)
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_addr(smem);
   const uint32_t sQ = sbase + C::kOffQ, sK = sbase + C::kOffK, sV = sbase + C::kOffV,
                  sP = sbase + C::kOffP;
 
-  const int b = blockIdx.z, kvh = blockIdx.y, tile = blockIdx.x;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = a.Hq / a.Hkv;
+#ifdef PHOTON_PROBE
+  const int cta_lin = (blockIdx.z * gridDim.y + blockIdx.y) * gridDim.x + blockIdx.x;
+  if (tid == 0 && cta_lin < 4096) g_tc_cta[cta_lin][0] = global_timer_ns();
+#endif
+  __shared__ int ord_hist[33], ord_wsum[64], ord_sel[5];
+  int b, kvh, tile;
+  tc_item_of<kSuper>(a, G, b, kvh, tile, ord_hist, ord_wsum, ord_sel);
+#ifdef PHOTON_PROBE
+  const bool probe_cta = cta_lin == 0;   // the first CTA started: the largest class
+#endif
   const int q0 = __ldg(a.query_start + b);
   const int n = __ldg(a.query_start + b + 1) - q0;
   const int ctx = __ldg(a.context_lens + b);
@@ -258,9 +405,13 @@ __global__ void __launch_bounds__(TcCfg<T, D>::kThreads)
 
   // ---- setup: barriers, TMEM, the Q tiles (rows past the CTA's rows zero)
   if (tid == 0) {
-    for (int i = 0; i < S; ++i) {
-      mbar_init(&kv_full[i], 1);
-      mbar_init(&kv_free[i], 1);
+    for (int i = 0; i < SK; ++i) {
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_free[i], 1);
+    }
+    for (int i = 0; i < SV; ++i) {
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_free[i], 1);
     }
     for (int t = 0; t < NT; ++t) {
       for (int i = 0; i < 2; ++i) {
@@ -296,13 +447,20 @@ __global__ void __launch_bounds__(TcCfg<T, D>::kThreads)
   bool ok = true;
 
   auto lane0_ok = [&](bool v) { return __shfl_sync(0xffffffffu, v ? 1 : 0, 0) != 0; };
-  if (warp == NT * 4) {
+  if (warp == NT * 4 || warp == NT * 4 + 1) {
     // ================================================================ copies
+    // warp NT*4: K chunks into the K ring; warp NT*4 + 1: V chunks into the V ring
+    const bool is_v = warp == NT * 4 + 1;
+    const int nst = is_v ? SV : SK;
+    uint64_t* full = is_v ? v_full : k_full;
+    uint64_t* freed = is_v ? v_free : k_free;
+    const CUtensorMap* map = is_v ? &tm_v : &tm_k;
+    const uint32_t ring = is_v ? sV : sK;
     const int32_t* table = a.block_tables + (size_t)b * a.MBS;
     for (int c = 0; c < nchunks && ok; ++c) {
-      const int st = c % S;
-      if (c >= S) {   // the stage's previous chunk, c - S, has been consumed
-        ok = lane0_ok(mbar_wait_bounded(&kv_free[st], ((c / S) - 1) & 1));
+      const int st = c % nst;
+      if (c >= nst) {   // the stage's previous chunk, c - nst, has been consumed
+        ok = lane0_ok(mbar_wait_bounded(&freed[st], ((c / nst) - 1) & 1));
         if (!ok) break;
       }
       if (lane != 0) continue;
@@ -317,8 +475,8 @@ __global__ void __launch_bounds__(TcCfg<T, D>::kThreads)
           const int p = __ldg(table + kb);
           if (p >= 0 && p < a.NB) {
             phys[i] = p;
-            bytes += 2u * kBlockSize * D * 2u;
-          } else {
+            bytes += kBlockSize * D * 2u;
+          } else if (!is_v) {
             raise_error(a.err, kErrBlock);
           }
         }
@@ -326,49 +484,37 @@ __global__ void __launch_bounds__(TcCfg<T, D>::kThreads)
         const int valid_rows = phys[i] < 0 ? 0 : min(kBlockSize, kend - kb * kBlockSize);
         if (valid_rows < kBlockSize && tail == kTcKeys) tail = i * kBlockSize + valid_rows;
       }
-      tail_rows[st] = tail;   // published by the barrier's arrive below
-      mbar_arrive_expect_tx(&kv_full[st], bytes);
+      if (is_v) tail_rows[st] = tail;   // published by the barrier's arrive below
+      if (!is_v) TC_PROBE(c, 6);
+      mbar_arrive_expect_tx(&full[st], bytes);
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         if (phys[i] < 0) continue;
         const int y = (phys[i] * a.Hkv + kvh) * kBlockSize;
 #pragma unroll
-        for (int h = 0; h < D / 64; ++h) {
-          tma_load_box(sK + st * C::kKBytes + h * (kTcKeys * 128) + i * 2048, &tm_k, h * 64, y,
-                      &kv_full[st]);
-          tma_load_box(sV + st * C::kVBytes + h * (kTcKeys * 128) + i * 2048, &tm_v, h * 64, y,
-                      &kv_full[st]);
-        }
+        for (int h = 0; h < D / 64; ++h)
+          tma_load_box(ring + st * C::kKBytes + h * (kTcKeys * 128) + i * 2048, map, h * 64, y,
+                       &full[st]);
       }
     }
     if (!ok && lane == 0) raise_error(a.err, kErrTimeout);
-  } else if (warp == NT * 4 + 1) {
+  } else if (warp == NT * 4 + 2) {
     // ================================================================ MMAs
     const uint32_t id_s = f16_idesc<T>(kTcRows, kTcKeys);
     const uint32_t id_o = f16_idesc<T>(kTcRows, D) | (1u << 16);   // B (V) MN-major
     for (int c = 0; c <= nchunks && ok; ++c) {
       if (c < nchunks) {
-        const int st = c % S;
-        ok = lane0_ok(mbar_wait_bounded(&kv_full[st], (c / S) & 1));
+        const int st = c % SK;
+        ok = lane0_ok(mbar_wait_bounded(&k_full[st], (c / SK) & 1));
         if (!ok) break;
-        // zero the V rows past the last key (a partial or missing block):
-        // they are multiplied by zero weights, and 0 x NaN would not vanish
-        const int tail = tail_rows[st];
-        if (tail < kTcKeys) {
-          unsigned char* vt = smem + C::kOffV + st * C::kVBytes;
-          for (int p = lane; p < (kTcKeys - tail) * (D / 8); p += 32) {
-            const int r = tail + p / (D / 8), ch = p % (D / 8);
-            *reinterpret_cast<uint4*>(vt + sw_chunk<kTcKeys>(r, ch)) = make_uint4(0, 0, 0, 0);
-          }
-          fence_async_smem();
-        }
-        __syncwarp();
+        if (lane == 0) TC_PROBE(c, 7);
         for (int t = 0; t < ntiles && ok; ++t) {
           if (c >= 2) {
             ok = lane0_ok(mbar_wait_bounded(&s_free[t][c & 1], ((c - 2) >> 1) & 1));
             if (!ok) break;
           }
           if (lane == 0) {
+            if (t == 0) TC_PROBE(c, 4);
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
@@ -382,14 +528,31 @@ __global__ void __launch_bounds__(TcCfg<T, D>::kThreads)
           }
         }
         if (!ok) break;
+        if (lane == 0) tc_commit(&k_free[st]);   // the K stage is free once these S are done
       }
       if (c >= 1) {
-        // P V of the previous chunk, tile by tile, once its weights are written
-        const int pc = c - 1, pst = pc % S, pb = pc & 1;
+        // P V of the previous chunk, tile by tile, once its V landed and its
+        // weights are written
+        const int pc = c - 1, pst = pc % SV, pb = pc & 1;
+        ok = lane0_ok(mbar_wait_bounded(&v_full[pst], (pc / SV) & 1));
+        if (!ok) break;
+        // zero the V rows past the last key (a partial or missing block):
+        // they are multiplied by zero weights, and 0 x NaN would not vanish
+        const int tail = tail_rows[pst];
+        if (tail < kTcKeys) {
+          unsigned char* vt = smem + C::kOffV + pst * C::kVBytes;
+          for (int p = lane; p < (kTcKeys - tail) * (D / 8); p += 32) {
+            const int r = tail + p / (D / 8), ch = p % (D / 8);
+            *reinterpret_cast<uint4*>(vt + sw_chunk<kTcKeys>(r, ch)) = make_uint4(0, 0, 0, 0);
+          }
+          fence_async_smem();
+        }
+        __syncwarp();
         for (int t = 0; t < ntiles && ok; ++t) {
           ok = lane0_ok(mbar_wait_bounded(&p_full[t][pb], (pc >> 1) & 1));
           if (!ok) break;
           if (lane == 0) {
+            if (t == 0) TC_PROBE(pc, 5);
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < kTcKeys / 16; ++kk)
@@ -401,7 +564,7 @@ __global__ void __launch_bounds__(TcCfg<T, D>::kThreads)
           }
         }
         if (!ok) break;
-        if (lane == 0) tc_commit(&kv_free[pst]);
+        if (lane == 0) tc_commit(&v_free[pst]);
       }
     }
     if (!ok && lane == 0) raise_error(a.err, kErrTimeout);
@@ -422,9 +585,11 @@ __global__ void __launch_bounds__(TcCfg<T, D>::kThreads)
     for (int c = 0; c < nchunks && tile_used; ++c) {
       ok = mbar_wait_bounded(&s_full[t][c & 1], (c >> 1) & 1);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+      if (lane == 0 && (warp == 0 || warp == 4)) TC_PROBE(c, warp == 0 ? 0 : 3);
       tc_fence_after();
       float s[kTcKeys];
       tmem_ld64(tbase + lane_base + kTmemS + (c & 1) * kTcKeys, s);
+      if (lane == 0 && warp == 0) TC_PROBE(c, 1);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cnt(&s_free[t][c & 1]);
@@ -500,6 +665,7 @@ __global__ void __launch_bounds__(TcCfg<T, D>::kThreads)
             make_uint4(w[0], w[1], w[2], w[3]);
       }
       l_run += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
+      if (lane == 0 && warp == 0) TC_PROBE(c, 2);
       fence_async_smem();
       mbar_arrive_cnt(&p_full[t][c & 1]);
     }
@@ -548,6 +714,9 @@ __global__ void __launch_bounds__(TcCfg<T, D>::kThreads)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
                  "r"(NT * kTmemCols)
                  : "memory");
+#ifdef PHOTON_PROBE
+  if (tid == 0 && cta_lin < 4096) g_tc_cta[cta_lin][1] = global_timer_ns();
+#endif
 }
 
 }  // namespace
@@ -566,15 +735,24 @@ cudaError_t make_pool_map(CUtensorMap* map, const void* pool, int dtype, int NB,
     if (e != cudaSuccess || q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
     encode = reinterpret_cast<EncodeFn>(fn);
   }
+  // 16-bit pools: boxes of 64 elements (128 bytes) per row, 128-byte swizzle.
+  // e4m3 pools (dtype 3): one box per block row of D codes, the 128-byte
+  // swizzle at D = 128 and the 64-byte one at D = 64 (a row is the swizzle
+  // span either way).
+  const bool codes = dtype == 3;
   const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)NB * Hkv * kBlockSize};
-  const cuuint64_t strides[1] = {(cuuint64_t)D * 2};
-  const cuuint32_t box[2] = {64, (cuuint32_t)kBlockSize};
+  const cuuint64_t strides[1] = {(cuuint64_t)D * (codes ? 1 : 2)};
+  const cuuint32_t box[2] = {codes ? (cuuint32_t)D : 64u, (cuuint32_t)kBlockSize};
   const cuuint32_t estr[2] = {1, 1};
-  const CUresult r = encode(
-      map, dtype == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
-      const_cast<void*>(pool), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-      CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  const CUtensorMapDataType type = codes        ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                   : dtype == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const CUtensorMapSwizzle swz =
+      codes && D == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
+  const CUresult r = encode(map, type, 2, const_cast<void*>(pool), dims, strides, box, estr,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
@@ -605,6 +783,16 @@ cudaError_t launch_tc(const MultiQueryArgs& a, cudaStream_t stream) {
 }
 
 }  // namespace
+
+#ifdef PHOTON_PROBE
+// Tuning builds only: the timeline of the last tcgen05 multi-query call.
+extern "C" int photon_tc_probe_read(void* chunks, size_t chunk_bytes, void* ctas,
+                                    size_t cta_bytes) {
+  cudaError_t e = cudaMemcpyFromSymbol(chunks, g_tc_probe, chunk_bytes);
+  if (e == cudaSuccess) e = cudaMemcpyFromSymbol(ctas, g_tc_cta, cta_bytes);
+  return (int)e;
+}
+#endif
 
 cudaError_t launch_multi_query_tc(const MultiQueryArgs& a, cudaStream_t stream) {
   if (!a.q || !a.k_cache || !a.v_cache || !a.block_tables || !a.context_lens || !a.query_start ||

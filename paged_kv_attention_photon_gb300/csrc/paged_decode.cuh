@@ -88,9 +88,9 @@ struct StageHdr {
 };
 enum : int { kFirst = 1, kLast = 2, kDone = 4 };
 
-// Runs of the work list: the full partitions, then up to log2(4096/16) + 1 = 9
-// classes of tail partitions.
-constexpr int kMaxRuns = 10;
+// Runs of the work list: partition 0 of every sequence, the further full
+// partitions, then up to log2(4096/16) + 1 = 9 classes of tail partitions.
+constexpr int kMaxRuns = 11;
 
 // Persistent-kernel geometry: NC consumer warps, 1 producer warp, S ring stages.
 // M: the tensor-core consumer, whose blocks arrive as swizzled tensor-map
@@ -100,9 +100,9 @@ constexpr int kMaxRuns = 10;
 // X: few-token multi-query mode (tensor-core consumer only): up to 8 query
 // slots (token, head) per item instead of the G heads of one token.
 // F: the cache holds e4m3 codes (one byte per element; q and out stay fp16):
-// the stages carry the fp8 blocks, moved by plain bulk copies, and each
-// consumer warp widens its K and V block to fp16 in a swizzled scratch of its
-// own that the tensor-core math reads.
+// the stages carry the code blocks as tensor-map copies in the swizzled
+// layout of code_chunk, and the tensor-core math widens the codes to fp16 in
+// registers as it loads its fragments.
 template <typename T, int D, int G, int NC, int S, bool R = false, bool M = false, bool X = false,
           bool F = false>
 struct PersistCfg {
@@ -111,7 +111,6 @@ struct PersistCfg {
   static constexpr int kBlockElems = kBlockSize * D;
   static constexpr int kElemBytes = F ? 1 : (int)sizeof(T);       // one cache element
   static constexpr int kBlockBytes = kBlockElems * kElemBytes;    // one cache block (a stage slot)
-  static constexpr int kWideBytes = kBlockElems * (int)sizeof(T);  // F: one block widened to T
   static constexpr int kSlots = X ? 8 : G;                      // query rows per item
   static constexpr int kQBytes = kSlots * D * (int)sizeof(T);
   // with RoPE the item's (cos, sin) row, D/2 float pairs, follows its q rows
@@ -130,13 +129,10 @@ struct PersistCfg {
   // M only: the new token's K row then V row, per stage
   static constexpr int kSideBytes = M && !F ? 2 * D * (int)sizeof(T) : 0;
   static constexpr int kOffSide = kOffKV + kStageBytes * S;
-  // F only: each consumer warp's widened K block, then V block
-  static constexpr int kOffWide = (kOffSide + kSideBytes * S + 1023) / 1024 * 1024;
-  static constexpr int kWideTotal = F ? NC * 2 * kWideBytes : 0;
   // Per-warp (m, l) at an item's end, double-buffered by item parity.  The
   // warps' o rows (kSlots x D fp32 each) go to their own K (then V) block
   // areas of the item's last stage, which is released only after the combine.
-  static constexpr int kOffPm = F ? kOffWide + kWideTotal : kOffSide + kSideBytes * S;
+  static constexpr int kOffPm = kOffSide + kSideBytes * S;
   static constexpr int kOffPl = kOffPm + 4 * 2 * NC * kSlots;   // float[2][NC][kSlots]
   static constexpr int kAlignPad = M ? 1024 : 0;
   static constexpr int kSmemBytes = kOffPl + 4 * 2 * NC * kSlots + kAlignPad;
@@ -260,7 +256,25 @@ __device__ __forceinline__ uint32_t blk_chunk(int row, int chunk) {
 // positions lim[0], lim[1] (key0 = position of the block's row 0); a slot can
 // then have no key in a block, or in a whole item, so the max and rescale
 // steps guard against -inf - -inf.
-template <typename T, int D, bool kQLo, bool kCausal>
+//
+// kCodes (e4m3 cache, fp16 q): kblk / vblk hold the blocks' codes, one byte per
+// element, rows of D codes in the tensor copies' swizzled layout (code_chunk),
+// and the fragments are widened from the codes in registers: ldmatrix moves
+// code pairs as 16-bit elements, cvt turns each pair into an fp16 pair.  The
+// head dimension is walked in a permuted order that keeps every widened pair
+// where its fragment wants it:
+//   S^T: k-step kk covers code chunk kk (dims 16kk .. 16kk+15); the MMA's k
+//        index 2t+j is dim 16kk + 4t + j, 2t+8+j is dim 16kk + 4t + 2 + j
+//        (t = lane % 4), so bq must hold q's dims in that order;
+//   O^T: tile i covers dims 16i .. 16i+15 with MMA row r as dim 16i + 2r and
+//        row r + 8 as dim 16i + 2r + 1 (the caller stores o in that order).
+template <int D>
+__device__ __forceinline__ uint32_t code_chunk(int row, int chunk) {
+  if constexpr (D == 128) return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
+  else return (uint32_t)(row * 64 + ((chunk ^ ((row >> 1) & 3)) << 4));
+}
+__device__ __forceinline__ uint32_t widen_e4m3x2(uint32_t pair);
+template <typename T, int D, bool kQLo, bool kCausal, bool kCodes = false>
 __device__ __forceinline__ void attend_block_mma(uint32_t kblk, uint32_t vblk, int n_valid,
                                                  float qscale, const uint32_t (&bq)[D / 16][2],
                                                  const uint32_t (&bql)[D / 16][2],
@@ -269,7 +283,31 @@ __device__ __forceinline__ void attend_block_mma(uint32_t kblk, uint32_t vblk, i
                                                  const int (&lim)[2]) {
   const int r = lane >> 2;
   float s[4] = {0.f, 0.f, 0.f, 0.f};
-  {
+  if constexpr (kCodes) {
+    // ldmatrix row addresses: matrices (keys 0-7 | 8-15) x (code chunks 2j | 2j+1);
+    // two independent accumulator chains (even and odd chunks)
+    const int krow = (lane & 7) + ((lane >> 3) & 1) * 8;
+    const int khi = lane >> 4;
+    float s2[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < D / 32; ++j) {
+      uint32_t c0, c1, c2, c3;
+      ldsm_x4(kblk + code_chunk<D>(krow, 2 * j + khi), c0, c1, c2, c3);
+      uint32_t a[4];
+      a[0] = widen_e4m3x2(c0 & 0xFFFFu);
+      a[2] = widen_e4m3x2(c0 >> 16);
+      a[1] = widen_e4m3x2(c1 & 0xFFFFu);
+      a[3] = widen_e4m3x2(c1 >> 16);
+      Mma<T>::run(s, a, bq[2 * j][0], bq[2 * j][1]);
+      a[0] = widen_e4m3x2(c2 & 0xFFFFu);
+      a[2] = widen_e4m3x2(c2 >> 16);
+      a[1] = widen_e4m3x2(c3 & 0xFFFFu);
+      a[3] = widen_e4m3x2(c3 >> 16);
+      Mma<T>::run(s2, a, bq[2 * j + 1][0], bq[2 * j + 1][1]);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) s[i] += s2[i];
+  } else {
     // ldmatrix row addresses: matrices (keys 0-7 | 8-15) x (dims lo | hi of the k-step)
     const int krow = (lane & 7) + ((lane >> 3) & 1) * 8;
     const int khi = lane >> 4;
@@ -331,7 +369,31 @@ __device__ __forceinline__ void attend_block_mma(uint32_t kblk, uint32_t vblk, i
   const uint32_t b0 = movmatrix_trans(h01), b1 = movmatrix_trans(h23);
   const uint32_t e0 = movmatrix_trans(Mma<T>::pack(p0 - r01.x, p1 - r01.y));
   const uint32_t e1 = movmatrix_trans(Mma<T>::pack(p2 - r23.x, p3 - r23.y));
-  {
+  if constexpr (kCodes) {
+    // ldmatrix.trans over code pairs: matrices (keys 0-7 | 8-15) x (code
+    // chunks 2j | 2j+1).  Lane (r, t) receives, per matrix, codes 2r and
+    // 2r+1 of keys 2t and 2t+1; a byte permute pairs them by dim (keys 2t,
+    // 2t+1 at dim 2r, then at dim 2r+1) and cvt widens each pair.
+    const int vrow = (lane & 7) + ((lane >> 3) & 1) * 8;
+    const int vhi = lane >> 4;
+#pragma unroll
+    for (int j = 0; j < D / 32; ++j) {
+      uint32_t c[4];
+      ldsm_x4_trans(vblk + code_chunk<D>(vrow, 2 * j + vhi), c[0], c[1], c[2], c[3]);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        const uint32_t w0 = __byte_perm(c[2 * h], 0u, 0x3120);
+        const uint32_t w1 = __byte_perm(c[2 * h + 1], 0u, 0x3120);
+        uint32_t a[4];
+        a[0] = widen_e4m3x2(w0 & 0xFFFFu);
+        a[1] = widen_e4m3x2(w0 >> 16);
+        a[2] = widen_e4m3x2(w1 & 0xFFFFu);
+        a[3] = widen_e4m3x2(w1 >> 16);
+        Mma<T>::run(o[2 * j + h], a, b0, b1);
+        Mma<T>::run(o[2 * j + h], a, e0, e1);
+      }
+    }
+  } else {
     // ldmatrix.trans row addresses: matrices (keys 0-7 | 8-15) x (dims lo | hi of the tile)
     const int vrow = (lane & 7) + (lane >> 4) * 8;
     const int vhi = (lane >> 3) & 1;
@@ -345,18 +407,11 @@ __device__ __forceinline__ void attend_block_mma(uint32_t kblk, uint32_t vblk, i
   }
 }
 
-// Two e4m3 codes (the low byte first) widened exactly to an fp16 pair, and
-// sixteen codes of a 16-byte load (code 0 at the lowest address) to elements
-// 0-7 (lo) and 8-15 (hi).  Every e4m3 value is an fp16 value.
+// Two e4m3 codes (the low byte first) widened exactly to an fp16 pair (the
+// low byte's value in the low half).  Every e4m3 value is an fp16 value.
 __device__ __forceinline__ uint32_t widen_e4m3x2(uint32_t pair) {
   const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)pair, __NV_E4M3);
   return (uint32_t)h.x | ((uint32_t)h.y << 16);
-}
-__device__ __forceinline__ void widen_e4m3x16(const uint4 q, uint4& lo, uint4& hi) {
-  lo = make_uint4(widen_e4m3x2(q.x & 0xFFFFu), widen_e4m3x2(q.x >> 16),
-                  widen_e4m3x2(q.y & 0xFFFFu), widen_e4m3x2(q.y >> 16));
-  hi = make_uint4(widen_e4m3x2(q.z & 0xFFFFu), widen_e4m3x2(q.z >> 16),
-                  widen_e4m3x2(q.w & 0xFFFFu), widen_e4m3x2(q.w >> 16));
 }
 
 // ------------------------------------------------------------------ RoPE
@@ -454,6 +509,8 @@ __device__ __forceinline__ bool consumer_sync(uint64_t* bar, uint32_t& phase, in
 constexpr int kProbeCtas = 1024;
 constexpr int kProbeSlots = 48;  // [8 + 2k]: item k's first copy issued, [9 + 2k]: item k combined
 static __device__ unsigned long long g_probe[kProbeCtas][kProbeSlots];
+// merge kernel CTAs: [0] entry, [1] past the dependency wait, [2] done
+static __device__ unsigned long long g_probe_merge[4096][4];
 #define PROBE_SET(i, v) \
   do { if (blockIdx.x < kProbeCtas && (i) < kProbeSlots) g_probe[blockIdx.x][i] = (v); } while (0)
 #else
@@ -476,7 +533,7 @@ static __device__ unsigned long long g_probe[kProbeCtas][kProbeSlots];
 // the K scale is folded into qscale, the V scale into the item's combine.
 template <typename T, int D, int G, int NC, int S, bool kRope, bool kMma, bool kMulti,
           bool kFp8 = false>
-__global__ void __launch_bounds__((NC + 1) * 32, 1)
+__global__ void __launch_bounds__((NC + 1) * 32, kFp8 && NC <= 4 ? 3 : 1)
     paged_decode_attention_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
                                   const __grid_constant__ CUtensorMap tmv) {
   using PC = PersistCfg<T, D, G, NC, S, kRope, kMma, kMulti, kFp8>;
@@ -491,6 +548,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + PC::kOffAbort);
   StageHdr* hdr = reinterpret_cast<StageHdr*>(smem + PC::kOffHdr);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (threadIdx.x == 0) PROBE_SET(5, global_timer_ns());
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -542,32 +600,50 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
   if (warp == NC) {
     // ================================================================ producer
     // Work list, derived here from context_lens with no planning kernel.  The
-    // (sequence, partition) pairs come in runs -- first every full partition
-    // (sequence order, then partition order), then the partial tail
-    // partitions, class by class from the longest to the shortest -- so the
-    // items handed out last are the smallest (longest-processing-time first,
-    // without a sort).  Each pair is expanded over the KV heads
-    // (item = pair * Hkv + kvh).  The warp keeps a
-    // window of 32 sequences (lane j: sequence wb + j's context length, its
-    // pair count in the current run and the pairs before it) and slides it
-    // forward as its items advance, with the next window's lengths already
-    // loaded.  A software pipeline keeps every round trip off the copy
-    // stream: while item i's stages are issued, the block-table slice of item
-    // i+1 is in flight and the index of item i+2 is taken (then located).
+    // (sequence, partition) pairs come in runs: first partition 0 of every
+    // sequence (sequence order: pair q is sequence q, located without any
+    // count, so a CTA's first item and its block-table slice load together
+    // with the context lengths), then every further full partition (sequence
+    // order, then partition order), then the partial tail partitions, class
+    // by class from the longest to the shortest -- so the items handed out
+    // last are the smallest (longest-processing-time first, without a sort).
+    // Each pair is expanded over the KV heads (item = pair * Hkv + kvh); an
+    // empty sequence's partition 0 is an item with no blocks and is skipped.
+    // For the runs after the first the warp keeps a window of 32 sequences
+    // (lane j: sequence wb + j's context length, its pair count in the
+    // current run and the pairs before it) and slides it forward as its
+    // items advance, with the next window's lengths already loaded.  A
+    // software pipeline keeps every round trip off the copy stream: while
+    // item i's stages are issued, the block-table slice of item i+1 is in
+    // flight and the index of item i+2 is taken (then located).
     PROBE_SET(0, global_timer_ns());
-    // Run sizes of the work list, counted by this warp: run 0 holds the full
-    // partitions, run 1 + k the tail partitions of class k, where a tail of nb
-    // blocks (of P16 = part / 16 per partition) has class
-    // floor(log2(floor(P16 / nb))): halves of the partition size, largest
-    // first.  Only this warp needs them, so the consumers never wait for it.
+    // Run sizes of the work list, counted by this warp: run 0 holds partition
+    // 0 of each sequence, run 1 the full partitions after it, run 2 + k the
+    // tail partitions of class k (of sequences with a full partition before
+    // them), where a tail of nb blocks (of P16 = part / 16 per partition) has
+    // class floor(log2(floor(P16 / nb))): halves of the partition size,
+    // largest first.  Only this warp needs them, so the consumers never wait
+    // for it.
     const int P16 = a.part / kBlockSize;
     auto tail_class = [&](int ctxv) -> int {
       const int tail = ctxv % a.part;
-      if (!tail) return -1;
+      if (!tail || ctxv < a.part) return -1;
       const int nb = (tail + kBlockSize - 1) / kBlockSize;
       return 31 - __clz(P16 / nb);
     };
     int* run_start = reinterpret_cast<int*>(smem + PC::kOffRuns);  // pairs before run r
+    const int N = gridDim.x;
+    // This CTA's first item (g0): partition 0 of sequence g0 / Hkv when there
+    // is one; its context length, table slice and new-row slot are loaded
+    // now, beside the windows of context lengths below.
+    const int b_first = blockIdx.x / a.Hkv;
+    const bool first_in_run0 = b_first < a.B;
+    const int ctx_first = first_in_run0 ? ctx_of(b_first) : 0;
+    const int tb_first =
+        first_in_run0 && lane < min(32, a.MBS) ? __ldg(a.block_tables + (size_t)b_first * a.MBS + lane)
+                                              : -1;
+    const bool fused = a.k_new != nullptr;
+    const long long sl_first = fused && first_in_run0 ? (long long)__ldg(a.slot_mapping + b_first) : -1ll;
     // The first two windows of context lengths are loaded once, up front, and
     // serve both this count and the walk below (a batch of up to 64 sequences
     // needs no other load).
@@ -579,25 +655,32 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
 #pragma unroll
       for (int r = 0; r < kMaxRuns; ++r) cnt[r] = 0;
       auto count = [&](int c) {
-        cnt[0] += c / a.part;
+        cnt[1] += c >= a.part ? c / a.part - 1 : 0;
         const int k = tail_class(c);
 #pragma unroll
-        for (int r = 1; r < kMaxRuns; ++r) cnt[r] += (k == r - 1) ? 1 : 0;
+        for (int r = 2; r < kMaxRuns; ++r) cnt[r] += (k == r - 2) ? 1 : 0;
       };
       count(ctx_w0);
       count(ctx_w1);
       for (int b = 64 + lane; b < a.B; b += 32) count(ctx_of(b));
       int acc = 0;
 #pragma unroll
-      for (int r = 0; r < kMaxRuns; ++r) {
+      for (int r = 1; r < kMaxRuns; ++r) {
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) cnt[r] += __shfl_xor_sync(0xffffffffu, cnt[r], o);
+      }
+      cnt[0] = a.B;
+#pragma unroll
+      for (int r = 0; r < kMaxRuns; ++r) {
         if (lane == 0) run_start[r] = acc;
         acc += cnt[r];
       }
       if (lane == 0) run_start[kMaxRuns] = acc;
       __syncwarp();
     }
+    // every K/V byte of the call is read once: evict first from L2, so the
+    // partials the merge kernel reads back stay there
+    const uint64_t kv_policy = l2_evict_first_policy();
     const T* kpool = static_cast<const T*>(a.k_cache);
     const T* vpool = static_cast<const T*>(a.v_cache);
     const T* qbase = static_cast<const T*>(a.q);
@@ -605,11 +688,12 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
     bool aborted = false;
     int items_done = 0;
 
-    int run = 0;  // 0: full partitions, 1 + k: tail partitions of class k
+    int run = 1;  // the run the window walk is in: 1 full partitions, 2 + k tails of class k
     int wb = 0, wbase = 0, w_ctx = 0, w_np = 0, w_excl = 0, w_tot = 0;
     auto set_window = [&](int ctxv) {
       w_ctx = ctxv;
-      w_np = run == 0 ? ctxv / a.part : (tail_class(ctxv) == run - 1 ? 1 : 0);
+      w_np = run == 1 ? (ctxv >= a.part ? ctxv / a.part - 1 : 0)
+                      : (tail_class(ctxv) == run - 2 ? 1 : 0);
       int incl = w_np;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -623,10 +707,31 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
     // never reloads context lengths when a new run starts.
     set_window(ctx_w0);
     int pre_ctx = ctx_w1;
+    // Partition 0 of sequence b (run 0), from its context length.
+    auto first_partition = [&](int b, int ctxb, WorkItem& it) {
+      const int nfull = ctxb / a.part;
+      it.b = b;
+      it.p = 0;
+      it.tok_end = min(ctxb, a.part);
+      it.nparts = nfull + (ctxb % a.part != 0 ? 1 : 0);
+      if constexpr (kRope || kMulti) it.ctx = ctxb;
+      if constexpr (kMulti) {
+        it.q0 = __ldg(a.query_start + b);
+        it.nq = __ldg(a.query_start + b + 1) - it.q0;
+      }
+    };
     // (sequence, partition) of pair index `pair`; false past the last pair.
-    // Pairs must be asked for in nondecreasing order.
+    // Pairs after run 0 must be asked for in nondecreasing order.
     auto locate = [&](int pair, WorkItem& it) -> bool {
       if (pair >= run_start[kMaxRuns]) return false;
+      if (pair < run_start[1]) {
+        // run 0: pair q is sequence q
+        const int ctxb = pair < 32   ? __shfl_sync(0xffffffffu, ctx_w0, pair)
+                         : pair < 64 ? __shfl_sync(0xffffffffu, ctx_w1, pair - 32)
+                                     : ctx_of(pair);
+        first_partition(pair, ctxb, it);
+        return true;
+      }
       if (pair >= run_start[run + 1]) {
         do {
           ++run;
@@ -651,8 +756,8 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
       const int ctxj = __shfl_sync(0xffffffffu, w_ctx, j);
       const int nfull = ctxj / a.part;
       it.b = wb + j;
-      it.p = run == 0 ? rel - excl : nfull;
-      it.tok_end = run == 0 ? (it.p + 1) * a.part : ctxj;
+      it.p = run == 1 ? rel - excl + 1 : nfull;
+      it.tok_end = run == 1 ? (it.p + 1) * a.part : ctxj;
       it.nparts = nfull + (ctxj % a.part != 0 ? 1 : 0);
       if constexpr (kRope || kMulti) it.ctx = ctxj;
       if constexpr (kMulti) {
@@ -674,7 +779,6 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
     // clean queue hands out 2N, 2N + 1, ... in the order CTAs ask (so a CTA
     // on a faster path takes more), and a fresh workspace falls back to the
     // fixed stride.  Each CTA's indices increase, as locate() requires.
-    const int N = gridDim.x;
     unsigned long long* queue = a.ws_ctrl + 1;
     int next_static = blockIdx.x + 2 * N;
     auto grab = [&]() -> int {  // value valid in lane 0 (dynamic) or all lanes (static)
@@ -688,15 +792,26 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
     auto bcast = [&](int raw) -> int { return dynamic ? __shfl_sync(0xffffffffu, raw, 0) : raw; };
     int g0 = blockIdx.x, g1 = g0 + N;
     WorkItem it0{}, it1{};
-    bool v0 = locate(g0 / a.Hkv, it0);
-    bool v1 = v0 && locate(g1 / a.Hkv, it1);
-    int tb0 = v0 ? load_table(it0, 0) : -1;
     // fused step: slot of the sequence's new row, needed by its last partition
-    const bool fused = a.k_new != nullptr;
     auto load_slot = [&](const WorkItem& it) -> long long {
       return fused && it.p == it.nparts - 1 ? (long long)__ldg(a.slot_mapping + it.b) : -1ll;
     };
-    long long sl0 = v0 ? load_slot(it0) : -1ll;
+    bool v0;
+    int tb0 = -1;
+    long long sl0 = -1ll;
+    if (first_in_run0) {
+      // the loads issued above: no round trip between the counts and the
+      // first copies
+      first_partition(b_first, ctx_first, it0);
+      v0 = true;
+      tb0 = tb_first;
+      sl0 = it0.nparts == 1 ? sl_first : -1ll;
+    } else {
+      v0 = locate(g0 / a.Hkv, it0);
+      tb0 = v0 ? load_table(it0, 0) : -1;
+      sl0 = v0 ? load_slot(it0) : -1ll;
+    }
+    bool v1 = v0 && locate(g1 / a.Hkv, it1);
     while (v0 && !aborted) {
       // The next item's table slice and slot load while this item's stages
       // are issued; the item after it is taken from the queue now and
@@ -745,7 +860,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
         const int new_phys = __shfl_sync(0xffffffffu, phys, new_lane >= 0 ? new_lane : 0);
         const int new_rows = __shfl_sync(0xffffffffu, rows, new_lane >= 0 ? new_lane : 0);
         // tensor-map copies move whole 16-row boxes; the new row rides beside them
-        int bytes = valid ? 2 * ((kMma && !kFp8) ? kBlockSize : rows) * D * PC::kElemBytes : 0;
+        int bytes = valid ? 2 * (kMma ? kBlockSize : rows) * D * PC::kElemBytes : 0;
         if (kMma && new_here) bytes += 2 * D * (int)sizeof(T);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) bytes += __shfl_xor_sync(0xffffffffu, bytes, o);
@@ -775,21 +890,20 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
         __syncwarp();
         unsigned char* stage = smem + PC::kOffKV + slot * PC::kStageBytes;
         if (kFp8 && valid) {
-          // the block's valid code rows, one contiguous run per K and V
-          const size_t src = ((size_t)phys * a.Hkv + kvh) * PC::kBlockBytes;
-          const uint32_t nbytes = (uint32_t)(rows * D);
-          bulk_copy_g2s(stage + lane * PC::kBlockBytes,
-                        static_cast<const unsigned char*>(a.k_cache) + src, nbytes, &full[slot]);
-          bulk_copy_g2s(stage + (NC + lane) * PC::kBlockBytes,
-                        static_cast<const unsigned char*>(a.v_cache) + src, nbytes, &full[slot]);
+          // one box of 16 code rows per K and V, swizzled (code_chunk)
+          const int y = (phys * a.Hkv + kvh) * kBlockSize;
+          tma_load_box_hint(smem_addr(stage + lane * PC::kBlockBytes), &tmk, 0, y, &full[slot],
+                            kv_policy);
+          tma_load_box_hint(smem_addr(stage + (NC + lane) * PC::kBlockBytes), &tmv, 0, y,
+                            &full[slot], kv_policy);
         } else if (kMma && valid) {
           const int y = (phys * a.Hkv + kvh) * kBlockSize;
           const uint32_t kd = smem_addr(stage + lane * PC::kBlockBytes);
           const uint32_t vd = smem_addr(stage + (NC + lane) * PC::kBlockBytes);
 #pragma unroll
           for (int hx = 0; hx < D / 64; ++hx) {
-            tma_load_box(kd + hx * 2048, &tmk, hx * 64, y, &full[slot]);
-            tma_load_box(vd + hx * 2048, &tmv, hx * 64, y, &full[slot]);
+            tma_load_box_hint(kd + hx * 2048, &tmk, hx * 64, y, &full[slot], kv_policy);
+            tma_load_box_hint(vd + hx * 2048, &tmv, hx * 64, y, &full[slot], kv_policy);
           }
           if (new_here) {
             const size_t nsrc = ((size_t)it0.b * a.Hkv + kvh) * D;
@@ -803,8 +917,10 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
           const int cache_rows = new_here ? rows - 1 : rows;
           const uint32_t nbytes = (uint32_t)(cache_rows * D * (int)sizeof(T));
           if (nbytes) {
-            bulk_copy_g2s(stage + lane * PC::kBlockBytes, kpool + src, nbytes, &full[slot]);
-            bulk_copy_g2s(stage + (NC + lane) * PC::kBlockBytes, vpool + src, nbytes, &full[slot]);
+            bulk_copy_g2s_hint(stage + lane * PC::kBlockBytes, kpool + src, nbytes, &full[slot],
+                               kv_policy);
+            bulk_copy_g2s_hint(stage + (NC + lane) * PC::kBlockBytes, vpool + src, nbytes,
+                               &full[slot], kv_policy);
           }
           if (new_here) {
             const size_t nsrc = ((size_t)it0.b * a.Hkv + kvh) * D;
@@ -965,10 +1081,13 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
             if (lane + 32 * i < D / 2) kcs.w[i] = cs_row[lane + 32 * i];
         }
       } else {
+        // e4m3 cache: the k-steps walk each 16-dim chunk in the order the
+        // widened code pairs come in (attend_block_mma, kCodes)
+        const int lo = kFp8 ? 2 * t2 : t2, hi = kFp8 ? 2 * t2 + 2 : t2 + 8;
 #pragma unroll
         for (int kk = 0; kk < (kMma ? D / 16 : 1); ++kk) {
-          tq[kk][0] = slot_g < PC::kSlots ? q32[(slot_g * D + 16 * kk + t2) / 2] : 0u;
-          tq[kk][1] = slot_g < PC::kSlots ? q32[(slot_g * D + 16 * kk + t2 + 8) / 2] : 0u;
+          tq[kk][0] = slot_g < PC::kSlots ? q32[(slot_g * D + 16 * kk + lo) / 2] : 0u;
+          tq[kk][1] = slot_g < PC::kSlots ? q32[(slot_g * D + 16 * kk + hi) / 2] : 0u;
         }
       }
 #pragma unroll
@@ -1011,42 +1130,21 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
       }
     }
     if (kFp8 && warp < h.nblk && ((h.flags >> (8 + warp)) & 1)) {
-      // fp8 cache: widen this warp's K and V code block into its fp16 scratch
-      // (the swizzled layout the tensor-core math reads); rows past the
-      // context become zeros (their V must not carry NaN into the sums)
-      const unsigned char* const k8 =
-          smem + PC::kOffKV + slot * PC::kStageBytes + warp * PC::kBlockBytes;
-      const unsigned char* const v8 = k8 + NC * PC::kBlockBytes;
-      unsigned char* const kw = smem + PC::kOffWide + warp * 2 * PC::kWideBytes;
-      unsigned char* const vw = kw + PC::kWideBytes;
+      // fp8 cache: the K and V code blocks are used as they landed; the V
+      // rows past the context (the box brought whatever the pool holds
+      // there) are zeroed first, since 0 x NaN would reach the sums
+      unsigned char* const kb = smem + PC::kOffKV + slot * PC::kStageBytes + warp * PC::kBlockBytes;
+      unsigned char* const vb = kb + NC * PC::kBlockBytes;
       const int n_valid = min(kBlockSize, h.tok_end - (h.blk0 + warp) * kBlockSize);
-      // lane: row lane / 2, and in every group of 32 codes of that row the 16
-      // at 16 * (lane % 2); step j takes group jj, rotated by the row (and
-      // the lane's half at d = 128) so that the eight lanes of each quarter
-      // warp hit eight different bank groups with their 16-byte loads and
-      // with both scratch stores
-      const int row = lane >> 1, half = lane & 1;
-#pragma unroll
-      for (int j = 0; j < D / 32; ++j) {
-        const int jj = D == 128 ? (j + row + half) & 3 : (j + (row >> 1)) & 1;
-        const int col = 32 * jj + 16 * half;         // first code of this 16-byte load
-        uint4 kq = make_uint4(0u, 0u, 0u, 0u), vq = make_uint4(0u, 0u, 0u, 0u);
-        if (row < n_valid) {
-          kq = *reinterpret_cast<const uint4*>(k8 + row * D + col);
-          vq = *reinterpret_cast<const uint4*>(v8 + row * D + col);
-        }
-        uint4 lo, hi;
-        widen_e4m3x16(kq, lo, hi);
-        *reinterpret_cast<uint4*>(kw + blk_chunk(row, col / 8)) = lo;
-        *reinterpret_cast<uint4*>(kw + blk_chunk(row, col / 8 + 1)) = hi;
-        widen_e4m3x16(vq, lo, hi);
-        *reinterpret_cast<uint4*>(vw + blk_chunk(row, col / 8)) = lo;
-        *reinterpret_cast<uint4*>(vw + blk_chunk(row, col / 8 + 1)) = hi;
+      if (n_valid < kBlockSize) {
+        for (int i = lane; i < (kBlockSize - n_valid) * (D / 16); i += 32)
+          *reinterpret_cast<uint4*>(vb + n_valid * D + i * 16) = make_uint4(0u, 0u, 0u, 0u);
+        fence_proxy_async_smem();  // the stage is refilled by tensor copies later
+        __syncwarp();
       }
-      __syncwarp();
       if constexpr (kFp8)
-        attend_block_mma<T, D, false, false>(smem_addr(kw), smem_addr(vw), n_valid, a.qscale, tq,
-                                             tq, tm, tl, to, lane, 0, tlim);
+        attend_block_mma<T, D, false, false, true>(smem_addr(kb), smem_addr(vb), n_valid,
+                                                   a.qscale, tq, tq, tm, tl, to, lane, 0, tlim);
     } else if (kMma && warp < h.nblk && ((h.flags >> (8 + warp)) & 1)) {
       unsigned char* const kb = smem + PC::kOffKV + slot * PC::kStageBytes + warp * PC::kBlockBytes;
       unsigned char* const vb = kb + NC * PC::kBlockBytes;
@@ -1162,8 +1260,10 @@ __global__ void __launch_bounds__((NC + 1) * 32, 1)
         if (g < nslots) {
 #pragma unroll
           for (int i = 0; i < (kMma ? D / 16 : 1); ++i) {
-            po_row(warp, g)[16 * i + r] = to[i][j];
-            po_row(warp, g)[16 * i + r + 8] = to[i][2 + j];
+            // accumulator rows r and r + 8 of tile i: dims 16i + r and
+            // 16i + r + 8, or 16i + 2r and 16i + 2r + 1 over an e4m3 cache
+            po_row(warp, g)[16 * i + (kFp8 ? 2 * r : r)] = to[i][j];
+            po_row(warp, g)[16 * i + (kFp8 ? 2 * r + 1 : r + 8)] = to[i][2 + j];
           }
           if (r == 0) {
             pm[warp * kSl + g] = tm[j];
@@ -1302,6 +1402,9 @@ __global__ void __launch_bounds__(kMergeWarps * 32) paged_decode_merge_kernel(co
   const int b = live ? bh / a.Hq : 0, hq = live ? bh % a.Hq : 0;
   const int ctx = live ? __ldg(a.context_lens + b) : 0;
   const int span = a.MBS * kBlockSize;
+#ifdef PHOTON_PROBE
+  if (threadIdx.x == 0 && blockIdx.x < 4096) g_probe_merge[blockIdx.x][0] = global_timer_ns();
+#endif
   // the sequence's output rows: decode, row b; few-token mode, rows q0 .. q0 + n - 1
   int q0 = b, n = 1;
   bool skip = !live;
@@ -1334,6 +1437,9 @@ __global__ void __launch_bounds__(kMergeWarps * 32) paged_decode_merge_kernel(co
     skip = true;
   }
   pdl_wait_primary();
+#ifdef PHOTON_PROBE
+  if (threadIdx.x == 0 && blockIdx.x < 4096) g_probe_merge[blockIdx.x][1] = global_timer_ns();
+#endif
   if (blockIdx.x == 0 && threadIdx.x == 0) {
     // The attention grid is done handing out items: leave the queue clean for
     // the next call.
@@ -1406,6 +1512,9 @@ __global__ void __launch_bounds__(kMergeWarps * 32) paged_decode_merge_kernel(co
 #pragma unroll
     for (int e = 0; e < EPL; ++e) out[e] = Elem<T>::narrow(O[e] * inv);
   }
+#ifdef PHOTON_PROBE
+  if (lane == 0 && blockIdx.x < 4096) g_probe_merge[blockIdx.x][2] = global_timer_ns();
+#endif
 }
 
 // Resident CTAs per SM of an attention-kernel instantiation (queried once per
@@ -1523,10 +1632,12 @@ cudaError_t launch_decode_impl(const DecodeArgs& a0, cudaStream_t stream) {
   return cudaSuccess;
 }
 
-// The e4m3 cache: stages of 4 fp8 blocks per K and V (8 KB at d = 64, 16 KB at
-// d = 128) in a 64 KB ring, which leaves room for the consumers' fp16
-// scratch at two CTAs per SM.
-constexpr int kRingBytesFp8 = 64 * 1024;
+// The e4m3 cache: stages of 4 code blocks per K and V (8 KB at d = 64, 16 KB at
+// d = 128) in a 64 KB ring, so that three CTAs share an SM.
+#ifndef PHOTON_RING_KB_FP8
+#define PHOTON_RING_KB_FP8 64
+#endif
+constexpr int kRingBytesFp8 = PHOTON_RING_KB_FP8 * 1024;
 
 template <int D, int G>
 cudaError_t launch_decode_fp8_impl(const DecodeArgs& a, cudaStream_t stream) {
@@ -1537,11 +1648,14 @@ cudaError_t launch_decode_fp8_impl(const DecodeArgs& a, cudaStream_t stream) {
       !a.ws_m || !a.ws_l || !a.ws_o || !a.ws_ctrl || !a.err || a.k_new || a.rope_cs ||
       a.query_start)
     return cudaErrorInvalidValue;
-  CUtensorMap unused;
-  memset(&unused, 0, sizeof(unused));
+  if ((int64_t)a.NB * a.Hkv * kBlockSize > INT32_MAX) return cudaErrorInvalidValue;
+  CUtensorMap tk, tv;
+  if (make_pool_map(&tk, a.k_cache, 3, a.NB, a.Hkv, D) != cudaSuccess ||
+      make_pool_map(&tv, a.v_cache, 3, a.NB, a.Hkv, D) != cudaSuccess)
+    return cudaErrorInvalidValue;
   if (a.ev_start) cudaEventRecord(a.ev_start, stream);
   cudaError_t err = launch_attention<__half, D, G, NC, S, false, true, false, true>(
-      a, unused, unused, stream);
+      a, tk, tv, stream);
   if (err != cudaSuccess) return err;
   err = launch_pdl(paged_decode_merge_kernel<__half, D>,
                    dim3((a.B * a.Hq + kMergeWarps - 1) / kMergeWarps), dim3(kMergeWarps * 32), 0,

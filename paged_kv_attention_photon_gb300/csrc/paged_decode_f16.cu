@@ -19,4 +19,7 @@ cudaError_t launch_paged_decode_fp8(const DecodeArgs& a, cudaStream_t stream) {
 extern "C" int photon_probe_read(void* dst, size_t bytes) {
   return (int)cudaMemcpyFromSymbol(dst, photon::g_probe, bytes);
 }
+extern "C" int photon_probe_merge_read(void* dst, size_t bytes) {
+  return (int)cudaMemcpyFromSymbol(dst, photon::g_probe_merge, bytes);
+}
 #endif

@@ -327,6 +327,25 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
       : "memory");
 }
 
+// L2 policy for data read exactly once (the K/V stream of a decode): evict
+// first, so that it does not push out what is read again soon (the split-KV
+// partials the merge reads).  A hint only: no effect on values.
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// 1-D bulk copy with an L2 cache policy (see bulk_copy_g2s).
+__device__ __forceinline__ void bulk_copy_g2s_hint(void* dst, const void* src, uint32_t bytes,
+                                                   uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], "
+      "%2, [%3], %4;" ::"r"(smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+
 // Hint: bring a line into L2 (no architectural effect on values).
 __device__ __forceinline__ void prefetch_l2(const void* p) {
   asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
@@ -342,8 +361,10 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 
 // ------------------------------------------------------------------ tensor copies and warp MMA
 // Tensor map over a K or V pool seen as rows of head_dim elements:
-// (num_blocks x Hkv x 16) rows, box 16 rows x 64 elements, 128-byte swizzle
-// (dtype 1 = fp16, 2 = bf16).  Defined in multi_query_tc.cu.
+// (num_blocks x Hkv x 16) rows; dtype 1 = fp16, 2 = bf16: box 16 rows x 64
+// elements, 128-byte swizzle; dtype 3 = e4m3 codes: box 16 rows x head_dim
+// codes, 128-byte swizzle at head_dim 128, 64-byte at 64.  Defined in
+// multi_query_tc.cu.
 cudaError_t make_pool_map(CUtensorMap* map, const void* pool, int dtype, int NB, int Hkv, int D);
 
 // 2-D tiled bulk tensor copy of one box into this CTA's shared memory,
@@ -354,6 +375,16 @@ __device__ __forceinline__ void tma_load_box(uint32_t dst, const CUtensorMap* ma
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
       "%3}], [%4];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar))
+      : "memory");
+}
+
+// tma_load_box with an L2 cache policy.
+__device__ __forceinline__ void tma_load_box_hint(uint32_t dst, const CUtensorMap* map, int x,
+                                                  int y, uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar)), "l"(policy)
       : "memory");
 }
 
