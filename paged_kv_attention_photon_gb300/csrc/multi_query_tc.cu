@@ -309,7 +309,7 @@ __device__ __forceinline__ void tc_item_of(const MultiQueryArgs& a, int G, int& 
 // per-chunk timeline of one CTA (the last tile of KV head 0 of the last
 // sequence) and the start and end of every CTA.
 constexpr int kTcProbeChunks = 160;
-static __device__ unsigned long long g_tc_probe[kTcProbeChunks][8];
+static __device__ unsigned long long g_tc_probe[kTcProbeChunks][16];
 static __device__ unsigned long long g_tc_cta[4096][2];
 #define TC_PROBE(c, i)                                                                \
   do {                                                                               \
@@ -525,6 +525,7 @@ __global__ void __launch_bounds__(TcCfg<T, D>::kThreads)
                      kk > 0);
             }
             tc_commit(&s_full[t][c & 1]);
+            TC_PROBE(c, 8 + t);
           }
         }
         if (!ok) break;
@@ -534,8 +535,10 @@ __global__ void __launch_bounds__(TcCfg<T, D>::kThreads)
         // P V of the previous chunk, tile by tile, once its V landed and its
         // weights are written
         const int pc = c - 1, pst = pc % SV, pb = pc & 1;
+        if (lane == 0) TC_PROBE(pc, 10);
         ok = lane0_ok(mbar_wait_bounded(&v_full[pst], (pc / SV) & 1));
         if (!ok) break;
+        if (lane == 0) TC_PROBE(pc, 11);
         // zero the V rows past the last key (a partial or missing block):
         // they are multiplied by zero weights, and 0 x NaN would not vanish
         const int tail = tail_rows[pst];
@@ -561,6 +564,7 @@ __global__ void __launch_bounds__(TcCfg<T, D>::kThreads)
                      sw128_mn_desc(sV + pst * C::kVBytes + kk * 2048), id_o,
                      (pc > 0 || kk > 0) ? 1u : 0u);
             tc_commit(&p_done[t][pb]);
+            TC_PROBE(pc, 12 + t);
           }
         }
         if (!ok) break;
@@ -665,7 +669,7 @@ __global__ void __launch_bounds__(TcCfg<T, D>::kThreads)
             make_uint4(w[0], w[1], w[2], w[3]);
       }
       l_run += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
-      if (lane == 0 && warp == 0) TC_PROBE(c, 2);
+      if (lane == 0 && (warp == 0 || warp == 4)) TC_PROBE(c, warp == 0 ? 2 : 14);
       fence_async_smem();
       mbar_arrive_cnt(&p_full[t][c & 1]);
     }

@@ -88,9 +88,34 @@ struct StageHdr {
 };
 enum : int { kFirst = 1, kLast = 2, kDone = 4 };
 
+// Split-KV partitions of a context of ctx tokens with partition size part:
+// nfull = ctx / part full partitions, then the remainder.  When there are two
+// or more full ones the last of them is cut in two halves (of part / 32 * 16
+// tokens and the rest), so that the work list can end with small items:
+// partitions 0 .. nfull - 2 full, nfull - 1 and nfull the halves, nfull + 1
+// the remainder.
+__host__ __device__ __forceinline__ int partition_split(int ctx, int part) {
+  return ctx / part >= 2 && part >= 32 ? 1 : 0;
+}
+__host__ __device__ __forceinline__ int partitions_of(int ctx, int part) {
+  return ctx / part + partition_split(ctx, part) + (ctx % part != 0 ? 1 : 0);
+}
+__device__ __forceinline__ void partition_range(int ctx, int part, int p, int& begin, int& end) {
+  const int nfull = ctx / part;
+  if (!partition_split(ctx, part) || p < nfull - 1) {
+    begin = p * part;
+    end = min(begin + part, ctx);
+    return;
+  }
+  const int last = (nfull - 1) * part, half = part / 32 * 16;
+  begin = p == nfull - 1 ? last : p == nfull ? last + half : nfull * part;
+  end = p == nfull - 1 ? last + half : p == nfull ? nfull * part : ctx;
+}
+
 // Runs of the work list: partition 0 of every sequence, the further full
-// partitions, then up to log2(4096/16) + 1 = 9 classes of tail partitions.
-constexpr int kMaxRuns = 11;
+// partitions, the halves of the last full ones, then up to log2(4096/16) + 1
+// = 9 classes of tail partitions.
+constexpr int kMaxRuns = 12;
 
 // Persistent-kernel geometry: NC consumer warps, 1 producer warp, S ring stages.
 // M: the tensor-core consumer, whose blocks arrive as swizzled tensor-map
@@ -511,6 +536,17 @@ constexpr int kProbeSlots = 48;  // [8 + 2k]: item k's first copy issued, [9 + 2
 static __device__ unsigned long long g_probe[kProbeCtas][kProbeSlots];
 // merge kernel CTAs: [0] entry, [1] past the dependency wait, [2] done
 static __device__ unsigned long long g_probe_merge[4096][4];
+// a one-thread kernel's time stamp, launched by the tuning harness just
+// before a call (the gap to the attention kernel's entry is its launch)
+static __device__ unsigned long long g_probe_stamp;
+static __global__ void probe_stamp_kernel() { g_probe_stamp = global_timer_ns(); }
+// the same with a large shared-memory request (the carveout of the attention
+// kernel), to tell a launch's own cost from a carveout change
+static __global__ void probe_stamp_big_kernel() {
+  extern __shared__ unsigned char stamp_smem[];
+  stamp_smem[threadIdx.x] = 0;
+  g_probe_stamp = global_timer_ns();
+}
 #define PROBE_SET(i, v) \
   do { if (blockIdx.x < kProbeCtas && (i) < kProbeSlots) g_probe[blockIdx.x][i] = (v); } while (0)
 #else
@@ -528,12 +564,17 @@ static __device__ unsigned long long g_probe_merge[4096][4];
 // kMulti: the few-token multi-query mode (photon_paged_multi_query with
 // max_query_len * G <= 8): an item's query slots are the (token, head) pairs
 // of its sequence's n query tokens, each with its causal limit.
-// kFp8: the e4m3 cache (photon_paged_decode_fp8): K/V blocks arrive by bulk
-// copy as codes, each consumer warp widens its pair into its fp16 scratch;
-// the K scale is folded into qscale, the V scale into the item's combine.
+// kFp8: the e4m3 cache (photon_paged_decode_fp8): K/V blocks arrive as
+// swizzled tensor-map boxes of codes, and the block math widens the codes it
+// needs in registers; the K scale is folded into qscale, the V scale into
+// the item's combine.  Three CTAs share an SM (PHOTON_FP8_CTAS, a tuning
+// knob for the register cap).
+#ifndef PHOTON_FP8_CTAS
+#define PHOTON_FP8_CTAS 3
+#endif
 template <typename T, int D, int G, int NC, int S, bool kRope, bool kMma, bool kMulti,
           bool kFp8 = false>
-__global__ void __launch_bounds__((NC + 1) * 32, kFp8 && NC <= 4 ? 3 : 1)
+__global__ void __launch_bounds__((NC + 1) * 32, kFp8 && NC <= 4 ? PHOTON_FP8_CTAS : 1)
     paged_decode_attention_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmk,
                                   const __grid_constant__ CUtensorMap tmv) {
   using PC = PersistCfg<T, D, G, NC, S, kRope, kMma, kMulti, kFp8>;
@@ -549,6 +590,11 @@ __global__ void __launch_bounds__((NC + 1) * 32, kFp8 && NC <= 4 ? 3 : 1)
   StageHdr* hdr = reinterpret_cast<StageHdr*>(smem + PC::kOffHdr);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (threadIdx.x == 0) PROBE_SET(5, global_timer_ns());
+  // the producer's first tensor copies need the maps' descriptors
+  if (kMma && threadIdx.x == NC * 32) {
+    prefetch_tensor_map(&tmk);
+    prefetch_tensor_map(&tmv);
+  }
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -618,12 +664,13 @@ __global__ void __launch_bounds__((NC + 1) * 32, kFp8 && NC <= 4 ? 3 : 1)
     // flight and the index of item i+2 is taken (then located).
     PROBE_SET(0, global_timer_ns());
     // Run sizes of the work list, counted by this warp: run 0 holds partition
-    // 0 of each sequence, run 1 the full partitions after it, run 2 + k the
-    // tail partitions of class k (of sequences with a full partition before
-    // them), where a tail of nb blocks (of P16 = part / 16 per partition) has
-    // class floor(log2(floor(P16 / nb))): halves of the partition size,
-    // largest first.  Only this warp needs them, so the consumers never wait
-    // for it.
+    // 0 of each sequence, run 1 the full partitions after it, run 2 the two
+    // halves of each sequence's last full partition (partition_split), run
+    // 3 + k the tail partitions of class k (of sequences with a full
+    // partition before them), where a tail of nb blocks (of P16 = part / 16
+    // per partition) has class floor(log2(floor(P16 / nb))): halves of the
+    // partition size, largest first.  Only this warp needs them, so the
+    // consumers never wait for it.
     const int P16 = a.part / kBlockSize;
     auto tail_class = [&](int ctxv) -> int {
       const int tail = ctxv % a.part;
@@ -655,10 +702,12 @@ __global__ void __launch_bounds__((NC + 1) * 32, kFp8 && NC <= 4 ? 3 : 1)
 #pragma unroll
       for (int r = 0; r < kMaxRuns; ++r) cnt[r] = 0;
       auto count = [&](int c) {
-        cnt[1] += c >= a.part ? c / a.part - 1 : 0;
+        const int split = partition_split(c, a.part);
+        cnt[1] += c >= a.part ? c / a.part - 1 - split : 0;
+        cnt[2] += 2 * split;
         const int k = tail_class(c);
 #pragma unroll
-        for (int r = 2; r < kMaxRuns; ++r) cnt[r] += (k == r - 2) ? 1 : 0;
+        for (int r = 3; r < kMaxRuns; ++r) cnt[r] += (k == r - 3) ? 1 : 0;
       };
       count(ctx_w0);
       count(ctx_w1);
@@ -678,6 +727,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, kFp8 && NC <= 4 ? 3 : 1)
       if (lane == 0) run_start[kMaxRuns] = acc;
       __syncwarp();
     }
+    PROBE_SET(6, global_timer_ns());
     // every K/V byte of the call is read once: evict first from L2, so the
     // partials the merge kernel reads back stay there
     const uint64_t kv_policy = l2_evict_first_policy();
@@ -688,12 +738,15 @@ __global__ void __launch_bounds__((NC + 1) * 32, kFp8 && NC <= 4 ? 3 : 1)
     bool aborted = false;
     int items_done = 0;
 
-    int run = 1;  // the run the window walk is in: 1 full partitions, 2 + k tails of class k
+    // the run the window walk is in: 1 full partitions, 2 halves, 3 + k tails of class k
+    int run = 1;
     int wb = 0, wbase = 0, w_ctx = 0, w_np = 0, w_excl = 0, w_tot = 0;
     auto set_window = [&](int ctxv) {
       w_ctx = ctxv;
-      w_np = run == 1 ? (ctxv >= a.part ? ctxv / a.part - 1 : 0)
-                      : (tail_class(ctxv) == run - 2 ? 1 : 0);
+      const int split = partition_split(ctxv, a.part);
+      w_np = run == 1   ? (ctxv >= a.part ? ctxv / a.part - 1 - split : 0)
+             : run == 2 ? 2 * split
+                        : (tail_class(ctxv) == run - 3 ? 1 : 0);
       int incl = w_np;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -709,11 +762,11 @@ __global__ void __launch_bounds__((NC + 1) * 32, kFp8 && NC <= 4 ? 3 : 1)
     int pre_ctx = ctx_w1;
     // Partition 0 of sequence b (run 0), from its context length.
     auto first_partition = [&](int b, int ctxb, WorkItem& it) {
-      const int nfull = ctxb / a.part;
       it.b = b;
       it.p = 0;
+      it.tok_begin = 0;
       it.tok_end = min(ctxb, a.part);
-      it.nparts = nfull + (ctxb % a.part != 0 ? 1 : 0);
+      it.nparts = partitions_of(ctxb, a.part);
       if constexpr (kRope || kMulti) it.ctx = ctxb;
       if constexpr (kMulti) {
         it.q0 = __ldg(a.query_start + b);
@@ -756,9 +809,11 @@ __global__ void __launch_bounds__((NC + 1) * 32, kFp8 && NC <= 4 ? 3 : 1)
       const int ctxj = __shfl_sync(0xffffffffu, w_ctx, j);
       const int nfull = ctxj / a.part;
       it.b = wb + j;
-      it.p = run == 1 ? rel - excl + 1 : nfull;
-      it.tok_end = run == 1 ? (it.p + 1) * a.part : ctxj;
-      it.nparts = nfull + (ctxj % a.part != 0 ? 1 : 0);
+      it.p = run == 1   ? rel - excl + 1
+             : run == 2 ? nfull - 1 + (rel - excl)
+                        : nfull + partition_split(ctxj, a.part);
+      partition_range(ctxj, a.part, it.p, it.tok_begin, it.tok_end);
+      it.nparts = partitions_of(ctxj, a.part);
       if constexpr (kRope || kMulti) it.ctx = ctxj;
       if constexpr (kMulti) {
         // first used two items later: the loads stay off this path
@@ -769,8 +824,8 @@ __global__ void __launch_bounds__((NC + 1) * 32, kFp8 && NC <= 4 ? 3 : 1)
     };
     // Lane j holds the physical block of logical block (chunk*32 + j) of the item.
     auto load_table = [&](const WorkItem& it, int chunk) -> int {
-      const int blk0 = it.p * (a.part / kBlockSize);
-      const int nblk = (it.tok_end - it.p * a.part + kBlockSize - 1) / kBlockSize;
+      const int blk0 = it.tok_begin / kBlockSize;
+      const int nblk = (it.tok_end - it.tok_begin + kBlockSize - 1) / kBlockSize;
       const int j = chunk * 32 + lane;
       return j < nblk ? __ldg(a.block_tables + (size_t)it.b * a.MBS + blk0 + j) : -1;
     };
@@ -821,7 +876,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, kFp8 && NC <= 4 ? 3 : 1)
       const int g2raw = grab();
 
       const int kvh = g0 % a.Hkv;
-      const int tok_begin = it0.p * a.part;
+      const int tok_begin = it0.tok_begin;
       const int blk0 = tok_begin / kBlockSize;
       const int nblk = (it0.tok_end - tok_begin + kBlockSize - 1) / kBlockSize;
       const size_t head_off = (size_t)kvh * PC::kBlockElems;
@@ -1447,7 +1502,7 @@ __global__ void __launch_bounds__(kMergeWarps * 32) paged_decode_merge_kernel(co
     a.ws_ctrl[0] = kQueueReady;
   }
   if (skip) return;
-  const int nparts = (ctx + a.part - 1) / a.part;
+  const int nparts = partitions_of(ctx, a.part);
   if (nparts < 2) return;                             // the attention kernel wrote out
 
   {

@@ -95,10 +95,15 @@ int partition_of(const photon_paged_shape_t* s, int kv_bytes = 0) {
   return part;
 }
 
+// Partitions of the longest context the shape allows: its full partitions,
+// one more when the last full one is cut in halves (two or more full ones,
+// partition size >= 32: the attention kernel's partition_split), and the
+// remainder.
 int max_partitions_of(const photon_paged_shape_t* s, int kv_bytes = 0) {
   const int64_t span = (int64_t)s->max_blocks_per_seq * s->block_size;
   const int part = partition_of(s, kv_bytes);
-  return (int)((span + part - 1) / part);
+  const int64_t nfull = span / part;
+  return (int)(nfull + (nfull >= 2 && part >= 32 ? 1 : 0) + (span % part != 0 ? 1 : 0));
 }
 
 // Workspace: [queue control][m][l][o] (the last three per query row, q head

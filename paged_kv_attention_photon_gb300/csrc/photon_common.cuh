@@ -99,11 +99,11 @@ __device__ __forceinline__ uint4 ld_stream16(const void* p) {
 }
 
 // ------------------------------------------------------------------ launches
-// One partition p of sequence b (the KV head is added by the kernel).  tok_end
-// is the exclusive end of the partition's token range, nparts the number of
-// partitions of the sequence.
+// One partition p of sequence b (the KV head is added by the kernel):
+// tokens [tok_begin, tok_end); nparts is the number of partitions of the
+// sequence.
 struct WorkItem {
-  int b, p, tok_end, nparts, ctx;
+  int b, p, tok_begin, tok_end, nparts, ctx;
   int q0, nq;  // few-token multi-query mode: the sequence's first query row and count
 };
 
@@ -386,6 +386,12 @@ __device__ __forceinline__ void tma_load_box_hint(uint32_t dst, const CUtensorMa
       "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar)), "l"(policy)
       : "memory");
+}
+
+// Brings a tensor map (a __grid_constant__ kernel parameter) into the copy
+// unit's descriptor cache ahead of its first use.  A hint only.
+__device__ __forceinline__ void prefetch_tensor_map(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
 // Orders this thread's generic-proxy shared-memory accesses before later

@@ -106,10 +106,11 @@ def test_fp8_validation(lib):
     assert dec(s, q=None) == 1
     assert dec(s, ws_bytes=16) == 4
     assert dec(_shape(num_seqs=0)) == 0
-    # fp8 partitions hold twice the tokens: half the fp16 decode's partials
+    # fp8 partitions hold twice the tokens: about half the fp16 decode's
+    # partials (each has one more for the halved last full partition)
     big = _shape(num_seqs=64, max_blocks_per_seq=512)
     assert 2 * lib.photon_paged_decode_fp8_workspace_size(ctypes.byref(big)) \
-        <= lib.photon_paged_decode_workspace_size(ctypes.byref(big)) + 1024
+        <= 1.1 * lib.photon_paged_decode_workspace_size(ctypes.byref(big))
     assert lib.photon_paged_decode_fp8_workspace_size(ctypes.byref(_shape(dtype=P.BF16))) == 0
 
 
@@ -124,9 +125,10 @@ def test_gather_validation(lib):
 def test_workspace_size_and_plan(lib):
     s = _shape(num_seqs=64, max_blocks_per_seq=512, partition_size=256)
     pl = P.photon_paged_decode_plan(s)
-    assert pl["partition_size"] == 256 and pl["max_partitions"] == 32
+    # 8192 tokens: 32 full partitions of 256, the last one cut in two halves
+    assert pl["partition_size"] == 256 and pl["max_partitions"] == 33
     ws = P.photon_paged_decode_workspace_size(s)
-    rows = 64 * 16 * 32
+    rows = 64 * 16 * 33
     assert ws >= rows * (128 + 2) * 4
     assert ws % 256 == 0
     assert P.photon_paged_decode_workspace_size(_shape(head_dim=96)) == 0
