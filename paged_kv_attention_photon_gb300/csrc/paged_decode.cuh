@@ -697,7 +697,10 @@ __global__ void __launch_bounds__((NC + 1) * 32, kFp8 && NC <= 4 ? PHOTON_FP8_CT
     const int ctx_w0 = ctx_of(lane), ctx_w1 = ctx_of(32 + lane);
     const bool dynamic =
         __shfl_sync(0xffffffffu, lane == 0 && a.ws_ctrl[0] == kQueueReady ? 1 : 0, 0) != 0;
-    {
+    // The run sizes (the second item on needs them).  When the first item is
+    // partition 0 of a sequence, they are counted right after its first
+    // stage is issued, so the counting stays off the path to the first copy.
+    auto count_runs = [&]() {
       int cnt[kMaxRuns];
 #pragma unroll
       for (int r = 0; r < kMaxRuns; ++r) cnt[r] = 0;
@@ -726,8 +729,8 @@ __global__ void __launch_bounds__((NC + 1) * 32, kFp8 && NC <= 4 ? PHOTON_FP8_CT
       }
       if (lane == 0) run_start[kMaxRuns] = acc;
       __syncwarp();
-    }
-    PROBE_SET(6, global_timer_ns());
+      PROBE_SET(6, global_timer_ns());
+    };
     // every K/V byte of the call is read once: evict first from L2, so the
     // partials the merge kernel reads back stay there
     const uint64_t kv_policy = l2_evict_first_policy();
@@ -854,26 +857,34 @@ __global__ void __launch_bounds__((NC + 1) * 32, kFp8 && NC <= 4 ? PHOTON_FP8_CT
     bool v0;
     int tb0 = -1;
     long long sl0 = -1ll;
-    if (first_in_run0) {
-      // the loads issued above: no round trip between the counts and the
-      // first copies
+    bool counted = false;
+    if (first_in_run0 && ctx_first > 0) {
+      // the loads issued above: the first copies need nothing else
       first_partition(b_first, ctx_first, it0);
       v0 = true;
       tb0 = tb_first;
       sl0 = it0.nparts == 1 ? sl_first : -1ll;
     } else {
+      count_runs();
+      counted = true;
       v0 = locate(g0 / a.Hkv, it0);
       tb0 = v0 ? load_table(it0, 0) : -1;
       sl0 = v0 ? load_slot(it0) : -1ll;
     }
-    bool v1 = v0 && locate(g1 / a.Hkv, it1);
+    bool v1 = counted && v0 && locate(g1 / a.Hkv, it1);
     while (v0 && !aborted) {
       // The next item's table slice and slot load while this item's stages
       // are issued; the item after it is taken from the queue now and
       // located once they are, so a CTA commits to at most two items ahead.
-      const int tb1 = v1 ? load_table(it1, 0) : -1;
-      const long long sl1 = v1 ? load_slot(it1) : -1ll;
-      const int g2raw = grab();
+      // (For the very first item this happens after its first stage.)
+      int tb1 = -1, g2raw = 0;
+      long long sl1 = -1ll;
+      auto prefetch_next = [&]() {
+        tb1 = v1 ? load_table(it1, 0) : -1;
+        sl1 = v1 ? load_slot(it1) : -1ll;
+        g2raw = grab();
+      };
+      if (counted) prefetch_next();
 
       const int kvh = g0 % a.Hkv;
       const int tok_begin = it0.tok_begin;
@@ -1008,6 +1019,12 @@ __global__ void __launch_bounds__((NC + 1) * 32, kFp8 && NC <= 4 ? PHOTON_FP8_CT
         if (st == 0) PROBE_SET(1, global_timer_ns());
         if (first && lane == 0) PROBE_SET(8 + 2 * items_done, global_timer_ns());
         ++st;
+        if (!counted) {
+          count_runs();
+          counted = true;
+          v1 = locate(g1 / a.Hkv, it1);
+          prefetch_next();
+        }
       }
       const int g2 = bcast(g2raw);
       WorkItem it2{};
@@ -1630,9 +1647,16 @@ cudaError_t launch_attention(const DecodeArgs& a, const CUtensorMap& tk, const C
   using PC = PersistCfg<T, D, G, NC, S, kRope, kMma, kMulti, kFp8>;
   const int per_sm = attention_ctas_per_sm<T, D, G, NC, S, kRope, kMma, kMulti, kFp8>();
   if (per_sm <= 0) return cudaErrorInvalidConfiguration;
+#ifdef PHOTON_PROBE_NO_PDL
+  // tuning builds only: the attention kernel as a plain launch
+  paged_decode_attention_kernel<T, D, G, NC, S, kRope, kMma, kMulti, kFp8>
+      <<<dim3(per_sm * a.num_sms), dim3(PC::kThreads), PC::kSmemBytes, stream>>>(a, tk, tv);
+  return cudaGetLastError();
+#else
   return launch_pdl(paged_decode_attention_kernel<T, D, G, NC, S, kRope, kMma, kMulti, kFp8>,
                     dim3(per_sm * a.num_sms), dim3(PC::kThreads), PC::kSmemBytes, stream, a, tk,
                     tv);
+#endif
 }
 
 template <typename T, int D, int G>
