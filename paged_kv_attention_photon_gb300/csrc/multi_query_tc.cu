@@ -9,8 +9,8 @@
 // attention for long sequences).
 //
 // A CTA owns 256 query rows of one (sequence, KV head) as two tiles of 128
-// and runs 11 warps in fixed roles: 8 softmax warps (4 per tile), a K copy
-// warp, a V copy warp and an MMA warp.  Row r of a tile is (token r / G, head
+// and runs 12 warps in fixed roles: 8 softmax warps (4 per tile), a K copy
+// warp, a V copy warp and one MMA warp per tile.  Row r of a tile is (token r / G, head
 // r % G of the KV head's group) and lives in TMEM lane r, so thread r of the
 // tile's softmax warps owns row r from the scores to the output: the softmax
 // needs no shuffles.  Per chunk of 64 keys:
@@ -178,8 +178,8 @@ struct TcCfg {
   static constexpr int kOffP = kOffV + kVStages * kVBytes;      // [kTiles][2]
   static constexpr int kUsed = kOffP + kTiles * 2 * kPBytes;
   static constexpr int kSmem = kUsed + 1024;   // + alignment of the base to a swizzle atom
-  // softmax warps, then the K copy warp, the V copy warp and the MMA warp
-  static constexpr int kThreads = kTiles * kTcThreads + 96;
+  // softmax warps, then the K copy warp, the V copy warp and one MMA warp per tile
+  static constexpr int kThreads = kTiles * kTcThreads + 64 + kTiles * 32;
 };
 
 // MN-major (V) operand: the same 128-byte-swizzled rows of 64 elements as the
@@ -327,18 +327,21 @@ static __device__ unsigned long long g_tc_cta[4096][2];
 // rings are separate because their stages are held for different spans: a
 // K chunk only until S of its chunk is computed, a V chunk until the P V
 // product, after the softmax; with one ring for both, the copy latency of
-// every chunk sat on the chain through the softmax.  Warp 10 computes: its
-// lanes zero the V rows that lie past the last key, its lane 0 issues every
-// MMA.  Both tiles use every K/V chunk, so each chunk is fetched once for 256
-// rows.  TMEM: tile t owns columns [256 t, 256 t + 256): two S buffers of 64,
-// then O.
+// every chunk sat on the chain through the softmax.  Warps 10 and 11 issue
+// the MMAs of tiles 0 and 1 (lane 0), so the two tiles' products go out in
+// parallel (one thread issuing every MMA took about twice the tensor cores'
+// execution time per chunk); warp 10's lanes also zero the V rows that lie
+// past the last key.  Both tiles use every K/V chunk, so each chunk is
+// fetched once for 256 rows.  TMEM: tile t owns columns [256 t, 256 t + 256):
+// two S buffers of 64, then O.
 // Barriers (each completes once per use; a use's parity is its index & 1):
 //   k_full[s], v_full[s]  K (V) of a chunk landed in stage s (copy transaction bytes)
-//   k_free[s]      the S products reading K stage s finished (MMA commit)
-//   v_free[s]      the P V products reading V stage s finished (MMA commit)
+//   k_free[s]      the S products reading K stage s finished (one commit per MMA warp)
+//   v_free[s]      the P V products reading V stage s finished (one commit per MMA warp)
+//   v_zeroed[s]    warp 10 zeroed the V rows of stage s past the last key
 //   s_full[t][b]   S of a chunk is in tile t's TMEM buffer b (MMA commit)
 //   s_free[t][b]   tile t's 4 softmax warps have read that buffer (4 arrivals)
-//   p_full[t][b]   tile t's P of a chunk is in its shared buffer b (128 arrivals)
+//   p_full[t][b]   tile t's P of a chunk is in its shared buffer b (4 warp arrivals)
 //   p_done[t][b]   the P V product reading that buffer finished (MMA commit)
 // The b-indexed barriers serve chunks b, b + 2, ...: chunk c's use of one has
 // parity (c / 2) & 1.
@@ -352,7 +355,7 @@ __global__ void __launch_bounds__(TcCfg<T, D>::kThreads)
   constexpr int kSuper = NT * kTcRows;
   extern __shared__ unsigned char tc_smem_raw[];
   __shared__ __align__(8) uint64_t k_full[SK], k_free[SK], v_full[SV], v_free[SV],
-      s_full[NT][2], s_free[NT][2], p_full[NT][2], p_done[NT][2];
+      s_full[NT][2], s_free[NT][2], p_full[NT][2], p_done[NT][2], v_zeroed[SV];
   __shared__ uint32_t tmem_slot;
   __shared__ int tail_rows[SV];   // per V stage: first V row to zero (64 = none)
   unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -407,17 +410,18 @@ __global__ void __launch_bounds__(TcCfg<T, D>::kThreads)
   if (tid == 0) {
     for (int i = 0; i < SK; ++i) {
       mbar_init(&k_full[i], 1);
-      mbar_init(&k_free[i], 1);
+      mbar_init(&k_free[i], NT);   // one commit per tile's MMA warp
     }
     for (int i = 0; i < SV; ++i) {
       mbar_init(&v_full[i], 1);
-      mbar_init(&v_free[i], 1);
+      mbar_init(&v_free[i], NT);
+      mbar_init(&v_zeroed[i], 1);
     }
     for (int t = 0; t < NT; ++t) {
       for (int i = 0; i < 2; ++i) {
         mbar_init(&s_full[t][i], 1);
         mbar_init(&s_free[t][i], 4);
-        mbar_init(&p_full[t][i], kTcThreads);
+        mbar_init(&p_full[t][i], 4);   // one arrival per softmax warp of the tile
         mbar_init(&p_done[t][i], 1);
       }
     }
@@ -498,17 +502,30 @@ __global__ void __launch_bounds__(TcCfg<T, D>::kThreads)
       }
     }
     if (!ok && lane == 0) raise_error(a.err, kErrTimeout);
-  } else if (warp == NT * 4 + 2) {
+  } else if (warp >= NT * 4 + 2) {
     // ================================================================ MMAs
+    // one warp per tile (lane 0 issues): the two tiles' products go out in
+    // parallel, and each warp waits only for its own tile's softmax
+    const int t = warp - (NT * 4 + 2);
+    const bool tile_used = t < ntiles;
     const uint32_t id_s = f16_idesc<T>(kTcRows, kTcKeys);
     const uint32_t id_o = f16_idesc<T>(kTcRows, D) | (1u << 16);   // B (V) MN-major
+    // Operand descriptors, built once: a descriptor's start-address field
+    // holds address >> 4 in its low 14 bits, and every operand here lies
+    // below 256 KB of the shared window, so the descriptor of base + off is
+    // the base's descriptor plus off >> 4 (no carry leaves the field).  Each
+    // MMA then costs one add per operand instead of a rebuilt descriptor.
+    const uint64_t qa = sw128_desc(sQ) + (uint64_t)((t * C::kQBytes) >> 4);
+    const uint64_t k_desc = sw128_desc(sK), v_desc = sw128_mn_desc(sV);
+    const uint64_t p_desc = sw128_desc(sP) + (uint64_t)((t * 2 * C::kPBytes) >> 4);
+    uint32_t zero_phase = 0;   // bit s: parity of V stage s's next zeroing (both warps alike)
     for (int c = 0; c <= nchunks && ok; ++c) {
       if (c < nchunks) {
         const int st = c % SK;
         ok = lane0_ok(mbar_wait_bounded(&k_full[st], (c / SK) & 1));
         if (!ok) break;
-        if (lane == 0) TC_PROBE(c, 7);
-        for (int t = 0; t < ntiles && ok; ++t) {
+        if (lane == 0 && t == 0) TC_PROBE(c, 7);
+        if (tile_used) {
           if (c >= 2) {
             ok = lane0_ok(mbar_wait_bounded(&s_free[t][c & 1], ((c - 2) >> 1) & 1));
             if (!ok) break;
@@ -516,58 +533,65 @@ __global__ void __launch_bounds__(TcCfg<T, D>::kThreads)
           if (lane == 0) {
             if (t == 0) TC_PROBE(c, 4);
             tc_fence_after();
+            const uint64_t kb = k_desc + (uint64_t)((st * C::kKBytes) >> 4);
+            const uint32_t dst = tmem + t * kTmemCols + kTmemS + (c & 1) * kTcKeys;
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk) {
               const uint32_t koff = (kk & 3) * 32;
-              tc_mma(tmem + t * kTmemCols + kTmemS + (c & 1) * kTcKeys,
-                     sw128_desc(sQ + t * C::kQBytes + (kk >> 2) * (kTcRows * 128) + koff),
-                     sw128_desc(sK + st * C::kKBytes + (kk >> 2) * (kTcKeys * 128) + koff), id_s,
-                     kk > 0);
+              tc_mma(dst, qa + (uint64_t)(((kk >> 2) * (kTcRows * 128) + koff) >> 4),
+                     kb + (uint64_t)(((kk >> 2) * (kTcKeys * 128) + koff) >> 4), id_s, kk > 0);
             }
             tc_commit(&s_full[t][c & 1]);
             TC_PROBE(c, 8 + t);
           }
         }
-        if (!ok) break;
-        if (lane == 0) tc_commit(&k_free[st]);   // the K stage is free once these S are done
+        if (lane == 0) tc_commit(&k_free[st]);   // this tile's S of the K stage are done
       }
       if (c >= 1) {
-        // P V of the previous chunk, tile by tile, once its V landed and its
-        // weights are written
+        // P V of the previous chunk, once its V landed and its weights are written
         const int pc = c - 1, pst = pc % SV, pb = pc & 1;
-        if (lane == 0) TC_PROBE(pc, 10);
+        if (lane == 0 && t == 0) TC_PROBE(pc, 10);
         ok = lane0_ok(mbar_wait_bounded(&v_full[pst], (pc / SV) & 1));
         if (!ok) break;
-        if (lane == 0) TC_PROBE(pc, 11);
+        if (lane == 0 && t == 0) TC_PROBE(pc, 11);
         // zero the V rows past the last key (a partial or missing block):
-        // they are multiplied by zero weights, and 0 x NaN would not vanish
+        // they are multiplied by zero weights, and 0 x NaN would not vanish.
+        // The first MMA warp writes the zeros and signals v_zeroed; the other
+        // waits for it before its products read the stage.
         const int tail = tail_rows[pst];
         if (tail < kTcKeys) {
-          unsigned char* vt = smem + C::kOffV + pst * C::kVBytes;
-          for (int p = lane; p < (kTcKeys - tail) * (D / 8); p += 32) {
-            const int r = tail + p / (D / 8), ch = p % (D / 8);
-            *reinterpret_cast<uint4*>(vt + sw_chunk<kTcKeys>(r, ch)) = make_uint4(0, 0, 0, 0);
+          if (t == 0) {
+            unsigned char* vt = smem + C::kOffV + pst * C::kVBytes;
+            for (int p = lane; p < (kTcKeys - tail) * (D / 8); p += 32) {
+              const int r = tail + p / (D / 8), ch = p % (D / 8);
+              *reinterpret_cast<uint4*>(vt + sw_chunk<kTcKeys>(r, ch)) = make_uint4(0, 0, 0, 0);
+            }
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&v_zeroed[pst]);
+          } else {
+            ok = lane0_ok(mbar_wait_bounded(&v_zeroed[pst], (zero_phase >> pst) & 1u));
+            if (!ok) break;
           }
-          fence_async_smem();
+          zero_phase ^= 1u << pst;
         }
         __syncwarp();
-        for (int t = 0; t < ntiles && ok; ++t) {
+        if (tile_used) {
           ok = lane0_ok(mbar_wait_bounded(&p_full[t][pb], (pc >> 1) & 1));
           if (!ok) break;
           if (lane == 0) {
             if (t == 0) TC_PROBE(pc, 5);
             tc_fence_after();
+            const uint64_t pa = p_desc + (uint64_t)((pb * C::kPBytes) >> 4);
+            const uint64_t vb = v_desc + (uint64_t)((pst * C::kVBytes) >> 4);
 #pragma unroll
             for (int kk = 0; kk < kTcKeys / 16; ++kk)
-              tc_mma(tmem + t * kTmemCols + kTmemO,
-                     sw128_desc(sP + (t * 2 + pb) * C::kPBytes + kk * 32),
-                     sw128_mn_desc(sV + pst * C::kVBytes + kk * 2048), id_o,
-                     (pc > 0 || kk > 0) ? 1u : 0u);
+              tc_mma(tmem + t * kTmemCols + kTmemO, pa + (uint64_t)((kk * 32) >> 4),
+                     vb + (uint64_t)((kk * 2048) >> 4), id_o, (pc > 0 || kk > 0) ? 1u : 0u);
             tc_commit(&p_done[t][pb]);
             TC_PROBE(pc, 12 + t);
           }
         }
-        if (!ok) break;
         if (lane == 0) tc_commit(&v_free[pst]);
       }
     }
@@ -670,8 +694,11 @@ __global__ void __launch_bounds__(TcCfg<T, D>::kThreads)
       }
       l_run += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
       if (lane == 0 && (warp == 0 || warp == 4)) TC_PROBE(c, warp == 0 ? 2 : 14);
+      // every thread orders its own P writes for the tensor cores, then one
+      // arrival per warp
       fence_async_smem();
-      mbar_arrive_cnt(&p_full[t][c & 1]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cnt(&p_full[t][c & 1]);
     }
     // ---- the last product, then O / l
     if (tile_used) {
