@@ -128,6 +128,9 @@ constexpr int kMaxRuns = 12;
 // the stages carry the code blocks as tensor-map copies in the swizzled
 // layout of code_chunk, and the tensor-core math widens the codes to fp16 in
 // registers as it loads its fragments.
+#ifndef PHOTON_FP8_BPW
+#define PHOTON_FP8_BPW 2
+#endif
 template <typename T, int D, int G, int NC, int S, bool R = false, bool M = false, bool X = false,
           bool F = false>
 struct PersistCfg {
@@ -141,7 +144,12 @@ struct PersistCfg {
   // with RoPE the item's (cos, sin) row, D/2 float pairs, follows its q rows
   static constexpr int kCsBytes = R ? 4 * D : 0;
   static constexpr int kQStride = (kQBytes + kCsBytes + 127) / 128 * 128;
-  static constexpr int kStageBytes = 2 * NC * kBlockBytes;     // K blocks, then V blocks
+  // blocks per warp and stage: over an e4m3 cache each consumer warp takes two
+  // consecutive blocks of a stage (the stage protocol and the producer's work
+  // per stage are then spread over twice the bytes)
+  static constexpr int kBPW = F ? PHOTON_FP8_BPW : 1;
+  static constexpr int kStageBlocks = NC * kBPW;
+  static constexpr int kStageBytes = 2 * kStageBlocks * kBlockBytes;  // K blocks, then V blocks
   static constexpr int kOffFull = 0;
   static constexpr int kOffEmpty = kOffFull + 8 * S;
   static constexpr int kOffSync = kOffEmpty + 8 * S;
@@ -164,7 +172,8 @@ struct PersistCfg {
   static constexpr int kPoRowsPerBlock = kBlockBytes / (D * 4);  // o rows in one block area
   static_assert(kSlots <= 2 * kPoRowsPerBlock, "a warp's o rows must fit its K and V block areas");
   // the producer's 32-entry block-table slices must split into whole stages
-  static_assert(NC >= 1 && NC <= 32 && 32 % NC == 0, "consumer warps must divide 32");
+  static_assert(NC >= 1 && NC <= 32 && 32 % kStageBlocks == 0 && kStageBlocks <= 8,
+                "blocks per stage must divide 32 and fit the stage header's mask");
   static_assert(!X || (M && !R), "the few-token mode runs on the tensor-core consumer, no RoPE");
   static_assert(!M || (kBlockBytes % 1024 == 0 && sizeof(T) == 2), "swizzled blocks");
   static_assert(!F || (M && !R && !X && std::is_same<T, __half>::value),
@@ -538,14 +547,14 @@ static __device__ unsigned long long g_probe[kProbeCtas][kProbeSlots];
 static __device__ unsigned long long g_probe_merge[4096][4];
 // a one-thread kernel's time stamp, launched by the tuning harness just
 // before a call (the gap to the attention kernel's entry is its launch)
-static __device__ unsigned long long g_probe_stamp;
-static __global__ void probe_stamp_kernel() { g_probe_stamp = global_timer_ns(); }
+static __device__ unsigned long long g_probe_stamp[2];
+static __global__ void probe_stamp_kernel(int slot) { g_probe_stamp[slot] = global_timer_ns(); }
 // the same with a large shared-memory request (the carveout of the attention
 // kernel), to tell a launch's own cost from a carveout change
 static __global__ void probe_stamp_big_kernel() {
   extern __shared__ unsigned char stamp_smem[];
   stamp_smem[threadIdx.x] = 0;
-  g_probe_stamp = global_timer_ns();
+  g_probe_stamp[0] = global_timer_ns();
 }
 #define PROBE_SET(i, v) \
   do { if (blockIdx.x < kProbeCtas && (i) < kProbeSlots) g_probe[blockIdx.x][i] = (v); } while (0)
@@ -570,7 +579,7 @@ static __global__ void probe_stamp_big_kernel() {
 // the item's combine.  Three CTAs share an SM (PHOTON_FP8_CTAS, a tuning
 // knob for the register cap).
 #ifndef PHOTON_FP8_CTAS
-#define PHOTON_FP8_CTAS 3
+#define PHOTON_FP8_CTAS (PHOTON_FP8_BPW > 1 ? 2 : 3)
 #endif
 template <typename T, int D, int G, int NC, int S, bool kRope, bool kMma, bool kMulti,
           bool kFp8 = false>
@@ -892,7 +901,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, kFp8 && NC <= 4 ? PHOTON_FP8_CT
       const int nblk = (it0.tok_end - tok_begin + kBlockSize - 1) / kBlockSize;
       const size_t head_off = (size_t)kvh * PC::kBlockElems;
       int tb = tb0, chunk = 0;
-      for (int k0 = 0; k0 < nblk; k0 += NC) {
+      for (int k0 = 0; k0 < nblk; k0 += PC::kStageBlocks) {
         if (k0 >= 32 * (chunk + 1)) tb = load_table(it0, ++chunk);
         const int slot = st % S;
         const uint32_t ph = (st / S) & 1u;
@@ -903,7 +912,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, kFp8 && NC <= 4 ? PHOTON_FP8_CT
           aborted = true;
           break;
         }
-        const int nb = min(NC, nblk - k0);
+        const int nb = min(PC::kStageBlocks, nblk - k0);
         const int phys = __shfl_sync(0xffffffffu, tb, (k0 + lane) & 31);
         const int tok = (blk0 + k0 + lane) * kBlockSize;
         const int rows = min(kBlockSize, it0.tok_end - tok);
@@ -940,7 +949,8 @@ __global__ void __launch_bounds__((NC + 1) * 32, kFp8 && NC <= 4 ? PHOTON_FP8_CT
           h.tok_end = it0.tok_end;
           h.blk0 = blk0 + k0;
           h.nblk = nb;
-          h.flags = (first ? kFirst : 0) | (k0 + NC >= nblk ? kLast : 0) | (int)(mask << 8);
+          h.flags = (first ? kFirst : 0) | (k0 + PC::kStageBlocks >= nblk ? kLast : 0) |
+                    (int)(mask << 8);
           h.new_warp = new_lane;
           h.new_phys = new_lane >= 0 ? new_phys : -1;
           h.new_row = new_lane >= 0 ? new_rows - 1 : -1;
@@ -960,12 +970,12 @@ __global__ void __launch_bounds__((NC + 1) * 32, kFp8 && NC <= 4 ? PHOTON_FP8_CT
           const int y = (phys * a.Hkv + kvh) * kBlockSize;
           tma_load_box_hint(smem_addr(stage + lane * PC::kBlockBytes), &tmk, 0, y, &full[slot],
                             kv_policy);
-          tma_load_box_hint(smem_addr(stage + (NC + lane) * PC::kBlockBytes), &tmv, 0, y,
+          tma_load_box_hint(smem_addr(stage + (PC::kStageBlocks + lane) * PC::kBlockBytes), &tmv, 0, y,
                             &full[slot], kv_policy);
         } else if (kMma && valid) {
           const int y = (phys * a.Hkv + kvh) * kBlockSize;
           const uint32_t kd = smem_addr(stage + lane * PC::kBlockBytes);
-          const uint32_t vd = smem_addr(stage + (NC + lane) * PC::kBlockBytes);
+          const uint32_t vd = smem_addr(stage + (PC::kStageBlocks + lane) * PC::kBlockBytes);
 #pragma unroll
           for (int hx = 0; hx < D / 64; ++hx) {
             tma_load_box_hint(kd + hx * 2048, &tmk, hx * 64, y, &full[slot], kv_policy);
@@ -985,7 +995,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, kFp8 && NC <= 4 ? PHOTON_FP8_CT
           if (nbytes) {
             bulk_copy_g2s_hint(stage + lane * PC::kBlockBytes, kpool + src, nbytes, &full[slot],
                                kv_policy);
-            bulk_copy_g2s_hint(stage + (NC + lane) * PC::kBlockBytes, vpool + src, nbytes,
+            bulk_copy_g2s_hint(stage + (PC::kStageBlocks + lane) * PC::kBlockBytes, vpool + src, nbytes,
                                &full[slot], kv_policy);
           }
           if (new_here) {
@@ -993,7 +1003,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, kFp8 && NC <= 4 ? PHOTON_FP8_CT
             const uint32_t rb = (uint32_t)(D * (int)sizeof(T));
             bulk_copy_g2s(stage + lane * PC::kBlockBytes + nbytes,
                           static_cast<const T*>(a.k_new) + nsrc, rb, &full[slot]);
-            bulk_copy_g2s(stage + (NC + lane) * PC::kBlockBytes + nbytes,
+            bulk_copy_g2s(stage + (PC::kStageBlocks + lane) * PC::kBlockBytes + nbytes,
                           static_cast<const T*>(a.v_new) + nsrc, rb, &full[slot]);
           }
         }
@@ -1201,25 +1211,31 @@ __global__ void __launch_bounds__((NC + 1) * 32, kFp8 && NC <= 4 ? PHOTON_FP8_CT
           for (int e = 0; e < C::kEPL; ++e) qf[g][e] *= a.qscale;
       }
     }
-    if (kFp8 && warp < h.nblk && ((h.flags >> (8 + warp)) & 1)) {
-      // fp8 cache: the K and V code blocks are used as they landed; the V
-      // rows past the context (the box brought whatever the pool holds
-      // there) are zeroed first, since 0 x NaN would reach the sums
-      unsigned char* const kb = smem + PC::kOffKV + slot * PC::kStageBytes + warp * PC::kBlockBytes;
-      unsigned char* const vb = kb + NC * PC::kBlockBytes;
-      const int n_valid = min(kBlockSize, h.tok_end - (h.blk0 + warp) * kBlockSize);
-      if (n_valid < kBlockSize) {
-        for (int i = lane; i < (kBlockSize - n_valid) * (D / 16); i += 32)
-          *reinterpret_cast<uint4*>(vb + n_valid * D + i * 16) = make_uint4(0u, 0u, 0u, 0u);
-        fence_proxy_async_smem();  // the stage is refilled by tensor copies later
-        __syncwarp();
+    if (kFp8) {
+      // fp8 cache: the warp's K and V code blocks are used as they landed;
+      // the V rows past the context (the box brought whatever the pool
+      // holds there) are zeroed first, since 0 x NaN would reach the sums
+#pragma unroll
+      for (int bb = 0; bb < PC::kBPW; ++bb) {
+        const int blk = warp * PC::kBPW + bb;
+        if (blk >= h.nblk || !((h.flags >> (8 + blk)) & 1)) continue;
+        unsigned char* const kb =
+            smem + PC::kOffKV + slot * PC::kStageBytes + blk * PC::kBlockBytes;
+        unsigned char* const vb = kb + PC::kStageBlocks * PC::kBlockBytes;
+        const int n_valid = min(kBlockSize, h.tok_end - (h.blk0 + blk) * kBlockSize);
+        if (n_valid < kBlockSize) {
+          for (int i = lane; i < (kBlockSize - n_valid) * (D / 16); i += 32)
+            *reinterpret_cast<uint4*>(vb + n_valid * D + i * 16) = make_uint4(0u, 0u, 0u, 0u);
+          fence_proxy_async_smem();  // the stage is refilled by tensor copies later
+          __syncwarp();
+        }
+        if constexpr (kFp8)
+          attend_block_mma<T, D, false, false, true>(smem_addr(kb), smem_addr(vb), n_valid,
+                                                     a.qscale, tq, tq, tm, tl, to, lane, 0, tlim);
       }
-      if constexpr (kFp8)
-        attend_block_mma<T, D, false, false, true>(smem_addr(kb), smem_addr(vb), n_valid,
-                                                   a.qscale, tq, tq, tm, tl, to, lane, 0, tlim);
     } else if (kMma && warp < h.nblk && ((h.flags >> (8 + warp)) & 1)) {
       unsigned char* const kb = smem + PC::kOffKV + slot * PC::kStageBytes + warp * PC::kBlockBytes;
-      unsigned char* const vb = kb + NC * PC::kBlockBytes;
+      unsigned char* const vb = kb + PC::kStageBlocks * PC::kBlockBytes;
       const int n_valid = min(kBlockSize, h.tok_end - (h.blk0 + warp) * kBlockSize);
       constexpr int kRowChunks = D * (int)sizeof(T) / 16;
       bool wrote = false;
@@ -1275,7 +1291,8 @@ __global__ void __launch_bounds__((NC + 1) * 32, kFp8 && NC <= 4 ? PHOTON_FP8_CT
         fence_proxy_async_smem();  // the stage is refilled by bulk copies later
         __syncwarp();
       }
-      attend_block<T, D, G>(stage + warp * PC::kBlockElems, stage + (NC + warp) * PC::kBlockElems,
+      attend_block<T, D, G>(stage + warp * PC::kBlockElems,
+                            stage + (PC::kStageBlocks + warp) * PC::kBlockElems,
                             n_valid, qf, m, l, o, lane);
       if (warp == h.new_warp) {
         // fused step: this block's row new_row is the new token; store it
@@ -1283,7 +1300,7 @@ __global__ void __launch_bounds__((NC + 1) * 32, kFp8 && NC <= 4 ? PHOTON_FP8_CT
         constexpr int kPerChunk = 16 / (int)sizeof(T);
         const size_t dst = (((size_t)h.new_phys * a.Hkv + h.kvh) * kBlockSize + h.new_row) * D;
         const T* krow = stage + warp * PC::kBlockElems + h.new_row * D;
-        const T* vrow = stage + (NC + warp) * PC::kBlockElems + h.new_row * D;
+        const T* vrow = stage + (PC::kStageBlocks + warp) * PC::kBlockElems + h.new_row * D;
         for (int i = lane; i < 2 * kRowChunks; i += 32) {
           const bool is_v = i >= kRowChunks;
           const int ch = is_v ? i - kRowChunks : i;
@@ -1314,7 +1331,8 @@ __global__ void __launch_bounds__((NC + 1) * 32, kFp8 && NC <= 4 ? PHOTON_FP8_CT
     // kPoRowsPerBlock rows, its V block area the rest
     auto po_row = [&](int w, int g) -> float* {
       constexpr int kPer = PC::kPoRowsPerBlock;
-      const int area = g < kPer ? w : NC + w;
+      // warp w's own (first) block of the stage: it has finished reading it
+      const int area = (g < kPer ? 0 : PC::kStageBlocks) + w * PC::kBPW;
       return reinterpret_cast<float*>(last_stage + area * PC::kBlockBytes) + (g % kPer) * D;
     };
     parity ^= 1;
@@ -1620,13 +1638,24 @@ int attention_ctas_per_sm() {
 #ifndef PHOTON_RING_KB
 #define PHOTON_RING_KB 96
 #endif
-constexpr int kRingBytes = PHOTON_RING_KB * 1024;
+#ifndef PHOTON_RING_KB_D64
+#define PHOTON_RING_KB_D64 64
+#endif
+// Ring budget of an instantiation.  16-bit blocks of head_dim 64 take a 64 KB
+// ring (four 16 KB stages) so that three CTAs share an SM: their consumers
+// do half the tensor-core work per byte of the head_dim-128 ones, and the
+// third CTA's warps keep more of them busy (batch-256 mix: 208 -> 168 us
+// against a 96 KB ring at two CTAs per SM).
+template <typename T, int D>
+constexpr int ring_bytes() {
+  return (D == 64 && sizeof(T) == 2 ? PHOTON_RING_KB_D64 : PHOTON_RING_KB) * 1024;
+}
 
 template <typename T, int D>
 constexpr int stages_for(int nc) {
-  return (kRingBytes / (2 * nc * kBlockSize * D * (int)sizeof(T))) < 2
+  return (ring_bytes<T, D>() / (2 * nc * kBlockSize * D * (int)sizeof(T))) < 2
              ? 2
-             : (kRingBytes / (2 * nc * kBlockSize * D * (int)sizeof(T)));
+             : (ring_bytes<T, D>() / (2 * nc * kBlockSize * D * (int)sizeof(T)));
 }
 
 // Which consumer a (D, G) instantiation runs by default: the tensor-core one
@@ -1714,14 +1743,14 @@ cudaError_t launch_decode_impl(const DecodeArgs& a0, cudaStream_t stream) {
 // The e4m3 cache: stages of 4 code blocks per K and V (8 KB at d = 64, 16 KB at
 // d = 128) in a 64 KB ring, so that three CTAs share an SM.
 #ifndef PHOTON_RING_KB_FP8
-#define PHOTON_RING_KB_FP8 64
+#define PHOTON_RING_KB_FP8 (PHOTON_FP8_BPW > 1 ? 96 : 64)
 #endif
 constexpr int kRingBytesFp8 = PHOTON_RING_KB_FP8 * 1024;
 
 template <int D, int G>
 cudaError_t launch_decode_fp8_impl(const DecodeArgs& a, cudaStream_t stream) {
   constexpr int NC = PHOTON_CONSUMER_WARPS;
-  constexpr int kStage = 2 * NC * kBlockSize * D;
+  constexpr int kStage = 2 * NC * PHOTON_FP8_BPW * kBlockSize * D;
   constexpr int S = kRingBytesFp8 / kStage < 2 ? 2 : kRingBytesFp8 / kStage;
   if (!a.q || !a.k_cache || !a.v_cache || !a.block_tables || !a.context_lens || !a.out ||
       !a.ws_m || !a.ws_l || !a.ws_o || !a.ws_ctrl || !a.err || a.k_new || a.rope_cs ||

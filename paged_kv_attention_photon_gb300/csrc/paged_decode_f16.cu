@@ -23,16 +23,16 @@ extern "C" int photon_probe_merge_read(void* dst, size_t bytes) {
   return (int)cudaMemcpyFromSymbol(dst, photon::g_probe_merge, bytes);
 }
 extern "C" int photon_probe_stamp(void* stream, int big) {
-  if (big) {
+  if (big > 0) {
     cudaFuncSetAttribute(photon::probe_stamp_big_kernel,
                          cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
     photon::probe_stamp_big_kernel<<<152, 32, 200 * 1024, static_cast<cudaStream_t>(stream)>>>();
   } else {
-    photon::probe_stamp_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>();
+    photon::probe_stamp_kernel<<<1, 1, 0, static_cast<cudaStream_t>(stream)>>>(big < 0 ? 1 : 0);
   }
   return (int)cudaGetLastError();
 }
 extern "C" int photon_probe_stamp_read(void* dst) {
-  return (int)cudaMemcpyFromSymbol(dst, photon::g_probe_stamp, 8);
+  return (int)cudaMemcpyFromSymbol(dst, photon::g_probe_stamp, 16);
 }
 #endif
