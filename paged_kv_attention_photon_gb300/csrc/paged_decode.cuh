@@ -129,7 +129,7 @@ constexpr int kMaxRuns = 12;
 // layout of code_chunk, and the tensor-core math widens the codes to fp16 in
 // registers as it loads its fragments.
 #ifndef PHOTON_FP8_BPW
-#define PHOTON_FP8_BPW 2
+#define PHOTON_FP8_BPW 1
 #endif
 template <typename T, int D, int G, int NC, int S, bool R = false, bool M = false, bool X = false,
           bool F = false>
@@ -144,9 +144,11 @@ struct PersistCfg {
   // with RoPE the item's (cos, sin) row, D/2 float pairs, follows its q rows
   static constexpr int kCsBytes = R ? 4 * D : 0;
   static constexpr int kQStride = (kQBytes + kCsBytes + 127) / 128 * 128;
-  // blocks per warp and stage: over an e4m3 cache each consumer warp takes two
-  // consecutive blocks of a stage (the stage protocol and the producer's work
-  // per stage are then spread over twice the bytes)
+  // blocks per warp and stage (PHOTON_FP8_BPW, e4m3 cache only; 1 by
+  // default): with two, each consumer warp takes two consecutive blocks of a
+  // stage, spreading the stage protocol over twice the bytes, but the larger
+  // stages leave room for two CTAs per SM instead of three, and the qwen_b64
+  // fp8 decode measured 70.5 against 67.2 us
   static constexpr int kBPW = F ? PHOTON_FP8_BPW : 1;
   static constexpr int kStageBlocks = NC * kBPW;
   static constexpr int kStageBytes = 2 * kStageBlocks * kBlockBytes;  // K blocks, then V blocks
@@ -1469,9 +1471,13 @@ __global__ void __launch_bounds__((NC + 1) * 32, kFp8 && NC <= 4 ? PHOTON_FP8_CT
 #define PHOTON_MERGE_WARPS 2
 #endif
 constexpr int kMergeWarps = PHOTON_MERGE_WARPS;
-// Partial rows loaded at once per lane: one round trip for up to 32
-// partitions.
-constexpr int kMergeRows = 32;
+// Partial rows loaded at once per lane: one round trip for up to
+// PHOTON_MERGE_ROWS partitions (a tuning knob: fewer rows take fewer
+// registers, so more merge warps are resident beside the attention CTAs).
+#ifndef PHOTON_MERGE_ROWS
+#define PHOTON_MERGE_ROWS 32
+#endif
+constexpr int kMergeRows = PHOTON_MERGE_ROWS;
 
 template <typename T, int D>
 __global__ void __launch_bounds__(kMergeWarps * 32) paged_decode_merge_kernel(const DecodeArgs a) {
