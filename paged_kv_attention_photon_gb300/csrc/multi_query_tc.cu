@@ -9,8 +9,8 @@
 // attention for long sequences).
 //
 // A CTA owns 256 query rows of one (sequence, KV head) as two tiles of 128
-// and runs 12 warps in fixed roles: 8 softmax warps (4 per tile), a K copy
-// warp, a V copy warp and one MMA warp per tile.  Row r of a tile is (token r / G, head
+// and runs 14 warps in fixed roles: 8 softmax warps (4 per tile), a K copy
+// warp, a V copy warp, and per tile an S-issuing and a P V-issuing MMA warp.  Row r of a tile is (token r / G, head
 // r % G of the KV head's group) and lives in TMEM lane r, so thread r of the
 // tile's softmax warps owns row r from the scores to the output: the softmax
 // needs no shuffles.  Per chunk of 64 keys:
@@ -74,12 +74,28 @@ __device__ __forceinline__ uint32_t f16_idesc(int M, int N) {
          ((uint32_t)(M >> 4) << 24);
 }
 
-__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc,
-                                       uint32_t accumulate) {
+// One tcgen05.mma (D += A B, kind::f16, A and B from shared-memory
+// descriptors, accumulate unless `accumulate` is 0), executed by the whole
+// (converged) warp with the product issued only where `issue` is nonzero:
+// the operand descriptors stay warp-uniform, and no branch separates the
+// issuing lane from the rest of the warp.
+__device__ __forceinline__ void tc_mma_warp(uint32_t d_tmem, uint64_t a, uint64_t b,
+                                            uint32_t idesc, uint32_t accumulate, uint32_t issue) {
   asm volatile(
-      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
-      "l"(a), "l"(b), "r"(idesc), "r"(accumulate));
+      "{\n.reg .pred p, q;\nsetp.ne.b32 p, %4, 0;\nsetp.ne.b32 q, %5, 0;\n"
+      "@q tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(d_tmem),
+      "l"(a), "l"(b), "r"(idesc), "r"(accumulate), "r"(issue));
+}
+// The same with A in tensor memory (a_tmem: lane 0 of the operand's 128
+// rows, first column; 16-bit elements packed two per column, the lower k in
+// the low half).
+__device__ __forceinline__ void tc_mma_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t b,
+                                               uint32_t idesc, uint32_t accumulate,
+                                               uint32_t issue) {
+  asm volatile(
+      "{\n.reg .pred p, q;\nsetp.ne.b32 p, %4, 0;\nsetp.ne.b32 q, %5, 0;\n"
+      "@q tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate), "r"(issue));
 }
 __device__ __forceinline__ void tc_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
@@ -163,23 +179,31 @@ __device__ __forceinline__ uint32_t sw_chunk(int r, int c) {
 // a ring of kStages K/V chunks (filled by the tensor memory accelerator), two
 // P buffers per Q tile (chunk c uses buffer c % 2, so the softmax of chunk c
 // writes its weights while the product of chunk c - 1 still reads the other).
+// Ring depths (tuning knobs).  Measured on the 16 x 1024 prefill: 3 + 3
+// stages 0.392 ms, 4 K + 2 V 0.394 ms, 5 K + 1 V 0.595 ms.
+#ifndef PHOTON_TC_KSTAGES
+#define PHOTON_TC_KSTAGES 3
+#endif
+#ifndef PHOTON_TC_VSTAGES
+#define PHOTON_TC_VSTAGES 3
+#endif
 template <typename T, int D>
 struct TcCfg {
   static constexpr int kTiles = 2;
-  static constexpr int kKStages = 3;   // K ring: a stage is free once S of its chunk is done
-  static constexpr int kVStages = 3;   // V ring: free once the P V product of its chunk is done
+  static constexpr int kKStages = PHOTON_TC_KSTAGES;   // K ring: a stage is free once S of its chunk is done
+  static constexpr int kVStages = PHOTON_TC_VSTAGES;   // V ring: free once the P V product of its chunk is done
   static constexpr int kQBytes = kTcRows * D * 2;     // one Q tile
   static constexpr int kKBytes = kTcKeys * D * 2;     // one K chunk
   static constexpr int kVBytes = kTcKeys * D * 2;     // one V chunk
-  static constexpr int kPBytes = kTcRows * kTcKeys * 2;
+
   static constexpr int kOffQ = 0;                               // [kTiles]
   static constexpr int kOffK = kOffQ + kTiles * kQBytes;        // [kKStages]
   static constexpr int kOffV = kOffK + kKStages * kKBytes;      // [kVStages]
-  static constexpr int kOffP = kOffV + kVStages * kVBytes;      // [kTiles][2]
-  static constexpr int kUsed = kOffP + kTiles * 2 * kPBytes;
+  static constexpr int kUsed = kOffV + kVStages * kVBytes;
   static constexpr int kSmem = kUsed + 1024;   // + alignment of the base to a swizzle atom
-  // softmax warps, then the K copy warp, the V copy warp and one MMA warp per tile
-  static constexpr int kThreads = kTiles * kTcThreads + 64 + kTiles * 32;
+  // softmax warps, then the K copy warp, the V copy warp, and per tile an
+  // S-issuing and a P V-issuing warp
+  static constexpr int kThreads = kTiles * kTcThreads + 64 + kTiles * 64;
 };
 
 // MN-major (V) operand: the same 128-byte-swizzled rows of 64 elements as the
@@ -328,17 +352,17 @@ static __device__ unsigned long long g_tc_cta[4096][2];
 // K chunk only until S of its chunk is computed, a V chunk until the P V
 // product, after the softmax; with one ring for both, the copy latency of
 // every chunk sat on the chain through the softmax.  Warps 10 and 11 issue
-// the MMAs of tiles 0 and 1 (lane 0), so the two tiles' products go out in
-// parallel (one thread issuing every MMA took about twice the tensor cores'
-// execution time per chunk); warp 10's lanes also zero the V rows that lie
-// past the last key.  Both tiles use every K/V chunk, so each chunk is
+// the S products of tiles 0 and 1, warps 12 and 13 their P V products (lane
+// 0 of each), so four instruction streams feed the tensor cores (one thread
+// issuing every MMA took about twice the tensor cores' execution time per
+// chunk); warp 12's lanes also zero the V rows that lie past the last key.  Both tiles use every K/V chunk, so each chunk is
 // fetched once for 256 rows.  TMEM: tile t owns columns [256 t, 256 t + 256):
 // two S buffers of 64, then O.
 // Barriers (each completes once per use; a use's parity is its index & 1):
 //   k_full[s], v_full[s]  K (V) of a chunk landed in stage s (copy transaction bytes)
 //   k_free[s]      the S products reading K stage s finished (one commit per MMA warp)
 //   v_free[s]      the P V products reading V stage s finished (one commit per MMA warp)
-//   v_zeroed[s]    warp 10 zeroed the V rows of stage s past the last key
+//   v_zeroed[s]    warp 12 zeroed the V rows of stage s past the last key
 //   s_full[t][b]   S of a chunk is in tile t's TMEM buffer b (MMA commit)
 //   s_free[t][b]   tile t's 4 softmax warps have read that buffer (4 arrivals)
 //   p_full[t][b]   tile t's P of a chunk is in its shared buffer b (4 warp arrivals)
@@ -355,14 +379,13 @@ __global__ void __launch_bounds__(TcCfg<T, D>::kThreads)
   constexpr int kSuper = NT * kTcRows;
   extern __shared__ unsigned char tc_smem_raw[];
   __shared__ __align__(8) uint64_t k_full[SK], k_free[SK], v_full[SV], v_free[SV],
-      s_full[NT][2], s_free[NT][2], p_full[NT][2], p_done[NT][2], v_zeroed[SV];
+      s_full[NT][2], p_full[NT][2], p_done[NT][2], v_zeroed[SV];
   __shared__ uint32_t tmem_slot;
   __shared__ int tail_rows[SV];   // per V stage: first V row to zero (64 = none)
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_addr(smem);
-  const uint32_t sQ = sbase + C::kOffQ, sK = sbase + C::kOffK, sV = sbase + C::kOffV,
-                 sP = sbase + C::kOffP;
+  const uint32_t sQ = sbase + C::kOffQ, sK = sbase + C::kOffK, sV = sbase + C::kOffV;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = a.Hq / a.Hkv;
@@ -420,7 +443,6 @@ __global__ void __launch_bounds__(TcCfg<T, D>::kThreads)
     for (int t = 0; t < NT; ++t) {
       for (int i = 0; i < 2; ++i) {
         mbar_init(&s_full[t][i], 1);
-        mbar_init(&s_free[t][i], 4);
         mbar_init(&p_full[t][i], 4);   // one arrival per softmax warp of the tile
         mbar_init(&p_done[t][i], 1);
       }
@@ -504,9 +526,11 @@ __global__ void __launch_bounds__(TcCfg<T, D>::kThreads)
     if (!ok && lane == 0) raise_error(a.err, kErrTimeout);
   } else if (warp >= NT * 4 + 2) {
     // ================================================================ MMAs
-    // one warp per tile (lane 0 issues): the two tiles' products go out in
-    // parallel, and each warp waits only for its own tile's softmax
-    const int t = warp - (NT * 4 + 2);
+    // per tile one warp issues the S products and one the P V products (lane
+    // 0 issues): the four streams go out in parallel, and each waits only for
+    // what its own products need
+    const int t = (warp - (NT * 4 + 2)) & (NT - 1);
+    const bool issues_s = warp - (NT * 4 + 2) < NT;
     const bool tile_used = t < ntiles;
     const uint32_t id_s = f16_idesc<T>(kTcRows, kTcKeys);
     const uint32_t id_o = f16_idesc<T>(kTcRows, D) | (1u << 16);   // B (V) MN-major
@@ -517,37 +541,38 @@ __global__ void __launch_bounds__(TcCfg<T, D>::kThreads)
     // MMA then costs one add per operand instead of a rebuilt descriptor.
     const uint64_t qa = sw128_desc(sQ) + (uint64_t)((t * C::kQBytes) >> 4);
     const uint64_t k_desc = sw128_desc(sK), v_desc = sw128_mn_desc(sV);
-    const uint64_t p_desc = sw128_desc(sP) + (uint64_t)((t * 2 * C::kPBytes) >> 4);
-    uint32_t zero_phase = 0;   // bit s: parity of V stage s's next zeroing (both warps alike)
+    uint32_t zero_phase = 0;   // bit s: parity of V stage s's next zeroing (both P V warps alike)
     for (int c = 0; c <= nchunks && ok; ++c) {
-      if (c < nchunks) {
+      if (issues_s && c < nchunks) {
         const int st = c % SK;
         ok = lane0_ok(mbar_wait_bounded(&k_full[st], (c / SK) & 1));
         if (!ok) break;
         if (lane == 0 && t == 0) TC_PROBE(c, 7);
         if (tile_used) {
           if (c >= 2) {
-            ok = lane0_ok(mbar_wait_bounded(&s_free[t][c & 1], ((c - 2) >> 1) & 1));
+            // buffer c & 1 holds P of chunk c - 2 until its P V product is done
+            ok = lane0_ok(mbar_wait_bounded(&p_done[t][c & 1], ((c - 2) >> 1) & 1));
             if (!ok) break;
           }
-          if (lane == 0) {
-            if (t == 0) TC_PROBE(c, 4);
-            tc_fence_after();
-            const uint64_t kb = k_desc + (uint64_t)((st * C::kKBytes) >> 4);
-            const uint32_t dst = tmem + t * kTmemCols + kTmemS + (c & 1) * kTcKeys;
+          if (lane == 0 && t == 0) TC_PROBE(c, 4);
+          tc_fence_after();
+          const uint64_t kb = k_desc + (uint64_t)((st * C::kKBytes) >> 4);
+          const uint32_t dst = tmem + t * kTmemCols + kTmemS + (c & 1) * kTcKeys;
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t koff = (kk & 3) * 32;
-              tc_mma(dst, qa + (uint64_t)(((kk >> 2) * (kTcRows * 128) + koff) >> 4),
-                     kb + (uint64_t)(((kk >> 2) * (kTcKeys * 128) + koff) >> 4), id_s, kk > 0);
-            }
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t koff = (kk & 3) * 32;
+            tc_mma_warp(dst, qa + (uint64_t)(((kk >> 2) * (kTcRows * 128) + koff) >> 4),
+                        kb + (uint64_t)(((kk >> 2) * (kTcKeys * 128) + koff) >> 4), id_s, kk > 0,
+                        lane == 0);
+          }
+          if (lane == 0) {
             tc_commit(&s_full[t][c & 1]);
             TC_PROBE(c, 8 + t);
           }
         }
         if (lane == 0) tc_commit(&k_free[st]);   // this tile's S of the K stage are done
       }
-      if (c >= 1) {
+      if (!issues_s && c >= 1) {
         // P V of the previous chunk, once its V landed and its weights are written
         const int pc = c - 1, pst = pc % SV, pb = pc & 1;
         if (lane == 0 && t == 0) TC_PROBE(pc, 10);
@@ -556,7 +581,7 @@ __global__ void __launch_bounds__(TcCfg<T, D>::kThreads)
         if (lane == 0 && t == 0) TC_PROBE(pc, 11);
         // zero the V rows past the last key (a partial or missing block):
         // they are multiplied by zero weights, and 0 x NaN would not vanish.
-        // The first MMA warp writes the zeros and signals v_zeroed; the other
+        // Tile 0's P V warp writes the zeros and signals v_zeroed; tile 1's
         // waits for it before its products read the stage.
         const int tail = tail_rows[pst];
         if (tail < kTcKeys) {
@@ -579,15 +604,17 @@ __global__ void __launch_bounds__(TcCfg<T, D>::kThreads)
         if (tile_used) {
           ok = lane0_ok(mbar_wait_bounded(&p_full[t][pb], (pc >> 1) & 1));
           if (!ok) break;
-          if (lane == 0) {
-            if (t == 0) TC_PROBE(pc, 5);
-            tc_fence_after();
-            const uint64_t pa = p_desc + (uint64_t)((pb * C::kPBytes) >> 4);
-            const uint64_t vb = v_desc + (uint64_t)((pst * C::kVBytes) >> 4);
+          if (lane == 0 && t == 0) TC_PROBE(pc, 5);
+          tc_fence_after();
+          // P of chunk pc: 16-bit pairs in the first 32 columns of S buffer pb
+          const uint32_t pa = tmem + t * kTmemCols + kTmemS + pb * kTcKeys;
+          const uint64_t vb = v_desc + (uint64_t)((pst * C::kVBytes) >> 4);
 #pragma unroll
-            for (int kk = 0; kk < kTcKeys / 16; ++kk)
-              tc_mma(tmem + t * kTmemCols + kTmemO, pa + (uint64_t)((kk * 32) >> 4),
-                     vb + (uint64_t)((kk * 2048) >> 4), id_o, (pc > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < kTcKeys / 16; ++kk)
+            tc_mma_ts_warp(tmem + t * kTmemCols + kTmemO, pa + kk * 8,
+                           vb + (uint64_t)((kk * 2048) >> 4), id_o, (pc > 0 || kk > 0) ? 1u : 0u,
+                           lane == 0);
+          if (lane == 0) {
             tc_commit(&p_done[t][pb]);
             TC_PROBE(pc, 12 + t);
           }
@@ -618,9 +645,6 @@ __global__ void __launch_bounds__(TcCfg<T, D>::kThreads)
       float s[kTcKeys];
       tmem_ld64(tbase + lane_base + kTmemS + (c & 1) * kTcKeys, s);
       if (lane == 0 && warp == 0) TC_PROBE(c, 1);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cnt(&s_free[t][c & 1]);
       const int key0 = c * kTcKeys;
       // mask (only the chunks that reach past a row's position), then the row
       // maximum as a tree of 8 independent chains.  With a positive scale the
@@ -650,13 +674,7 @@ __global__ void __launch_bounds__(TcCfg<T, D>::kThreads)
       const float corr = moved ? softmax_exp2(m_run - mx) : 1.f;   // 0 on the first chunk
       l_run *= corr;
       if (moved) m_run = mx;
-      // the product of chunk c - 2 read the P buffer this chunk writes; the
-      // product of chunk c - 1 updates O, so a rescale waits for it too
-      if (c >= 2) {
-        ok = mbar_wait_bounded(&p_done[t][c & 1], ((c - 2) >> 1) & 1);
-        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-        tc_fence_after();
-      }
+      // the product of chunk c - 1 updates O, so a rescale waits for it
       if (c > 0 && __any_sync(0xffffffffu, moved)) {
         ok = mbar_wait_bounded(&p_done[t][(c - 1) & 1], ((c - 1) >> 1) & 1);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
@@ -671,32 +689,31 @@ __global__ void __launch_bounds__(TcCfg<T, D>::kThreads)
         }
         tc_fence_before();
       }
+      // P as 16-bit pairs (key 2j in the low half of column j) over the first
+      // 32 columns of this chunk's S buffer, whose scores are all read
       float sum4[4] = {0.f, 0.f, 0.f, 0.f};
-      unsigned char* prow = smem + C::kOffP + (t * 2 + (c & 1)) * C::kPBytes;
+      float w[kTcKeys / 2];
 #pragma unroll
-      for (int ch = 0; ch < kTcKeys / 8; ++ch) {
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float p0 = softmax_exp2(fmaf(s[ch * 8 + 2 * e], qmul, -m_run));
-          const float p1 = softmax_exp2(fmaf(s[ch * 8 + 2 * e + 1], qmul, -m_run));
-          sum4[e] += p0 + p1;
-          if constexpr (std::is_same<T, __nv_bfloat16>::value) {
-            __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
-            w[e] = *reinterpret_cast<uint32_t*>(&h);
-          } else {
-            __half2 h = __floats2half2_rn(p0, p1);
-            w[e] = *reinterpret_cast<uint32_t*>(&h);
-          }
+      for (int j = 0; j < kTcKeys / 2; ++j) {
+        const float p0 = softmax_exp2(fmaf(s[2 * j], qmul, -m_run));
+        const float p1 = softmax_exp2(fmaf(s[2 * j + 1], qmul, -m_run));
+        sum4[j & 3] += p0 + p1;
+        uint32_t bits;
+        if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+          __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
+          bits = *reinterpret_cast<uint32_t*>(&h);
+        } else {
+          __half2 h = __floats2half2_rn(p0, p1);
+          bits = *reinterpret_cast<uint32_t*>(&h);
         }
-        *reinterpret_cast<uint4*>(prow + sw_chunk<kTcRows>(trow, ch)) =
-            make_uint4(w[0], w[1], w[2], w[3]);
+        w[j] = __uint_as_float(bits);
       }
+      tmem_st32(tbase + lane_base + kTmemS + (c & 1) * kTcKeys, w);   // waits for the store
       l_run += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
       if (lane == 0 && (warp == 0 || warp == 4)) TC_PROBE(c, warp == 0 ? 2 : 14);
-      // every thread orders its own P writes for the tensor cores, then one
-      // arrival per warp
-      fence_async_smem();
+      // the tensor-memory stores are ordered before the P V product, then
+      // one arrival per warp
+      tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cnt(&p_full[t][c & 1]);
     }
