@@ -10,20 +10,23 @@
 //
 // A CTA owns 256 query rows of one (sequence, KV head) as two tiles of 128
 // and runs 14 warps in fixed roles: 8 softmax warps (4 per tile), a K copy
-// warp, a V copy warp, and per tile an S-issuing and a P V-issuing MMA warp.  Row r of a tile is (token r / G, head
-// r % G of the KV head's group) and lives in TMEM lane r, so thread r of the
-// tile's softmax warps owns row r from the scores to the output: the softmax
-// needs no shuffles.  Per chunk of 64 keys:
+// warp, a V copy warp, and per tile an S-issuing and a P V-issuing MMA warp.
+// Row r of a tile is (token r / G, head r % G of the KV head's group) and
+// lives in TMEM lane r, so thread r of the tile's softmax warps owns row r
+// from the scores to the output: the softmax needs no shuffles.  Per chunk of
+// kTcKeys keys:
 //   K, V     2-D tensor-map copies (boxes of 16 rows x 64 elements, 128-byte
 //            swizzle) straight from the paged pool through the block table,
-//            into a K ring and a V ring of three stages each
-//   S = Q K^T    D/16 MMAs per tile (M=128, N=64, K=16), fp32 in TMEM, two S
-//                buffers per tile
-//   softmax  each thread loads its 64 scores (tcgen05.ld), masks the keys
-//            after its position, updates (m, l), writes its 64 weights P as
-//            fp16/bf16 into a swizzled shared tile (two P buffers per tile)
-//   O += P V     4 MMAs per tile (M=128, N=D, K=16) accumulate in TMEM, V read
-//                as an MN-major operand from the same swizzled rows
+//            into a K ring and a V ring
+//   S = Q K^T    D/16 MMAs per tile (M=128, N=kTcKeys, K=16), fp32 in TMEM,
+//                128 / kTcKeys S buffers per tile
+//   softmax  each thread loads its scores (tcgen05.ld), masks the keys after
+//            its position, updates (m, l), and writes its weights P as
+//            fp16/bf16 pairs back over the first half of the same S buffer
+//            (tcgen05.st)
+//   O += P V     kTcKeys/16 MMAs per tile (M=128, N=D, K=16) with A (= P)
+//                read from TMEM, accumulating in TMEM; V is an MN-major
+//                operand read from the same swizzled rows as K
 // The running maximum only moves when a new score exceeds it by more than
 // 2^8 (log2 domain), and only then is the TMEM accumulator rescaled: between
 // rescales the weights use a stale maximum, which the final O / l cancels
@@ -49,9 +52,16 @@ namespace {
 
 constexpr int kTcRows = 128;    // query rows per CTA = TMEM lanes
 constexpr int kTcThreads = 128;
-constexpr int kTcKeys = 64;     // keys per chunk
+// Keys per chunk (tuning knob: 64 or 32).  A tile's S buffers fill columns
+// [0, 128) of its TMEM, so there are 128 / kTcKeys of them.
+#ifndef PHOTON_TC_KEYS
+#define PHOTON_TC_KEYS 64
+#endif
+constexpr int kTcKeys = PHOTON_TC_KEYS;
+static_assert(kTcKeys == 32 || kTcKeys == 64, "chunks of 32 or 64 keys");
+constexpr int kNumS = 128 / kTcKeys;   // S buffers per tile; chunk c uses buffer c % kNumS
 constexpr uint32_t kTmemCols = 256;
-constexpr uint32_t kTmemS = 0;     // S: two buffers, columns [0, 64) and [64, 128)
+constexpr uint32_t kTmemS = 0;     // S buffers: columns [0, 128)
 constexpr uint32_t kTmemO = 128;   // O: columns [128, 128 + D)
 constexpr float kRescaleLog2 = 8.f;
 
@@ -157,6 +167,85 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
       : "memory");
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+      "%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15]))
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Softmax arithmetic on Blackwell's paired fp32 instructions (tuning knobs):
+// PHOTON_TC_PACKED: the exponent arguments and the row sum two lanes per
+// instruction (fma/add .f32x2, each lane rounded as the scalar form);
+// PHOTON_TC_FMAX3: the row maximum with three-input max.
+#ifndef PHOTON_TC_PACKED
+#define PHOTON_TC_PACKED 1
+#endif
+#ifndef PHOTON_TC_FMAX3
+#define PHOTON_TC_FMAX3 1
+#endif
+// (d0, d1) = (a0 * b + c, a1 * b + c), one rounding per lane
+__device__ __forceinline__ void fma_f32x2(float& d0, float& d1, float a0, float a1, float b,
+                                          float c) {
+  asm("{\n.reg .b64 ra, rb, rc, rd;\nmov.b64 ra, {%2, %3};\nmov.b64 rb, {%4, %4};\n"
+      "mov.b64 rc, {%5, %5};\nfma.rn.f32x2 rd, ra, rb, rc;\nmov.b64 {%0, %1}, rd;\n}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b), "f"(c));
+}
+// (d0, d1) += (a0, a1)
+__device__ __forceinline__ void add_f32x2(float& d0, float& d1, float a0, float a1) {
+  asm("{\n.reg .b64 ra, rb, rd;\nmov.b64 ra, {%2, %3};\nmov.b64 rb, {%4, %5};\n"
+      "add.rn.f32x2 rd, ra, rb;\nmov.b64 {%0, %1}, rd;\n}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(d0), "f"(d1), "f"(a0), "f"(a1));
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// The weights of one row's chunk against the maximum m (log2 domain):
+// p_j = 2^(s_j * qmul - m), packed as 16-bit pairs into w (key 2j in the low
+// half of w[j]); returns their fp32 sum.
+template <typename T>
+__device__ __forceinline__ float tc_weights(const float (&s)[kTcKeys], float qmul, float m,
+                                            float (&w)[kTcKeys / 2]) {
+  float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int j = 0; j < kTcKeys / 2; ++j) {
+    float x0, x1;
+#if PHOTON_TC_PACKED
+    fma_f32x2(x0, x1, s[2 * j], s[2 * j + 1], qmul, -m);
+#else
+    x0 = fmaf(s[2 * j], qmul, -m);
+    x1 = fmaf(s[2 * j + 1], qmul, -m);
+#endif
+    const float p0 = softmax_exp2(x0), p1 = softmax_exp2(x1);
+#if PHOTON_TC_PACKED
+    add_f32x2(sum4[(j & 1) * 2], sum4[(j & 1) * 2 + 1], p0, p1);
+#else
+    sum4[j & 3] += p0 + p1;
+#endif
+    uint32_t bits;
+    if constexpr (std::is_same<T, __nv_bfloat16>::value) {
+      __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
+      bits = *reinterpret_cast<uint32_t*>(&h);
+    } else {
+      __half2 h = __floats2half2_rn(p0, p1);
+      bits = *reinterpret_cast<uint32_t*>(&h);
+    }
+    w[j] = __uint_as_float(bits);
+  }
+  return (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
+}
 
 __device__ __forceinline__ void cp_async16_zfill(uint32_t dst, const void* src, bool valid) {
   const int n = valid ? 16 : 0;
@@ -176,16 +265,15 @@ __device__ __forceinline__ uint32_t sw_chunk(int r, int c) {
 }
 
 // Shared-memory plan of the warp-specialised kernel: two Q tiles of 128 rows,
-// a ring of kStages K/V chunks (filled by the tensor memory accelerator), two
-// P buffers per Q tile (chunk c uses buffer c % 2, so the softmax of chunk c
-// writes its weights while the product of chunk c - 1 still reads the other).
-// Ring depths (tuning knobs).  Measured on the 16 x 1024 prefill: 3 + 3
-// stages 0.392 ms, 4 K + 2 V 0.394 ms, 5 K + 1 V 0.595 ms.
+// then a K ring and a V ring of chunks (filled by the tensor memory
+// accelerator).  Ring depths are tuning knobs; measured on the 16 x 1024
+// prefill while P still went through shared memory: 3 + 3 stages 0.392 ms,
+// 4 K + 2 V 0.394 ms, 5 K + 1 V 0.595 ms.
 #ifndef PHOTON_TC_KSTAGES
-#define PHOTON_TC_KSTAGES 3
+#define PHOTON_TC_KSTAGES (PHOTON_TC_KEYS == 64 ? 3 : 6)
 #endif
 #ifndef PHOTON_TC_VSTAGES
-#define PHOTON_TC_VSTAGES 3
+#define PHOTON_TC_VSTAGES (PHOTON_TC_KEYS == 64 ? 3 : 6)
 #endif
 template <typename T, int D>
 struct TcCfg {
@@ -333,7 +421,7 @@ __device__ __forceinline__ void tc_item_of(const MultiQueryArgs& a, int G, int& 
 // per-chunk timeline of one CTA (the last tile of KV head 0 of the last
 // sequence) and the start and end of every CTA.
 constexpr int kTcProbeChunks = 160;
-static __device__ unsigned long long g_tc_probe[kTcProbeChunks][16];
+static __device__ unsigned long long g_tc_probe[kTcProbeChunks][20];
 static __device__ unsigned long long g_tc_cta[4096][2];
 #define TC_PROBE(c, i)                                                                \
   do {                                                                               \
@@ -355,20 +443,22 @@ static __device__ unsigned long long g_tc_cta[4096][2];
 // the S products of tiles 0 and 1, warps 12 and 13 their P V products (lane
 // 0 of each), so four instruction streams feed the tensor cores (one thread
 // issuing every MMA took about twice the tensor cores' execution time per
-// chunk); warp 12's lanes also zero the V rows that lie past the last key.  Both tiles use every K/V chunk, so each chunk is
-// fetched once for 256 rows.  TMEM: tile t owns columns [256 t, 256 t + 256):
-// two S buffers of 64, then O.
+// chunk); warp 12's lanes also zero the V rows that lie past the last key.
+// Both tiles use every K/V chunk, so each chunk is fetched once for 256 rows.
+// TMEM: tile t owns columns [256 t, 256 t + 256): the S buffers in [0, 128),
+// then O.  P of a chunk overwrites the first half of its own S buffer, so S
+// of chunk c + kNumS, which reuses the buffer, waits for the P V product of
+// chunk c.
 // Barriers (each completes once per use; a use's parity is its index & 1):
 //   k_full[s], v_full[s]  K (V) of a chunk landed in stage s (copy transaction bytes)
 //   k_free[s]      the S products reading K stage s finished (one commit per MMA warp)
 //   v_free[s]      the P V products reading V stage s finished (one commit per MMA warp)
 //   v_zeroed[s]    warp 12 zeroed the V rows of stage s past the last key
 //   s_full[t][b]   S of a chunk is in tile t's TMEM buffer b (MMA commit)
-//   s_free[t][b]   tile t's 4 softmax warps have read that buffer (4 arrivals)
-//   p_full[t][b]   tile t's P of a chunk is in its shared buffer b (4 warp arrivals)
-//   p_done[t][b]   the P V product reading that buffer finished (MMA commit)
-// The b-indexed barriers serve chunks b, b + 2, ...: chunk c's use of one has
-// parity (c / 2) & 1.
+//   p_full[t][b]   tile t's P of that chunk is in buffer b (4 softmax warp arrivals)
+//   p_done[t][b]   the P V product reading buffer b finished (MMA commit)
+// The b-indexed barriers serve chunks b, b + kNumS, ...: chunk c's use of one
+// has parity (c / kNumS) & 1.
 template <typename T, int D>
 __global__ void __launch_bounds__(TcCfg<T, D>::kThreads)
     paged_multi_query_tc_kernel(const __grid_constant__ CUtensorMap tm_k,
@@ -379,9 +469,9 @@ __global__ void __launch_bounds__(TcCfg<T, D>::kThreads)
   constexpr int kSuper = NT * kTcRows;
   extern __shared__ unsigned char tc_smem_raw[];
   __shared__ __align__(8) uint64_t k_full[SK], k_free[SK], v_full[SV], v_free[SV],
-      s_full[NT][2], p_full[NT][2], p_done[NT][2], v_zeroed[SV];
+      s_full[NT][kNumS], p_full[NT][kNumS], p_done[NT][kNumS], v_zeroed[SV];
   __shared__ uint32_t tmem_slot;
-  __shared__ int tail_rows[SV];   // per V stage: first V row to zero (64 = none)
+  __shared__ int tail_rows[SV];   // per V stage: first V row to zero (kTcKeys = none)
   unsigned char* smem = reinterpret_cast<unsigned char*>(
       (reinterpret_cast<uintptr_t>(tc_smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sbase = smem_addr(smem);
@@ -441,7 +531,7 @@ __global__ void __launch_bounds__(TcCfg<T, D>::kThreads)
       mbar_init(&v_zeroed[i], 1);
     }
     for (int t = 0; t < NT; ++t) {
-      for (int i = 0; i < 2; ++i) {
+      for (int i = 0; i < kNumS; ++i) {
         mbar_init(&s_full[t][i], 1);
         mbar_init(&p_full[t][i], 4);   // one arrival per softmax warp of the tile
         mbar_init(&p_done[t][i], 1);
@@ -492,10 +582,11 @@ __global__ void __launch_bounds__(TcCfg<T, D>::kThreads)
       if (lane != 0) continue;
       uint32_t bytes = 0;
       int tail = kTcKeys;
-      int phys[4];
+      constexpr int kBlocks = kTcKeys / kBlockSize;   // pool blocks per chunk
+      int phys[kBlocks];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const int kb = c * 4 + i;   // 16-key block of the sequence
+      for (int i = 0; i < kBlocks; ++i) {
+        const int kb = c * kBlocks + i;   // 16-key block of the sequence
         phys[i] = -1;
         if (kb * kBlockSize < kend) {
           const int p = __ldg(table + kb);
@@ -514,7 +605,7 @@ __global__ void __launch_bounds__(TcCfg<T, D>::kThreads)
       if (!is_v) TC_PROBE(c, 6);
       mbar_arrive_expect_tx(&full[st], bytes);
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
+      for (int i = 0; i < kBlocks; ++i) {
         if (phys[i] < 0) continue;
         const int y = (phys[i] * a.Hkv + kvh) * kBlockSize;
 #pragma unroll
@@ -549,15 +640,15 @@ __global__ void __launch_bounds__(TcCfg<T, D>::kThreads)
         if (!ok) break;
         if (lane == 0 && t == 0) TC_PROBE(c, 7);
         if (tile_used) {
-          if (c >= 2) {
-            // buffer c & 1 holds P of chunk c - 2 until its P V product is done
-            ok = lane0_ok(mbar_wait_bounded(&p_done[t][c & 1], ((c - 2) >> 1) & 1));
+          if (c >= kNumS) {
+            // buffer c % kNumS holds P of chunk c - kNumS until its P V product is done
+            ok = lane0_ok(mbar_wait_bounded(&p_done[t][c % kNumS], ((c - kNumS) / kNumS) & 1));
             if (!ok) break;
           }
           if (lane == 0 && t == 0) TC_PROBE(c, 4);
           tc_fence_after();
           const uint64_t kb = k_desc + (uint64_t)((st * C::kKBytes) >> 4);
-          const uint32_t dst = tmem + t * kTmemCols + kTmemS + (c & 1) * kTcKeys;
+          const uint32_t dst = tmem + t * kTmemCols + kTmemS + (c % kNumS) * kTcKeys;
 #pragma unroll
           for (int kk = 0; kk < D / 16; ++kk) {
             const uint32_t koff = (kk & 3) * 32;
@@ -566,7 +657,7 @@ __global__ void __launch_bounds__(TcCfg<T, D>::kThreads)
                         lane == 0);
           }
           if (lane == 0) {
-            tc_commit(&s_full[t][c & 1]);
+            tc_commit(&s_full[t][c % kNumS]);
             TC_PROBE(c, 8 + t);
           }
         }
@@ -574,7 +665,7 @@ __global__ void __launch_bounds__(TcCfg<T, D>::kThreads)
       }
       if (!issues_s && c >= 1) {
         // P V of the previous chunk, once its V landed and its weights are written
-        const int pc = c - 1, pst = pc % SV, pb = pc & 1;
+        const int pc = c - 1, pst = pc % SV, pb = pc % kNumS;
         if (lane == 0 && t == 0) TC_PROBE(pc, 10);
         ok = lane0_ok(mbar_wait_bounded(&v_full[pst], (pc / SV) & 1));
         if (!ok) break;
@@ -602,7 +693,7 @@ __global__ void __launch_bounds__(TcCfg<T, D>::kThreads)
         }
         __syncwarp();
         if (tile_used) {
-          ok = lane0_ok(mbar_wait_bounded(&p_full[t][pb], (pc >> 1) & 1));
+          ok = lane0_ok(mbar_wait_bounded(&p_full[t][pb], (pc / kNumS) & 1));
           if (!ok) break;
           if (lane == 0 && t == 0) TC_PROBE(pc, 5);
           tc_fence_after();
@@ -638,19 +729,21 @@ __global__ void __launch_bounds__(TcCfg<T, D>::kThreads)
     const float qscale = a.qscale;
     const float qmul = qscale > 0.f ? qscale : 1.f;   // multiplier left for the exponent
     for (int c = 0; c < nchunks && tile_used; ++c) {
-      ok = mbar_wait_bounded(&s_full[t][c & 1], (c >> 1) & 1);
+      ok = mbar_wait_bounded(&s_full[t][c % kNumS], (c / kNumS) & 1);
       if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
       if (lane == 0 && (warp == 0 || warp == 4)) TC_PROBE(c, warp == 0 ? 0 : 3);
       tc_fence_after();
-      float s[kTcKeys];
-      tmem_ld64(tbase + lane_base + kTmemS + (c & 1) * kTcKeys, s);
-      if (lane == 0 && warp == 0) TC_PROBE(c, 1);
+      // the chunk's scores (tcgen05.ld), masked where they reach past the
+      // row's position.  With a positive scale the maximum is taken on the
+      // raw scores and the scale is folded into the exponent's fused
+      // multiply-add; otherwise the scores are scaled here and the
+      // multiplier is 1.
       const int key0 = c * kTcKeys;
-      // mask (only the chunks that reach past a row's position), then the row
-      // maximum as a tree of 8 independent chains.  With a positive scale the
-      // maximum is taken on the raw scores and the scale is folded into the
-      // exponent's fused multiply-add below; otherwise the scores are scaled
-      // first and the multiplier becomes 1.
+      float s[kTcKeys];
+      if constexpr (kTcKeys == 64)
+        tmem_ld64(tbase + lane_base + kTmemS + (c % kNumS) * kTcKeys, s);
+      else
+        tmem_ld32(tbase + lane_base + kTmemS + (c % kNumS) * kTcKeys, s);
       if (key0 + kTcKeys - 1 > pos_min) {
 #pragma unroll
         for (int j = 0; j < kTcKeys; ++j)
@@ -660,23 +753,37 @@ __global__ void __launch_bounds__(TcCfg<T, D>::kThreads)
 #pragma unroll
         for (int j = 0; j < kTcKeys; ++j) s[j] *= qscale;
       }
+      if (lane == 0 && warp == 0) TC_PROBE(c, 1);
+      // the row maximum as 8 independent chains; the running maximum only
+      // moves when a score passes it by more than 2^8, and then what is
+      // accumulated so far is rescaled (warp-wide TMEM access: a warp
+      // rescales if any of its rows must, the others by 1)
       float m8[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) m8[k] = s[k];
+#if PHOTON_TC_FMAX3
+#pragma unroll
+      for (int j = 8; j + 16 <= kTcKeys; j += 16)
+#pragma unroll
+        for (int k = 0; k < 8; ++k) m8[k] = fmax3(m8[k], s[j + k], s[j + 8 + k]);
+      if ((kTcKeys - 8) % 16) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) m8[k] = fmaxf(m8[k], s[kTcKeys - 8 + k]);
+      }
+#else
 #pragma unroll
       for (int j = 8; j < kTcKeys; ++j) m8[j & 7] = fmaxf(m8[j & 7], s[j]);
+#endif
       const float mx = qmul * fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])),
                                     fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
-      // the maximum moves only when a score passes it by more than 2^8; then
-      // what is accumulated so far is rescaled (warp-wide TMEM access: a warp
-      // rescales if any of its rows must, the others by 1)
       const bool moved = mx > m_run + kRescaleLog2;
       const float corr = moved ? softmax_exp2(m_run - mx) : 1.f;   // 0 on the first chunk
       l_run *= corr;
       if (moved) m_run = mx;
+      if (lane == 0 && warp == 0) TC_PROBE(c, 15);
       // the product of chunk c - 1 updates O, so a rescale waits for it
       if (c > 0 && __any_sync(0xffffffffu, moved)) {
-        ok = mbar_wait_bounded(&p_done[t][(c - 1) & 1], ((c - 1) >> 1) & 1);
+        ok = mbar_wait_bounded(&p_done[t][(c - 1) % kNumS], ((c - 1) / kNumS) & 1);
         if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll 1
@@ -689,38 +796,27 @@ __global__ void __launch_bounds__(TcCfg<T, D>::kThreads)
         }
         tc_fence_before();
       }
-      // P as 16-bit pairs (key 2j in the low half of column j) over the first
-      // 32 columns of this chunk's S buffer, whose scores are all read
-      float sum4[4] = {0.f, 0.f, 0.f, 0.f};
+      // P as 16-bit pairs over the first kTcKeys / 2 columns of this chunk's
+      // S buffer, whose scores are all read
       float w[kTcKeys / 2];
-#pragma unroll
-      for (int j = 0; j < kTcKeys / 2; ++j) {
-        const float p0 = softmax_exp2(fmaf(s[2 * j], qmul, -m_run));
-        const float p1 = softmax_exp2(fmaf(s[2 * j + 1], qmul, -m_run));
-        sum4[j & 3] += p0 + p1;
-        uint32_t bits;
-        if constexpr (std::is_same<T, __nv_bfloat16>::value) {
-          __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
-          bits = *reinterpret_cast<uint32_t*>(&h);
-        } else {
-          __half2 h = __floats2half2_rn(p0, p1);
-          bits = *reinterpret_cast<uint32_t*>(&h);
-        }
-        w[j] = __uint_as_float(bits);
-      }
-      tmem_st32(tbase + lane_base + kTmemS + (c & 1) * kTcKeys, w);   // waits for the store
-      l_run += (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
+      const float lsum = tc_weights<T>(s, qmul, m_run, w);
+      if (lane == 0 && warp == 0) TC_PROBE(c, 16);
+      if constexpr (kTcKeys == 64)
+        tmem_st32(tbase + lane_base + kTmemS + (c % kNumS) * kTcKeys, w);   // waits for the store
+      else
+        tmem_st16(tbase + lane_base + kTmemS + (c % kNumS) * kTcKeys, w);
+      l_run += lsum;
       if (lane == 0 && (warp == 0 || warp == 4)) TC_PROBE(c, warp == 0 ? 2 : 14);
       // the tensor-memory stores are ordered before the P V product, then
       // one arrival per warp
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive_cnt(&p_full[t][c & 1]);
+      if (lane == 0) mbar_arrive_cnt(&p_full[t][c % kNumS]);
     }
     // ---- the last product, then O / l
     if (tile_used) {
       if (ok) {
-        ok = mbar_wait_bounded(&p_done[t][(nchunks - 1) & 1], ((nchunks - 1) >> 1) & 1);
+        ok = mbar_wait_bounded(&p_done[t][(nchunks - 1) % kNumS], ((nchunks - 1) / kNumS) & 1);
         ok = __all_sync(0xffffffffu, ok);
       }
       if (!ok) {
