@@ -53,8 +53,6 @@
 #include <math.h>
 #include <string.h>
 
-#include <cuda_fp8.h>
-
 #include <type_traits>
 
 #include "photon_common.cuh"
@@ -129,7 +127,7 @@ constexpr int kMaxRuns = 12;
 // layout of code_chunk, and the tensor-core math widens the codes to fp16 in
 // registers as it loads its fragments.
 #ifndef PHOTON_FP8_BPW
-#define PHOTON_FP8_BPW 1
+#define PHOTON_FP8_BPW 2
 #endif
 template <typename T, int D, int G, int NC, int S, bool R = false, bool M = false, bool X = false,
           bool F = false>
@@ -144,11 +142,12 @@ struct PersistCfg {
   // with RoPE the item's (cos, sin) row, D/2 float pairs, follows its q rows
   static constexpr int kCsBytes = R ? 4 * D : 0;
   static constexpr int kQStride = (kQBytes + kCsBytes + 127) / 128 * 128;
-  // blocks per warp and stage (PHOTON_FP8_BPW, e4m3 cache only; 1 by
-  // default): with two, each consumer warp takes two consecutive blocks of a
-  // stage, spreading the stage protocol over twice the bytes, but the larger
-  // stages leave room for two CTAs per SM instead of three, and the qwen_b64
-  // fp8 decode measured 70.5 against 67.2 us
+  // blocks per warp and stage (PHOTON_FP8_BPW, e4m3 cache only; 2 by
+  // default): each consumer warp takes two consecutive blocks of a stage,
+  // which spreads the stage protocol over twice the bytes and gives the warp
+  // two blocks of independent work; the larger stages leave room for two
+  // CTAs per SM instead of three.  qwen_b64 fp8 decode: 56.9 us with two,
+  // 60.0 us with one block per warp (three CTAs per SM)
   static constexpr int kBPW = F ? PHOTON_FP8_BPW : 1;
   static constexpr int kStageBlocks = NC * kBPW;
   static constexpr int kStageBytes = 2 * kStageBlocks * kBlockBytes;  // K blocks, then V blocks
@@ -309,7 +308,7 @@ __device__ __forceinline__ uint32_t code_chunk(int row, int chunk) {
   if constexpr (D == 128) return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
   else return (uint32_t)(row * 64 + ((chunk ^ ((row >> 1) & 3)) << 4));
 }
-__device__ __forceinline__ uint32_t widen_e4m3x2(uint32_t pair);
+__device__ __forceinline__ void widen_e4m3x4(uint32_t codes, uint32_t& lo, uint32_t& hi);
 template <typename T, int D, bool kQLo, bool kCausal, bool kCodes = false>
 __device__ __forceinline__ void attend_block_mma(uint32_t kblk, uint32_t vblk, int n_valid,
                                                  float qscale, const uint32_t (&bq)[D / 16][2],
@@ -330,15 +329,11 @@ __device__ __forceinline__ void attend_block_mma(uint32_t kblk, uint32_t vblk, i
       uint32_t c0, c1, c2, c3;
       ldsm_x4(kblk + code_chunk<D>(krow, 2 * j + khi), c0, c1, c2, c3);
       uint32_t a[4];
-      a[0] = widen_e4m3x2(c0 & 0xFFFFu);
-      a[2] = widen_e4m3x2(c0 >> 16);
-      a[1] = widen_e4m3x2(c1 & 0xFFFFu);
-      a[3] = widen_e4m3x2(c1 >> 16);
+      widen_e4m3x4(c0, a[0], a[2]);
+      widen_e4m3x4(c1, a[1], a[3]);
       Mma<T>::run(s, a, bq[2 * j][0], bq[2 * j][1]);
-      a[0] = widen_e4m3x2(c2 & 0xFFFFu);
-      a[2] = widen_e4m3x2(c2 >> 16);
-      a[1] = widen_e4m3x2(c3 & 0xFFFFu);
-      a[3] = widen_e4m3x2(c3 >> 16);
+      widen_e4m3x4(c2, a[0], a[2]);
+      widen_e4m3x4(c3, a[1], a[3]);
       Mma<T>::run(s2, a, bq[2 * j + 1][0], bq[2 * j + 1][1]);
     }
 #pragma unroll
@@ -421,10 +416,8 @@ __device__ __forceinline__ void attend_block_mma(uint32_t kblk, uint32_t vblk, i
         const uint32_t w0 = __byte_perm(c[2 * h], 0u, 0x3120);
         const uint32_t w1 = __byte_perm(c[2 * h + 1], 0u, 0x3120);
         uint32_t a[4];
-        a[0] = widen_e4m3x2(w0 & 0xFFFFu);
-        a[1] = widen_e4m3x2(w0 >> 16);
-        a[2] = widen_e4m3x2(w1 & 0xFFFFu);
-        a[3] = widen_e4m3x2(w1 >> 16);
+        widen_e4m3x4(w0, a[0], a[1]);
+        widen_e4m3x4(w1, a[2], a[3]);
         Mma<T>::run(o[2 * j + h], a, b0, b1);
         Mma<T>::run(o[2 * j + h], a, e0, e1);
       }
@@ -443,11 +436,15 @@ __device__ __forceinline__ void attend_block_mma(uint32_t kblk, uint32_t vblk, i
   }
 }
 
-// Two e4m3 codes (the low byte first) widened exactly to an fp16 pair (the
-// low byte's value in the low half).  Every e4m3 value is an fp16 value.
-__device__ __forceinline__ uint32_t widen_e4m3x2(uint32_t pair) {
-  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)pair, __NV_E4M3);
-  return (uint32_t)h.x | ((uint32_t)h.y << 16);
+// Four e4m3 codes (bytes 0..3 of `codes`) widened exactly to two fp16
+// pairs: bytes 0, 1 into lo, bytes 2, 3 into hi (the lower byte's value in
+// the low half).  Every e4m3 value is an fp16 value.  The 16-bit halves are
+// handed to the conversions as register halves, so no shift separates them.
+__device__ __forceinline__ void widen_e4m3x4(uint32_t codes, uint32_t& lo, uint32_t& hi) {
+  asm("{\n.reg .b16 l, h;\nmov.b32 {l, h}, %2;\ncvt.rn.f16x2.e4m3x2 %0, l;\n"
+      "cvt.rn.f16x2.e4m3x2 %1, h;\n}"
+      : "=r"(lo), "=r"(hi)
+      : "r"(codes));
 }
 
 // ------------------------------------------------------------------ RoPE
@@ -578,8 +575,8 @@ static __global__ void probe_stamp_big_kernel() {
 // kFp8: the e4m3 cache (photon_paged_decode_fp8): K/V blocks arrive as
 // swizzled tensor-map boxes of codes, and the block math widens the codes it
 // needs in registers; the K scale is folded into qscale, the V scale into
-// the item's combine.  Three CTAs share an SM (PHOTON_FP8_CTAS, a tuning
-// knob for the register cap).
+// the item's combine.  Two CTAs share an SM with two blocks per warp, three
+// with one (PHOTON_FP8_CTAS, a tuning knob for the register cap).
 #ifndef PHOTON_FP8_CTAS
 #define PHOTON_FP8_CTAS (PHOTON_FP8_BPW > 1 ? 2 : 3)
 #endif
@@ -1746,8 +1743,10 @@ cudaError_t launch_decode_impl(const DecodeArgs& a0, cudaStream_t stream) {
   return cudaSuccess;
 }
 
-// The e4m3 cache: stages of 4 code blocks per K and V (8 KB at d = 64, 16 KB at
-// d = 128) in a 64 KB ring, so that three CTAs share an SM.
+// The e4m3 cache: stages of 4 code blocks per warp-block slot, i.e. 8 blocks
+// per K and V with two blocks per warp (32 KB a stage at d = 128), in a 96 KB
+// ring, so that two CTAs share an SM (64 KB and three CTAs with one block per
+// warp).
 #ifndef PHOTON_RING_KB_FP8
 #define PHOTON_RING_KB_FP8 (PHOTON_FP8_BPW > 1 ? 96 : 64)
 #endif
