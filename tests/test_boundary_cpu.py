@@ -122,6 +122,35 @@ def test_gather_validation(lib):
     assert f(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.byref(_shape(num_seqs=0)), None) == 0
 
 
+def test_default_partition_sizes(lib):
+    """The default partition: 192 KB of K+V per (partition, KV head) item,
+    and for a batch whose worst case (num_seqs x max_blocks_per_seq x 16 x
+    Hkv tokens) would give fewer than about two items per resident CTA (608
+    items), that worst case / 608 rounded to the nearest whole stage of 64
+    tokens (one 16-token block per consumer warp), at least 64 tokens."""
+    def part(**over):
+        return P.photon_paged_decode_plan(_shape(**over))["partition_size"]
+    d64 = dict(num_q_heads=32, num_kv_heads=8, head_dim=64, num_blocks=40000)
+    # the item cap: 192 KB / (2 x d x 2 bytes)
+    assert part(num_seqs=64, max_blocks_per_seq=512) == 384
+    assert part(num_seqs=256, max_blocks_per_seq=1024, **d64) == 768
+    # small batches of the d = 64 sweep shape (contexts up to 2048 tokens):
+    # 4 x 128 x 16 x 8 / 608 = 107.8 -> 128; 8 x ... = 215.6 -> 192;
+    # 16 x ... = 431.2 -> 448; 32 x ... = 862.3 -> the cap, 768
+    assert part(num_seqs=4, max_blocks_per_seq=128, **d64) == 128
+    assert part(num_seqs=8, max_blocks_per_seq=128, **d64) == 192
+    assert part(num_seqs=16, max_blocks_per_seq=128, **d64) == 448
+    assert part(num_seqs=32, max_blocks_per_seq=128, **d64) == 768
+    # 16 x 71 x 16 x 8 / 608 = 239.2 -> 256 (round to nearest, not down)
+    assert part(num_seqs=16, max_blocks_per_seq=71, **d64) == 256
+    # tiny: 64 at the least
+    assert part(num_seqs=2, max_blocks_per_seq=4, num_q_heads=4, num_kv_heads=1,
+                head_dim=64) == 64
+    # every shrunk partition is whole stages
+    for b in (1, 2, 3, 5, 6, 7, 9, 12, 20, 24):
+        assert part(num_seqs=b, max_blocks_per_seq=128, **d64) % 64 == 0
+
+
 def test_workspace_size_and_plan(lib):
     s = _shape(num_seqs=64, max_blocks_per_seq=512, partition_size=256)
     pl = P.photon_paged_decode_plan(s)
